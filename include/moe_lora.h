@@ -1,0 +1,251 @@
+/*
+ * moe_lora.h -- C ABI of libmoelora, a GB300 (sm_103a) library for the
+ * routed BF16 Mixture-of-Experts layer forward with per-token multi-adapter
+ * LoRA.
+ *
+ * The forward follows the single-stream pipeline described in
+ * "[WIP][LoRA] BF16 support for the experimental_sgl_trtllm MoE-LoRA path &
+ * lora expert_outer_shared" (yushengsu-thu/sglang#4), "Files changed" table
+ * (launcher row) and Flow 1(A):
+ *   routing -> permute (bf16 gather) -> gate_up GEMM (K = hidden, N = 2*inter)
+ *   -> LoRA-aware SwiGLU (gate_up LoRA delta added before the activation)
+ *   -> down GEMM (K = inter, N = hidden) + down LoRA delta -> finalize
+ * and the interface of ``trtllm_bf16_routed_moe_lora`` in the prhub digest
+ * of sgl-project/sglang#28953 (core.py excerpt).
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers unless stated otherwise.  The
+ *     caller owns every buffer; the library never allocates, frees,
+ *     synchronises the stream (except moe_read_device_status) or calls back.
+ *   - Tensors are dense row-major.  bf16 tensors are passed as void* (the
+ *     bits of __nv_bfloat16).  Rows of bf16 tensors must start on 16-byte
+ *     boundaries: base pointers 16-byte aligned and H, I multiples of 8.
+ *   - Arguments are checked on the host before anything is launched; a
+ *     failed check returns a negative moe_status_t and launches nothing.
+ *   - Work is enqueued on ``stream`` (a cudaStream_t) in stream order, with
+ *     no allocation and no host synchronisation, so a call can be captured
+ *     into a CUDA graph.  The device-side status word (see
+ *     moe_read_device_status) reports problems found on the device.
+ *   - Calls on one stream that share a workspace are ordered by the stream;
+ *     calls that overlap on the GPU must not share a workspace.
+ */
+#ifndef MOE_LORA_H_
+#define MOE_LORA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                          /* cudaStream_t == struct CUstream_st* */
+typedef struct CUstream_st* moe_stream_t;
+struct CUevent_st;                           /* cudaEvent_t  == struct CUevent_st*  */
+
+#define MOE_LORA_ABI_VERSION 1
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_NULL = -1,            /* a required pointer is NULL                         */
+  MOE_ERR_SHAPE = -2,           /* a size is out of range (T < 0, top_k > E, ...)     */
+  MOE_ERR_ALIGN = -3,           /* a pointer, size or stride breaks the 16-byte rule  */
+  MOE_ERR_UNSUPPORTED = -4,     /* outside the supported limits listed below          */
+  MOE_ERR_WORKSPACE = -5,       /* workspace NULL, misaligned or too small            */
+  MOE_ERR_CUDA = -6,            /* a CUDA runtime/driver call failed                   */
+  MOE_ERR_DEVICE_TIMEOUT = -7,  /* device: a pipeline wait hit its time limit         */
+  MOE_ERR_BAD_MAPPING = -8,     /* device: token_lora_mapping outside [-1, A)         */
+  MOE_ERR_BAD_EXPERT_ID = -9    /* device: a topk id outside [-1, E)                  */
+} moe_status_t;
+
+/* Supported limits (larger values return MOE_ERR_UNSUPPORTED). */
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_TOP_K 32
+#define MOE_MAX_RANK 128
+#define MOE_MAX_ADAPTERS 64
+
+/* Human-readable name of a status code.  Never returns NULL. */
+const char* moe_status_string(int status);
+
+/* ABI version of the loaded library (MOE_LORA_ABI_VERSION at build time). */
+int moe_lora_abi_version(void);
+
+/* ---------------------------------------------------------------------------
+ * moe_route_topk -- step 1, routing.
+ *
+ * The pages take the router's top-k ids and weights in sglang's standard
+ * top-k format (prhub digest of sgl-project/sglang#28953, lora_dispatch.py
+ * and moe_overlap.py excerpts: ``topk_output.topk_ids / topk_weights``) and
+ * do not show the routing function.  It is read as: softmax over the logits,
+ * top-k, renormalise over the selected experts.  Selection compares the raw
+ * float32 logits, ties go to the lower expert id, and slots are ordered by
+ * descending logit; weights are exp(l_j - m) / sum exp(l_j' - m) over the
+ * selected slots, m the largest selected logit, in float32.
+ *
+ *   logits   [T, E] float32, device.  NaN logits give unspecified (but valid,
+ *            distinct, in-range) ids.
+ *   topk_ids [T, top_k] int32, device, written.
+ *   topk_w   [T, top_k] float32, device, written.
+ * Limits: 1 <= top_k <= min(E, 32), E <= 1024, T >= 0 (T == 0 is a no-op).
+ * ------------------------------------------------------------------------- */
+int moe_route_topk(const float* logits, int T, int E, int top_k,
+                   int32_t* topk_ids, float* topk_w, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_permute -- step 2, expert-grouped permutation and row gather.
+ *
+ * The "moe::dev::permute (bf16 gather)" stage of the launcher row in the
+ * "Files changed" table of yushengsu-thu/sglang#4; the expanded-to-permuted
+ * index is the one ``trtllm_bf16_routed_moe_lora`` returns with
+ * do_finalize=False (prhub digest of sgl-project/sglang#28953, core.py).
+ *
+ * Expanded index x = t*top_k + j.  With n_e the number of slots routed to
+ * expert e:  expert_offsets[e] = sum_{e' < e} n_e', expert_offsets[E] =
+ * number of routed slots; expanded_to_permuted[x] = expert_offsets[id[x]] +
+ * #{x' < x : id[x'] == id[x]} (stable); permuted_to_expanded is its inverse
+ * on [0, expert_offsets[E]) and -1 beyond.  If ``hidden`` and
+ * ``permuted_hidden`` are both non-NULL, permuted_hidden[p] = hidden[t(p)].
+ *
+ * An id of -1 means "not routed" (the slot gets permuted index -1).  Any
+ * other id outside [0, E) is treated like -1 and sets MOE_ERR_BAD_EXPERT_ID
+ * in the device status word, which lives at the start of ``ws``.
+ *
+ *   topk_ids [T, top_k] int32, device.
+ *   hidden   [T, H] bf16, device, or NULL (then no gather).
+ *   expert_offsets [E + 1], expanded_to_permuted [T*top_k],
+ *   permuted_to_expanded [T*top_k]: int32, device, written.
+ *   permuted_hidden [T*top_k, H] bf16, device, written, or NULL.
+ *   ws, ws_bytes: device scratch of at least moe_permute_workspace_size(),
+ *            256-byte aligned; its contents need not be initialised.
+ * ------------------------------------------------------------------------- */
+size_t moe_permute_workspace_size(int T, int top_k, int E);
+int moe_permute(const int32_t* topk_ids, int T, int top_k, int E,
+                const void* hidden, int H,
+                int32_t* expert_offsets, int32_t* expanded_to_permuted,
+                int32_t* permuted_to_expanded, void* permuted_hidden,
+                void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * LoRA factors of one projection (gate_up or down).
+ *
+ * One rank-r pair per (adapter, expert) (sglang#4 Flow 1(A):
+ * ``merged_experts_fused_moe_lora_add`` shrink then expand into the
+ * gate_up / down deltas; the shrink intermediate is [tokens, top_k,
+ * lora_a.shape[2]] per the prhub report on sgl-project/sglang#28091).
+ *   gate_up: A is [r, H], B is [2I, r];   down: A is [r, I], B is [H, r].
+ * The factor of (adapter a, expert e) starts at
+ *   A + a*a_stride_adapter + e*a_stride_expert   (elements of bf16)
+ * and its rows are contiguous.  An expert stride of 0 makes that factor
+ * shared by all experts: the "shared-outer (TML)" layout of sglang#4 Flow 2,
+ * where gate_up A is [1, r, H] and down B is [1, H, r] per adapter.
+ * Strides must be multiples of 8 elements and of r for the B factor.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  const void* A;
+  const void* B;
+  int64_t a_stride_adapter, a_stride_expert;
+  int64_t b_stride_adapter, b_stride_expert;
+} moe_lora_factors_t;
+
+/* Number of stage boundaries recorded when moe_lora_args_t.stage_events is set. */
+#define MOE_NUM_STAGE_EVENTS 8
+
+/* ---------------------------------------------------------------------------
+ * moe_lora_forward arguments.
+ *
+ *   hidden [T, H] bf16; router_logits [T, E] float32;
+ *   w13 [E, 2I, H] bf16 (rows [0, I) gate, rows [I, 2I) up);
+ *   w2 [E, H, I] bf16;
+ *   token_lora_mapping [T] int32: adapter slot per token, -1 = no adapter;
+ *     values outside [-1, num_adapters) are treated as -1 and set
+ *     MOE_ERR_BAD_MAPPING in the device status word.  May be NULL when
+ *     num_adapters == 0 or rank == 0.
+ *   gate_up, down: LoRA factors (ignored when num_adapters == 0 or rank == 0).
+ *   scaling: LoRA scale s; each delta is s * B (A x).
+ *   out [T, H] bf16, written.
+ *   topk_ids_out [T, top_k] int32, topk_w_out [T, top_k] float32,
+ *   expanded_to_permuted_out [T*top_k] int32: optional copies of the
+ *     routing, NULL to skip.
+ *   workspace, workspace_bytes: device scratch of at least
+ *     moe_lora_workspace_size(), 256-byte aligned.  It holds the device
+ *     status word and every intermediate; see moe_lora_workspace_plan.
+ *   tile_n: token-tile width of the expert GEMMs (16, 32, 64, 128 or 256;
+ *     0 = chosen from T*top_k/E).
+ *   wait_timeout_ms: limit of every device-side pipeline wait (0 = 2000 ms).
+ *     A wait that runs out sets MOE_ERR_DEVICE_TIMEOUT and the kernel exits.
+ *   stage_events: NULL, or an array of MOE_NUM_STAGE_EVENTS cudaEvent_t
+ *     that are recorded on ``stream`` before the first stage, between
+ *     stages and after the last one (unused slots are recorded at the end).
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  uint32_t struct_size;           /* sizeof(moe_lora_args_t) */
+  int T, H, I, E, top_k, num_adapters, rank;
+  float scaling;
+  const void* hidden;
+  const void* w13;
+  const void* w2;
+  const float* router_logits;
+  const int32_t* token_lora_mapping;
+  moe_lora_factors_t gate_up;
+  moe_lora_factors_t down;
+  void* out;
+  int32_t* topk_ids_out;
+  float* topk_w_out;
+  int32_t* expanded_to_permuted_out;
+  void* workspace;
+  size_t workspace_bytes;
+  int tile_n;
+  int wait_timeout_ms;
+  struct CUevent_st* const* stage_events;
+} moe_lora_args_t;
+
+/* Byte offsets of the intermediates inside the workspace (for inspection). */
+typedef struct {
+  size_t total_bytes;
+  size_t status;              /* int32[4]: status word, detail                 */
+  size_t topk_ids;            /* int32 [T*top_k]                               */
+  size_t topk_w;              /* float [T*top_k]                               */
+  size_t expert_offsets;      /* int32 [E+1]                                   */
+  size_t expanded_to_permuted;/* int32 [T*top_k]                               */
+  size_t permuted_to_expanded;/* int32 [T*top_k]                               */
+  size_t row_adapter;         /* int32 [T*top_k] adapter of each permuted row  */
+  size_t permute_scratch;     /* counting-sort scratch                         */
+  size_t permuted_hidden;     /* bf16  [T*top_k, H]                            */
+  size_t lora_u;              /* bf16  [T*top_k, A*r] s*A_gu x, one-hot slot   */
+  size_t act;                 /* bf16  [T*top_k, I]   h = silu(gate)*up        */
+  size_t lora_v;              /* bf16  [T*top_k, A*r] s*A_dn h, one-hot slot   */
+  size_t expert_out;          /* bf16  [T*top_k, H]   y = w2 h + delta         */
+} moe_lora_workspace_plan_t;
+
+/* Fills ``plan`` (host pointer).  Returns MOE_OK or MOE_ERR_SHAPE/UNSUPPORTED. */
+int moe_lora_workspace_plan(int T, int H, int I, int E, int top_k, int num_adapters,
+                            int rank, moe_lora_workspace_plan_t* plan);
+/* Bytes of workspace moe_lora_forward needs (0 on invalid sizes). */
+size_t moe_lora_workspace_size(int T, int H, int I, int E, int top_k, int num_adapters,
+                               int rank);
+
+/* ---------------------------------------------------------------------------
+ * moe_lora_forward -- the whole layer forward (steps 1-7) on one stream.
+ *
+ * out[t] = sum_j w[t,j] * ( w2[e] h + s * B_dn (A_dn h) ),
+ *   h = silu(g[:I]) * g[I:],  g = w13[e] x_t + s * B_gu (A_gu x_t),
+ * e = topk_ids[t, j], LoRA terms present only when mapping[t] >= 0 and
+ * rank > 0 (sglang#4 "Files changed" launcher and dispatch rows; Flow 1(A)
+ * and Flow 2).  Intermediates are bf16 between kernels; every GEMM
+ * accumulates in float32.
+ * Limits: H, I multiples of 8; rank a multiple of 8 and <= 128;
+ * num_adapters <= 64; E <= 1024; top_k <= 32.
+ * Returns MOE_OK once everything is enqueued; device-side problems are in
+ * the status word (moe_read_device_status).
+ * ------------------------------------------------------------------------- */
+int moe_lora_forward(const moe_lora_args_t* args, moe_stream_t stream);
+
+/* Synchronises ``stream``, then returns the device status word that the
+ * last call using ``workspace`` left (MOE_OK or a negative device code), or
+ * MOE_ERR_CUDA if the synchronisation or the copy failed. */
+int moe_read_device_status(const void* workspace, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_LORA_H_ */

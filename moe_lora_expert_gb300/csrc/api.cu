@@ -1,0 +1,437 @@
+// C ABI of libmoelora: argument checks, workspace plan, TMA descriptors and
+// the launch sequence of the routed MoE-LoRA forward.
+//
+// Stage order follows the single-stream pipeline of "[WIP][LoRA] BF16
+// support for the experimental_sgl_trtllm MoE-LoRA path & lora
+// expert_outer_shared" (yushengsu-thu/sglang#4), Flow 1(A):
+//   routing -> permute -> gate_up LoRA shrink -> gate_up GEMM (+ expand,
+//   + LoRA-aware SwiGLU) -> down LoRA shrink -> down GEMM (+ expand)
+//   -> finalize.
+// Everything is enqueued on the caller's stream; nothing is allocated and
+// the host never waits, so the sequence can be captured into a CUDA graph.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/moe_lora.h"
+#include "kernels.cuh"
+
+namespace {
+
+using moe::GemmParams;
+using moe::PermuteParams;
+using moe::ShrinkParams;
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------ TMA encoding
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor [outer, inner] with row pitch row_bytes, box
+// [box_outer, box_inner], 128-byte swizzle, zero fill out of bounds.
+bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+               uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------ workspace plan
+bool sizes_ok(int T, int H, int I, int E, int top_k, int num_adapters, int rank) {
+  return T >= 0 && H > 0 && I > 0 && E > 0 && top_k > 0 && num_adapters >= 0 && rank >= 0;
+}
+
+int limits_status(int H, int I, int E, int top_k, int num_adapters, int rank) {
+  if (E > MOE_MAX_EXPERTS || top_k > MOE_MAX_TOP_K || rank > MOE_MAX_RANK ||
+      num_adapters > MOE_MAX_ADAPTERS)
+    return MOE_ERR_UNSUPPORTED;
+  if (top_k > E) return MOE_ERR_SHAPE;
+  if (H % 8 != 0 || I % 8 != 0) return MOE_ERR_ALIGN;
+  if (rank % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+void fill_plan(int T, int H, int I, int E, int top_k, int num_adapters, int rank,
+               moe_lora_workspace_plan_t* pl) {
+  const size_t n = static_cast<size_t>(T) * top_k;
+  const size_t lora_cols = (num_adapters > 0 && rank > 0) ? static_cast<size_t>(num_adapters) * rank : 0;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align_up(bytes);
+    return at;
+  };
+  std::memset(pl, 0, sizeof(*pl));
+  pl->status = take(16);
+  pl->topk_ids = take(n * 4);
+  pl->topk_w = take(n * 4);
+  pl->expert_offsets = take((static_cast<size_t>(E) + 1) * 4);
+  pl->expanded_to_permuted = take(n * 4);
+  pl->permuted_to_expanded = take(n * 4);
+  pl->row_adapter = take(n * 4);
+  pl->permute_scratch = take(moe::permute_scratch_bytes(static_cast<int>(n), E));
+  // The permuted hidden rows are dead once the gate_up GEMM has run, so the
+  // down GEMM's output reuses them; likewise the two LoRA operands.
+  pl->permuted_hidden = take(n * static_cast<size_t>(H) * 2);
+  pl->expert_out = pl->permuted_hidden;
+  pl->lora_u = take(n * lora_cols * 2);
+  pl->lora_v = pl->lora_u;
+  pl->act = take(n * static_cast<size_t>(I) * 2);
+  pl->total_bytes = o;
+}
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+int auto_tile_n(int n_rows, int E) {
+  const int touched = std::max(1, std::min(E, n_rows));
+  const int avg = (n_rows + touched - 1) / touched;
+  int bn = 16;
+  while (bn < 256 && bn < 2 * avg) bn *= 2;
+  return bn;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_NULL: return "MOE_ERR_NULL: a required pointer is NULL";
+    case MOE_ERR_SHAPE: return "MOE_ERR_SHAPE: a size is out of range";
+    case MOE_ERR_ALIGN: return "MOE_ERR_ALIGN: pointer, size or stride breaks the 16-byte rule";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: outside the supported limits";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace NULL, misaligned or too small";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call failed";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT: a device pipeline wait timed out";
+    case MOE_ERR_BAD_MAPPING: return "MOE_ERR_BAD_MAPPING: token_lora_mapping outside [-1, A)";
+    case MOE_ERR_BAD_EXPERT_ID: return "MOE_ERR_BAD_EXPERT_ID: a topk id outside [-1, E)";
+    default: return "unknown moe status";
+  }
+}
+
+int moe_lora_abi_version(void) { return MOE_LORA_ABI_VERSION; }
+
+int moe_route_topk(const float* logits, int T, int E, int top_k, int32_t* topk_ids, float* topk_w,
+                   moe_stream_t stream) {
+  if (T < 0 || E <= 0 || top_k <= 0) return MOE_ERR_SHAPE;
+  if (E > MOE_MAX_EXPERTS || top_k > MOE_MAX_TOP_K) return MOE_ERR_UNSUPPORTED;
+  if (top_k > E) return MOE_ERR_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (logits == nullptr || topk_ids == nullptr || topk_w == nullptr) return MOE_ERR_NULL;
+  return cuda_status(moe::launch_route_topk(logits, T, E, top_k, topk_ids, topk_w, stream));
+}
+
+size_t moe_permute_workspace_size(int T, int top_k, int E) {
+  if (T < 0 || top_k <= 0 || E <= 0) return 0;
+  return align_up(16) + moe::permute_scratch_bytes(T * top_k, E);
+}
+
+int moe_permute(const int32_t* topk_ids, int T, int top_k, int E, const void* hidden, int H,
+                int32_t* expert_offsets, int32_t* expanded_to_permuted,
+                int32_t* permuted_to_expanded, void* permuted_hidden, void* ws, size_t ws_bytes,
+                moe_stream_t stream) {
+  if (T < 0 || E <= 0 || top_k <= 0) return MOE_ERR_SHAPE;
+  if (E > MOE_MAX_EXPERTS || top_k > MOE_MAX_TOP_K) return MOE_ERR_UNSUPPORTED;
+  if (expert_offsets == nullptr || ws == nullptr) return MOE_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0 ||
+      ws_bytes < moe_permute_workspace_size(T, top_k, E))
+    return MOE_ERR_WORKSPACE;
+  const bool gather = hidden != nullptr && permuted_hidden != nullptr;
+  if (gather && (H <= 0 || H % 8 != 0 || !aligned16(hidden) || !aligned16(permuted_hidden)))
+    return MOE_ERR_ALIGN;
+  int* status = static_cast<int*>(ws);
+  if (cudaMemsetAsync(status, 0, 16, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (T == 0) return cuda_status(cudaMemsetAsync(expert_offsets, 0, (E + 1) * sizeof(int32_t), stream));
+  if (topk_ids == nullptr || expanded_to_permuted == nullptr || permuted_to_expanded == nullptr)
+    return MOE_ERR_NULL;
+  const int n = T * top_k;
+  uint8_t* scratch = static_cast<uint8_t*>(ws) + align_up(16);
+  PermuteParams p{};
+  p.topk_ids = topk_ids;
+  p.n = n;
+  p.top_k = top_k;
+  p.E = E;
+  p.H = H;
+  p.hidden = gather ? static_cast<const __nv_bfloat16*>(hidden) : nullptr;
+  p.permuted = gather ? static_cast<__nv_bfloat16*>(permuted_hidden) : nullptr;
+  p.expert_offsets = expert_offsets;
+  p.e2p = expanded_to_permuted;
+  p.p2e = permuted_to_expanded;
+  p.chunk_counts = reinterpret_cast<int32_t*>(scratch);
+  p.tile_start = nullptr;
+  p.status = status;
+  return cuda_status(moe::launch_permute(p, stream));
+}
+
+int moe_lora_workspace_plan(int T, int H, int I, int E, int top_k, int num_adapters, int rank,
+                            moe_lora_workspace_plan_t* plan) {
+  if (plan == nullptr) return MOE_ERR_NULL;
+  if (!sizes_ok(T, H, I, E, top_k, num_adapters, rank)) return MOE_ERR_SHAPE;
+  const int st = limits_status(H, I, E, top_k, num_adapters, rank);
+  if (st != MOE_OK) return st;
+  fill_plan(T, H, I, E, top_k, num_adapters, rank, plan);
+  return MOE_OK;
+}
+
+size_t moe_lora_workspace_size(int T, int H, int I, int E, int top_k, int num_adapters, int rank) {
+  moe_lora_workspace_plan_t pl;
+  if (moe_lora_workspace_plan(T, H, I, E, top_k, num_adapters, rank, &pl) != MOE_OK) return 0;
+  return pl.total_bytes;
+}
+
+int moe_read_device_status(const void* workspace, moe_stream_t stream) {
+  if (workspace == nullptr) return MOE_ERR_NULL;
+  int host[4] = {0, 0, 0, 0};
+  if (cudaMemcpyAsync(host, workspace, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  return host[0];
+}
+
+int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
+  if (a == nullptr) return MOE_ERR_NULL;
+  if (a->struct_size < sizeof(moe_lora_args_t)) return MOE_ERR_UNSUPPORTED;
+  const int T = a->T, H = a->H, I = a->I, E = a->E, K = a->top_k;
+  if (!sizes_ok(T, H, I, E, K, a->num_adapters, a->rank)) return MOE_ERR_SHAPE;
+  int st = limits_status(H, I, E, K, a->num_adapters, a->rank);
+  if (st != MOE_OK) return st;
+  const bool lora = a->num_adapters > 0 && a->rank > 0;
+  const int A = lora ? a->num_adapters : 0;
+  const int r = lora ? a->rank : 0;
+  if (a->tile_n != 0 && a->tile_n != 16 && a->tile_n != 32 && a->tile_n != 64 && a->tile_n != 128 &&
+      a->tile_n != 256)
+    return MOE_ERR_UNSUPPORTED;
+  if (a->wait_timeout_ms < 0) return MOE_ERR_SHAPE;
+
+  if (a->hidden == nullptr || a->w13 == nullptr || a->w2 == nullptr ||
+      a->router_logits == nullptr || a->out == nullptr || a->workspace == nullptr)
+    return MOE_ERR_NULL;
+  if (!aligned16(a->hidden) || !aligned16(a->w13) || !aligned16(a->w2) || !aligned16(a->out))
+    return MOE_ERR_ALIGN;
+  if (lora) {
+    if (a->token_lora_mapping == nullptr || a->gate_up.A == nullptr || a->gate_up.B == nullptr ||
+        a->down.A == nullptr || a->down.B == nullptr)
+      return MOE_ERR_NULL;
+    const moe_lora_factors_t* fs[2] = {&a->gate_up, &a->down};
+    for (const moe_lora_factors_t* f : fs) {
+      if (!aligned16(f->A) || !aligned16(f->B)) return MOE_ERR_ALIGN;
+      if (f->a_stride_adapter < 0 || f->a_stride_expert < 0 || f->b_stride_adapter < 0 ||
+          f->b_stride_expert < 0)
+        return MOE_ERR_SHAPE;
+      if (f->a_stride_adapter % 8 || f->a_stride_expert % 8 || f->b_stride_adapter % 8 ||
+          f->b_stride_expert % 8)
+        return MOE_ERR_ALIGN;
+      if (f->b_stride_adapter % r || f->b_stride_expert % r) return MOE_ERR_ALIGN;
+    }
+  }
+  if ((reinterpret_cast<uintptr_t>(a->workspace) & (kAlign - 1)) != 0) return MOE_ERR_WORKSPACE;
+  moe_lora_workspace_plan_t pl;
+  fill_plan(T, H, I, E, K, A, r, &pl);
+  if (a->workspace_bytes < pl.total_bytes) return MOE_ERR_WORKSPACE;
+  const int64_t n = static_cast<int64_t>(T) * K;
+  if (n >= (int64_t(1) << 31) || static_cast<int64_t>(E) * 2 * I >= (int64_t(1) << 31) ||
+      static_cast<int64_t>(E) * H >= (int64_t(1) << 31))
+    return MOE_ERR_UNSUPPORTED;
+
+  struct CUevent_st* const* ev = a->stage_events;
+  int ev_next = 0;
+  auto mark = [&]() -> bool {
+    if (ev == nullptr || ev_next >= MOE_NUM_STAGE_EVENTS) return true;
+    return cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[ev_next++]), stream) == cudaSuccess;
+  };
+  auto finish_marks = [&]() -> bool {
+    while (ev != nullptr && ev_next < MOE_NUM_STAGE_EVENTS)
+      if (!mark()) return false;
+    return true;
+  };
+
+  uint8_t* ws = static_cast<uint8_t*>(a->workspace);
+  int* status = reinterpret_cast<int*>(ws + pl.status);
+  if (cudaMemsetAsync(status, 0, 16, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (T == 0) return finish_marks() ? MOE_OK : MOE_ERR_CUDA;
+
+  int32_t* topk_ids = a->topk_ids_out ? a->topk_ids_out : reinterpret_cast<int32_t*>(ws + pl.topk_ids);
+  float* topk_w = a->topk_w_out ? a->topk_w_out : reinterpret_cast<float*>(ws + pl.topk_w);
+  int32_t* e2p = a->expanded_to_permuted_out ? a->expanded_to_permuted_out
+                                             : reinterpret_cast<int32_t*>(ws + pl.expanded_to_permuted);
+  int32_t* offsets = reinterpret_cast<int32_t*>(ws + pl.expert_offsets);
+  int32_t* p2e = reinterpret_cast<int32_t*>(ws + pl.permuted_to_expanded);
+  int32_t* row_adapter = reinterpret_cast<int32_t*>(ws + pl.row_adapter);
+  int32_t* chunk_counts = reinterpret_cast<int32_t*>(ws + pl.permute_scratch);
+  const size_t nchunks = (static_cast<size_t>(n) + moe::kPermuteChunk - 1) / moe::kPermuteChunk;
+  int32_t* tile_start = reinterpret_cast<int32_t*>(
+      ws + pl.permute_scratch + align_up(nchunks * E * sizeof(int32_t)));
+  __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(ws + pl.permuted_hidden);
+  __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(ws + pl.expert_out);
+  __nv_bfloat16* U = reinterpret_cast<__nv_bfloat16*>(ws + pl.lora_u);
+  __nv_bfloat16* V = reinterpret_cast<__nv_bfloat16*>(ws + pl.lora_v);
+  __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(ws + pl.act);
+
+  const int bn = a->tile_n ? a->tile_n : auto_tile_n(static_cast<int>(n), E);
+  const int sms = num_sms();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  const uint64_t timeout_ns =
+      static_cast<uint64_t>(a->wait_timeout_ms ? a->wait_timeout_ms : 2000) * 1000000ull;
+
+  // TMA descriptors (host-encoded, passed by value as kernel parameters).
+  CUtensorMap tm_w13, tm_w2, tm_xp, tm_h, tm_bgu, tm_bdn, tm_u, tm_v;
+  bool enc = encode_2d(&tm_w13, a->w13, H, static_cast<uint64_t>(E) * 2 * I, H * 2ull, 64, 16) &&
+             encode_2d(&tm_w2, a->w2, I, static_cast<uint64_t>(E) * H, I * 2ull, 64, 128) &&
+             encode_2d(&tm_xp, xp, H, n, H * 2ull, 64, bn) &&
+             encode_2d(&tm_h, h, I, n, I * 2ull, 64, bn);
+  int64_t gu_rs_a = 0, gu_rs_e = 0, dn_rs_a = 0, dn_rs_e = 0;
+  if (enc && lora) {
+    gu_rs_a = a->gate_up.b_stride_adapter / r;
+    gu_rs_e = a->gate_up.b_stride_expert / r;
+    dn_rs_a = a->down.b_stride_adapter / r;
+    dn_rs_e = a->down.b_stride_expert / r;
+    const uint64_t gu_rows = (A - 1) * gu_rs_a + (E - 1) * gu_rs_e + 2ull * I;
+    const uint64_t dn_rows = (A - 1) * dn_rs_a + (E - 1) * dn_rs_e + static_cast<uint64_t>(H);
+    if (gu_rows >= (1ull << 31) || dn_rows >= (1ull << 31)) return MOE_ERR_UNSUPPORTED;
+    enc = encode_2d(&tm_bgu, a->gate_up.B, r, gu_rows, r * 2ull, 64, 16) &&
+          encode_2d(&tm_bdn, a->down.B, r, dn_rows, r * 2ull, 64, 128) &&
+          encode_2d(&tm_u, U, static_cast<uint64_t>(A) * r, n, A * r * 2ull, 64, bn) &&
+          encode_2d(&tm_v, V, static_cast<uint64_t>(A) * r, n, A * r * 2ull, 64, bn);
+  } else {
+    tm_bgu = tm_w13;
+    tm_bdn = tm_w2;
+    tm_u = tm_xp;
+    tm_v = tm_h;
+  }
+  if (!enc) return MOE_ERR_CUDA;
+
+  if (!mark()) return MOE_ERR_CUDA;
+  // 1. routing
+  if (moe::launch_route_topk(a->router_logits, T, E, K, topk_ids, topk_w, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (!mark()) return MOE_ERR_CUDA;
+  // 2. permute + gather
+  PermuteParams pp{};
+  pp.topk_ids = topk_ids;
+  pp.n = static_cast<int>(n);
+  pp.top_k = K;
+  pp.E = E;
+  pp.H = H;
+  pp.hidden = static_cast<const __nv_bfloat16*>(a->hidden);
+  pp.permuted = xp;
+  pp.mapping = lora ? a->token_lora_mapping : nullptr;
+  pp.num_adapters = A;
+  pp.row_adapter = row_adapter;
+  pp.expert_offsets = offsets;
+  pp.e2p = e2p;
+  pp.p2e = p2e;
+  pp.chunk_counts = chunk_counts;
+  pp.tile_start = tile_start;
+  pp.status = status;
+  if (moe::launch_permute(pp, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!mark()) return MOE_ERR_CUDA;
+  // 3. gate_up LoRA shrink: U = s * A_gu x (one-hot per adapter)
+  ShrinkParams sp{};
+  if (lora) {
+    sp.X = xp;
+    sp.K = H;
+    sp.A = static_cast<const __nv_bfloat16*>(a->gate_up.A);
+    sp.a_stride_adapter = a->gate_up.a_stride_adapter;
+    sp.a_stride_expert = a->gate_up.a_stride_expert;
+    sp.row_adapter = row_adapter;
+    sp.expert_offsets = offsets;
+    sp.tile_start16 = tile_start + moe::tile_width_index(16) * (E + 1);
+    sp.E = E;
+    sp.num_adapters = A;
+    sp.rank = r;
+    sp.scaling = a->scaling;
+    sp.U = U;
+    if (moe::launch_lora_shrink(sp, static_cast<int>(n), stream) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (!mark()) return MOE_ERR_CUDA;
+  // 4. gate_up GEMM + LoRA expand + SwiGLU -> h
+  GemmParams gp{};
+  gp.expert_offsets = offsets;
+  gp.tile_start = tile_start + moe::tile_width_index(bn) * (E + 1);
+  gp.row_adapter = row_adapter;
+  gp.E = E;
+  gp.K = H;
+  gp.rows_per_expert = 2 * I;
+  gp.n_feat = I;
+  gp.feat_blocks = (I + 63) / 64;
+  gp.num_adapters = A;
+  gp.rank = r;
+  gp.lb_row_stride_adapter = gu_rs_a;
+  gp.lb_row_stride_expert = gu_rs_e;
+  gp.out = h;
+  gp.status = status;
+  gp.timeout_ns = timeout_ns;
+  if (moe::launch_expert_gemm(moe::kGateUp, bn, tm_w13, tm_xp, tm_bgu, tm_u, gp, sms, stream) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (!mark()) return MOE_ERR_CUDA;
+  // 5. down LoRA shrink: V = s * A_dn h
+  if (lora) {
+    sp.X = h;
+    sp.K = I;
+    sp.A = static_cast<const __nv_bfloat16*>(a->down.A);
+    sp.a_stride_adapter = a->down.a_stride_adapter;
+    sp.a_stride_expert = a->down.a_stride_expert;
+    sp.U = V;
+    if (moe::launch_lora_shrink(sp, static_cast<int>(n), stream) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (!mark()) return MOE_ERR_CUDA;
+  // 6. down GEMM + LoRA expand -> y
+  gp.K = I;
+  gp.rows_per_expert = H;
+  gp.n_feat = H;
+  gp.feat_blocks = (H + 127) / 128;
+  gp.lb_row_stride_adapter = dn_rs_a;
+  gp.lb_row_stride_expert = dn_rs_e;
+  gp.out = y;
+  if (moe::launch_expert_gemm(moe::kDown, bn, tm_w2, tm_h, tm_bdn, tm_v, gp, sms, stream) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (!mark()) return MOE_ERR_CUDA;
+  // 7. finalize
+  if (moe::launch_finalize(y, e2p, topk_w, T, K, H, static_cast<__nv_bfloat16*>(a->out), stream) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (!finish_marks()) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // extern "C"

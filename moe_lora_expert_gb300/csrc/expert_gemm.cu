@@ -1,0 +1,425 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM),
+// operands staged by TMA.
+//
+// The gate_up GEMM (K = hidden, N = 2*inter) and the down GEMM (K = inter,
+// N = hidden) of the launcher row in the "Files changed" table of
+// "[WIP][LoRA] BF16 support for the experimental_sgl_trtllm MoE-LoRA path &
+// lora expert_outer_shared" (yushengsu-thu/sglang#4), with
+//   * the LoRA expand (s * B u, u = A x computed by the shrink kernel) run as
+//     extra K blocks of the same accumulation: for each adapter present in
+//     the token tile, B[a, e] (rows = output features, K = rank) against the
+//     one-hot operand U[:, a*r : a*r + r] whose rows are zero for tokens of
+//     other adapters;
+//   * for gate_up, the LoRA-aware SwiGLU in the epilogue: the delta is
+//     already inside the accumulator when h = silu(gate) * up is taken,
+//     which is the "adds gate_up_lora_delta pre-SwiGLU" order of the
+//     launcher row.
+//
+// Orientation ("swap AB"): the MMA's M side is 128 weight rows (output
+// features), its N side is the token tile.  D[feature, token] lives in TMEM,
+// lane = feature row, column = token.  Both operands are K-major, loaded by
+// TMA with 128-byte swizzle.
+//
+// gate_up feature block fb covers gate features [64 fb, 64 fb + 64) and the
+// matching up features.  Its 128 A rows are eight 16-row boxes interleaved
+// so that TMEM lanes [32q, 32q + 16) hold gate rows 64 fb + 16q + (0..15)
+// and lanes [32q + 16, 32q + 32) the up rows of the same features: warp q of
+// the epilogue then pairs gate and up with one shuffle.
+//
+// Roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
+// owner, warps 2..5 = epilogue (TMEM lane quadrant = warp % 4).  The kernel
+// is persistent: CTA b takes work items b, b + gridDim.x, ...; the TMEM
+// accumulator is double-buffered so the epilogue of one item overlaps the
+// MMAs of the next.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/moe_lora.h"
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+constexpr unsigned kFullMask = 0xFFFFFFFFu;
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int kABytes = 128 * 64 * 2;   // 128 rows x 64 K of bf16
+  static constexpr int kBBytes = BN * 64 * 2;    // BN rows x 64 K of bf16
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStagesRaw = (200 * 1024) / kStageBytes;
+  static constexpr int kStages = kStagesRaw > 16 ? 16 : kStagesRaw;
+  static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
+  static constexpr int kMetaBytes = 512;                         // barriers, flags
+  static constexpr int kTableBytes = 2 * (MOE_MAX_EXPERTS + 1) * 4;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kMetaBytes + kTableBytes;
+};
+
+struct Work {
+  int e, fb, row0, nrows;
+};
+
+template <int BN>
+__device__ __forceinline__ Work decode_work(int w, const int* s_off, const int* s_ts, int E,
+                                            int FB) {
+  Work wk;
+  const int tile = w / FB;
+  wk.fb = w - tile * FB;
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {  // largest e with s_ts[e] <= tile
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_ts[mid] <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  wk.e = lo;
+  wk.row0 = s_off[lo] + (tile - s_ts[lo]) * BN;
+  wk.nrows = min(BN, s_off[lo + 1] - wk.row0);
+  return wk;
+}
+
+// OR of (1 << adapter) over the tile's rows, computed by a whole warp.
+__device__ __forceinline__ uint64_t tile_adapter_mask(const int32_t* row_adapter, int row0,
+                                                      int nrows, int lane) {
+  uint64_t m = 0;
+  for (int i = lane; i < nrows; i += 32) {
+    const int a = row_adapter[row0 + i];
+    if (a >= 0) m |= 1ull << a;
+  }
+  const uint32_t lo = __reduce_or_sync(kFullMask, static_cast<uint32_t>(m));
+  const uint32_t hi = __reduce_or_sync(kFullMask, static_cast<uint32_t>(m >> 32));
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+// Bounded wait that also gives up as soon as another role raised the abort flag.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                              volatile int* abort_flag) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(a, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+__device__ __forceinline__ void raise_timeout(int* status, volatile int* abort_flag) {
+  set_status(status, MOE_ERR_DEVICE_TIMEOUT);
+  *abort_flag = 1;
+}
+
+// A-operand (weight-side) loads for one K block: 128 rows starting at the
+// feature block of ``row_base`` (a weight matrix or a LoRA B factor).
+template <int MODE>
+__device__ __forceinline__ void load_a_block(uint8_t* sA, const CUtensorMap* map, uint64_t* bar,
+                                             int kc, int64_t row_base, int fb, int n_feat,
+                                             uint64_t pol) {
+  if (MODE == kGateUp) {
+#pragma unroll
+    for (int bx = 0; bx < 8; ++bx) {
+      const int q = bx >> 1, up = bx & 1;
+      const int64_t row = row_base + static_cast<int64_t>(up) * n_feat + fb * 64 + q * 16;
+      tma_load_2d(sA + bx * 2048, map, bar, kc, static_cast<int>(row), pol);
+    }
+  } else {
+    tma_load_2d(sA, map, bar, kc, static_cast<int>(row_base + fb * 128), pol);
+  }
+}
+
+template <int BN, int MODE>
+__global__ void __launch_bounds__(192, 1)
+    expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+                       const __grid_constant__ CUtensorMap tm_lb, const __grid_constant__ CUtensorMap tm_lu,
+                       const GemmParams p) {
+  using C = GemmCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* meta = smem + C::kStages * C::kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(meta);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* accf = empty + C::kStages;
+  uint64_t* acce = accf + 2;
+  uint64_t* drain = acce + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_off = reinterpret_cast<int*>(meta + C::kMetaBytes);
+  int* s_ts = s_off + (MOE_MAX_EXPERTS + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool use_lora = p.num_adapters > 0 && p.rank > 0;
+  const int nk = (p.K + 63) / 64;
+  const int lkb = (p.rank + 63) / 64;  // K blocks per adapter of the LoRA expand
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf[b], 1);
+      mbar_init(&acce[b], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tm_w);
+    tma_prefetch_map(&tm_x);
+    if (use_lora) {
+      tma_prefetch_map(&tm_lb);
+      tma_prefetch_map(&tm_lu);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
+    s_off[i] = p.expert_offsets[i];
+    s_ts[i] = p.tile_start[i];
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_work = s_ts[p.E] * p.feat_blocks;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_x = l2_policy_evict_last();
+    uint32_t stage = 0, phase = 0;
+    uint32_t armed = 0, armed_parity = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < total_work && ok; w += gridDim.x) {
+      if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
+      const Work wk = decode_work<BN>(w, s_off, s_ts, p.E, p.feat_blocks);
+      uint64_t amask = use_lora ? tile_adapter_mask(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
+      const int nblocks = nk + __popcll(amask) * lkb;
+      int adapter = -1, j = 0;
+      for (int b = 0; b < nblocks; ++b) {
+        if (b >= nk) {  // next LoRA block: adapters in ascending order, lkb blocks each
+          if (j == 0) {
+            adapter = __ffsll(static_cast<long long>(amask)) - 1;
+            amask &= amask - 1;
+          }
+        }
+        if (lane == 0) {
+          ok = wait_or_abort(&empty[stage], phase ^ 1, p.timeout_ns, abort_flag);
+          if (ok) {
+            uint8_t* sA = smem + stage * C::kStageBytes;
+            uint8_t* sB = sA + C::kABytes;
+            mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+            if (b < nk) {
+              load_a_block<MODE>(sA, &tm_w, &full[stage], b * 64,
+                                 static_cast<int64_t>(wk.e) * p.rows_per_expert, wk.fb, p.n_feat,
+                                 pol_w);
+              tma_load_2d(sB, &tm_x, &full[stage], b * 64, wk.row0, pol_x);
+            } else {
+              const int64_t frow = static_cast<int64_t>(adapter) * p.lb_row_stride_adapter +
+                                   static_cast<int64_t>(wk.e) * p.lb_row_stride_expert;
+              load_a_block<MODE>(sA, &tm_lb, &full[stage], j * 64, frow, wk.fb, p.n_feat, pol_x);
+              tma_load_2d(sB, &tm_lu, &full[stage], adapter * p.rank + j * 64, wk.row0, pol_x);
+            }
+            armed |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          } else {
+            raise_timeout(p.status, abort_flag);
+          }
+        }
+        ok = __shfl_sync(kFullMask, ok, 0);
+        if (!ok) break;
+        if (b >= nk) j = (j + 1 == lkb) ? 0 : j + 1;
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    // Every load issued must have landed before the CTA leaves.
+    if (lane == 0) {
+      for (int s = 0; s < C::kStages; ++s)
+        if (armed & (1u << s))
+          if (!mbar_wait(&full[s], (armed_parity >> s) & 1u, p.timeout_ns))
+            set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer
+    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < total_work && ok; w += gridDim.x) {
+      if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
+      const Work wk = decode_work<BN>(w, s_off, s_ts, p.E, p.feat_blocks);
+      const uint64_t amask =
+          use_lora ? tile_adapter_mask(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
+      const int nblocks = nk + __popcll(amask) * lkb;
+      const int ncols = ((wk.nrows + 15) / 16) * 16;
+      const uint32_t idesc = make_idesc_bf16(128, ncols);
+      if (lane == 0) {
+        ok = wait_or_abort(&acce[acc], acc_phase ^ 1, p.timeout_ns, abort_flag);
+        if (!ok) raise_timeout(p.status, abort_flag);
+      }
+      ok = __shfl_sync(kFullMask, ok, 0);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      int j = 0;
+      for (int b = 0; b < nblocks; ++b) {
+        if (lane == 0) {
+          ok = wait_or_abort(&full[stage], phase, p.timeout_ns, abort_flag);
+          if (ok) {
+            tc_fence_after_sync();
+            const uint32_t a_addr = smem_u32(smem + stage * C::kStageBytes);
+            const uint64_t adesc = make_sdesc_sw128(a_addr);
+            const uint64_t bdesc = make_sdesc_sw128(a_addr + C::kABytes);
+            int ksteps = 4;
+            if (b >= nk) {
+              const int rem = p.rank - j * 64;
+              ksteps = rem >= 64 ? 4 : (rem + 15) / 16;
+            }
+            for (int ks = 0; ks < ksteps; ++ks)
+              tc_mma_bf16(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc,
+                          (b > 0 || ks > 0) ? 1u : 0u);
+            tc_commit(&empty[stage]);
+          } else {
+            raise_timeout(p.status, abort_flag);
+          }
+        }
+        ok = __shfl_sync(kFullMask, ok, 0);
+        if (!ok) break;
+        if (b >= nk) j = (j + 1 == lkb) ? 0 : j + 1;
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(&accf[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+    // Every MMA issued must be complete before TMEM is released.
+    if (lane == 0) {
+      tc_commit(drain);
+      if (!mbar_wait(drain, 0, p.timeout_ns)) set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int w = blockIdx.x; w < total_work; w += gridDim.x) {
+      if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
+      const Work wk = decode_work<BN>(w, s_off, s_ts, p.E, p.feat_blocks);
+      const int ncols = ((wk.nrows + 15) / 16) * 16;
+      bool ok = true;
+      if (lane == 0) {
+        ok = wait_or_abort(&accf[acc], acc_phase, p.timeout_ns, abort_flag);
+        if (!ok) raise_timeout(p.status, abort_flag);
+      }
+      ok = __shfl_sync(kFullMask, ok, 0);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      for (int c0 = 0; c0 < ncols; c0 += 16) {
+        float v[16];
+        tmem_ld16(t_row + c0, v);
+        if (MODE == kGateUp) {
+          // lanes < 16 hold gate rows, lanes >= 16 the up rows of the same
+          // 16 features.  Column pairs (2i, 2i+1): the low half finishes
+          // column 2i, the high half column 2i+1, after one exchange.
+          const bool hi = lane >= 16;
+          const int feat = wk.fb * 64 + q * 16 + (lane & 15);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float send = hi ? v[2 * i] : v[2 * i + 1];
+            const float recv = __shfl_xor_sync(kFullMask, send, 16);
+            const float gate = hi ? recv : v[2 * i];
+            const float up = hi ? v[2 * i + 1] : recv;
+            const int col = c0 + 2 * i + (hi ? 1 : 0);
+            if (col < wk.nrows && feat < p.n_feat) {
+              const float h = gate / (1.0f + expf(-gate)) * up;
+              p.out[static_cast<size_t>(wk.row0 + col) * p.n_feat + feat] = __float2bfloat16_rn(h);
+            }
+          }
+        } else {
+          const int feat = wk.fb * 128 + q * 32 + lane;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int col = c0 + i;
+            if (col < wk.nrows && feat < p.n_feat)
+              p.out[static_cast<size_t>(wk.row0 + col) * p.n_feat + feat] = __float2bfloat16_rn(v[i]);
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+int gemm_stage_count(int bn) {
+  switch (bn) {
+    case 16: return GemmCfg<16>::kStages;
+    case 32: return GemmCfg<32>::kStages;
+    case 64: return GemmCfg<64>::kStages;
+    case 128: return GemmCfg<128>::kStages;
+    default: return GemmCfg<256>::kStages;
+  }
+}
+
+size_t gemm_smem_bytes(int bn) {
+  switch (bn) {
+    case 16: return GemmCfg<16>::kSmemBytes;
+    case 32: return GemmCfg<32>::kSmemBytes;
+    case 64: return GemmCfg<64>::kSmemBytes;
+    case 128: return GemmCfg<128>::kSmemBytes;
+    default: return GemmCfg<256>::kSmemBytes;
+  }
+}
+
+template <int BN, int MODE>
+static cudaError_t launch_one(const CUtensorMap& tm_w, const CUtensorMap& tm_x,
+                              const CUtensorMap& tm_lb, const CUtensorMap& tm_lu,
+                              const GemmParams& p, int grid, cudaStream_t s) {
+  auto kern = expert_gemm_kernel<BN, MODE>;
+  const int smem = GemmCfg<BN>::kSmemBytes;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  kern<<<grid, 192, smem, s>>>(tm_w, tm_x, tm_lb, tm_lu, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_expert_gemm(int mode, int bn, const CUtensorMap& tm_w, const CUtensorMap& tm_x,
+                               const CUtensorMap& tm_lb, const CUtensorMap& tm_lu,
+                               const GemmParams& p, int grid, cudaStream_t s) {
+#define MOE_GEMM_CASE(BNV)                                                          \
+  case BNV:                                                                         \
+    return mode == kGateUp ? launch_one<BNV, kGateUp>(tm_w, tm_x, tm_lb, tm_lu, p, grid, s) \
+                           : launch_one<BNV, kDown>(tm_w, tm_x, tm_lb, tm_lu, p, grid, s);
+  switch (bn) {
+    MOE_GEMM_CASE(16)
+    MOE_GEMM_CASE(32)
+    MOE_GEMM_CASE(64)
+    MOE_GEMM_CASE(128)
+    MOE_GEMM_CASE(256)
+    default: return cudaErrorInvalidValue;
+  }
+#undef MOE_GEMM_CASE
+}
+
+}  // namespace moe

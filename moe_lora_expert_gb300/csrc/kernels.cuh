@@ -1,0 +1,97 @@
+// Internal declarations shared by the kernel translation units and the C-ABI
+// shim.  Nothing here is part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Token-tile widths for which the permute scan writes per-expert tile
+// prefixes: tile_start[bn_index][e] = sum_{e' < e} ceil(n_e' / bn).
+constexpr int kNumTileWidths = 5;
+__host__ __device__ constexpr int tile_width_of(int idx) { return 16 << idx; }  // 16..256
+__host__ __device__ constexpr int tile_width_index(int bn) {
+  return bn == 16 ? 0 : bn == 32 ? 1 : bn == 64 ? 2 : bn == 128 ? 3 : 4;
+}
+
+// ---------------------------------------------------------------- routing
+cudaError_t launch_route_topk(const float* logits, int T, int E, int top_k, int32_t* ids,
+                              float* w, cudaStream_t s);
+
+// ---------------------------------------------------------------- permute
+struct PermuteParams {
+  const int32_t* topk_ids;      // [n] expanded ids
+  int n;                        // T * top_k
+  int top_k;
+  int E;
+  int H;
+  const __nv_bfloat16* hidden;  // [T, H] or null
+  __nv_bfloat16* permuted;      // [n, H] or null
+  const int32_t* mapping;       // [T] or null (forward only)
+  int num_adapters;
+  int32_t* row_adapter;         // [n] or null (forward only)
+  int32_t* expert_offsets;      // [E + 1]
+  int32_t* e2p;                 // [n]
+  int32_t* p2e;                 // [n]
+  int32_t* chunk_counts;        // [nchunks, E]
+  int32_t* tile_start;          // [kNumTileWidths, E + 1] or null
+  int* status;
+};
+constexpr int kPermuteChunk = 1024;
+size_t permute_scratch_bytes(int n, int E);
+cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s);
+
+// ------------------------------------------------------------ LoRA shrink
+// U[p, a*r + i] = bf16(scaling * sum_k A[a, e(p)][i, k] * X[p, k]) for the
+// row's own adapter a, and 0 in every other column of the row.
+struct ShrinkParams {
+  const __nv_bfloat16* X;       // [n, K]
+  int K;
+  const __nv_bfloat16* A;       // factor base
+  int64_t a_stride_adapter;     // elements
+  int64_t a_stride_expert;      // elements (0 = shared)
+  const int32_t* row_adapter;   // [n]
+  const int32_t* expert_offsets;// [E + 1]
+  const int32_t* tile_start16;  // [E + 1] prefix of ceil(n_e / 16)
+  int E;
+  int num_adapters;
+  int rank;
+  float scaling;
+  __nv_bfloat16* U;             // [n, num_adapters * rank]
+};
+cudaError_t launch_lora_shrink(const ShrinkParams& p, int n_rows, cudaStream_t s);
+
+// ------------------------------------------------------- expert GEMMs
+// Swap-AB grouped GEMM: D[feature, token] = W_e[feature, :] . X[token, :]
+// (+ LoRA expand as extra K blocks), accumulated in TMEM.
+struct GemmParams {
+  const int32_t* expert_offsets;  // [E + 1]
+  const int32_t* tile_start;      // [E + 1] tile prefix for this tile width
+  const int32_t* row_adapter;     // [n]
+  int E;
+  int K;                          // main reduction length (H or I)
+  int rows_per_expert;            // rows of the weight per expert (2I or H)
+  int n_feat;                     // output features (I for gate_up, H for down)
+  int feat_blocks;                // feature blocks per expert
+  int num_adapters;               // 0 = no LoRA
+  int rank;
+  int64_t lb_row_stride_adapter;  // B-factor rows between adapters
+  int64_t lb_row_stride_expert;   // B-factor rows between experts (0 = shared)
+  __nv_bfloat16* out;             // [n, n_feat]
+  int* status;
+  uint64_t timeout_ns;
+};
+enum GemmMode { kGateUp = 0, kDown = 1 };
+int gemm_stage_count(int bn);
+size_t gemm_smem_bytes(int bn);
+cudaError_t launch_expert_gemm(int mode, int bn, const CUtensorMap& tm_w, const CUtensorMap& tm_x,
+                               const CUtensorMap& tm_lb, const CUtensorMap& tm_lu,
+                               const GemmParams& p, int grid, cudaStream_t s);
+
+// --------------------------------------------------------------- finalize
+cudaError_t launch_finalize(const __nv_bfloat16* y, const int32_t* e2p, const float* w, int T,
+                            int top_k, int H, __nv_bfloat16* out, cudaStream_t s);
+
+}  // namespace moe

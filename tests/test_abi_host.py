@@ -1,0 +1,187 @@
+"""C ABI checks that need no GPU: the library loads, exports every function
+that include/moe_lora.h declares, plans workspaces, and rejects invalid
+arguments on the host before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import moe_lora_expert_gb300 as m
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_lora.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(m.LIB_PATH):
+        from moe_lora_expert_gb300 import _build
+        _build.build()
+    return m.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(moe_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ["moe_route_topk", "moe_permute", "moe_lora_forward", "moe_lora_workspace_size",
+                 "moe_read_device_status", "moe_status_string"]:
+        assert must in names
+    assert sorted(names) == sorted(m.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_abi_version_and_struct_layout(lib, tmp_path):
+    """ctypes field offsets equal the C compiler's offsetof for every field."""
+    import shutil
+    import subprocess
+    assert lib.moe_lora_abi_version() == 1
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    checks = []
+    for struct, ctype in [(m.LoraFactors, "moe_lora_factors_t"), (m.MoeLoraArgs, "moe_lora_args_t"),
+                          (m.WorkspacePlan, "moe_lora_workspace_plan_t")]:
+        checks.append(f'printf("%s sizeof %zu\\n", "{ctype}", sizeof({ctype}));')
+        for fname, _ in struct._fields_:
+            checks.append(f'printf("%s %s %zu\\n", "{ctype}", "{fname}", offsetof({ctype}, {fname}));')
+    prog = tmp_path / "layout.c"
+    prog.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "moe_lora.h"\n'
+                    "int main(void) {\n" + "\n".join(checks) + "\nreturn 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(prog), "-o", str(exe)], check=True)
+    lines = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    got = {}
+    for ln in lines:
+        if ln.strip():
+            *key, val = ln.split()
+            got[" ".join(key)] = int(val)
+    for struct, ctype in [(m.LoraFactors, "moe_lora_factors_t"), (m.MoeLoraArgs, "moe_lora_args_t"),
+                          (m.WorkspacePlan, "moe_lora_workspace_plan_t")]:
+        assert got[f"{ctype} sizeof"] == ctypes.sizeof(struct), ctype
+        for fname, _ in struct._fields_:
+            assert got[f"{ctype} {fname}"] == getattr(struct, fname).offset, (ctype, fname)
+
+
+def test_status_strings(lib):
+    for code in range(0, -10, -1):
+        s = m.status_string(code)
+        assert s.startswith("MOE_"), (code, s)
+    assert "unknown" in m.status_string(-99)
+
+
+def test_workspace_plan(lib):
+    T, H, I, E, k, A, r = 16, 2048, 768, 128, 8, 4, 16
+    plan = m.moe_lora_workspace_plan(T, H, I, E, k, A, r)
+    n = T * k
+    assert plan.total_bytes == m.moe_lora_workspace_size(T, H, I, E, k, A, r)
+    offs = [plan.status, plan.topk_ids, plan.topk_w, plan.expert_offsets, plan.expanded_to_permuted,
+            plan.permuted_to_expanded, plan.row_adapter, plan.permute_scratch, plan.permuted_hidden,
+            plan.lora_u, plan.act]
+    assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    assert plan.act + n * I * 2 <= plan.total_bytes
+    assert plan.lora_u + n * A * r * 2 <= plan.act
+    # the down GEMM output reuses the permuted hidden rows, the down operand the gate_up one
+    assert plan.expert_out == plan.permuted_hidden and plan.lora_v == plan.lora_u
+    # no LoRA -> no LoRA operand
+    p0 = m.moe_lora_workspace_plan(T, H, I, E, k, 0, 0)
+    assert p0.act == p0.lora_u
+    assert m.moe_lora_workspace_size(0, H, I, E, k, A, r) > 0
+
+
+@pytest.mark.parametrize("args,status", [
+    ((16, 2048, 768, 128, 129, 4, 16), m.MOE_ERR_UNSUPPORTED),   # top_k > 32
+    ((16, 2048, 768, 8, 9, 4, 16), m.MOE_ERR_SHAPE),             # top_k > E
+    ((16, 2044, 768, 128, 8, 4, 16), m.MOE_ERR_ALIGN),           # H % 8
+    ((16, 2048, 770, 128, 8, 4, 16), m.MOE_ERR_ALIGN),           # I % 8
+    ((16, 2048, 768, 128, 8, 4, 12), m.MOE_ERR_UNSUPPORTED),     # rank % 8
+    ((16, 2048, 768, 128, 8, 4, 136), m.MOE_ERR_UNSUPPORTED),    # rank > 128
+    ((16, 2048, 768, 128, 8, 65, 16), m.MOE_ERR_UNSUPPORTED),    # adapters > 64
+    ((16, 2048, 768, 1025, 8, 4, 16), m.MOE_ERR_UNSUPPORTED),    # E > 1024
+    ((-1, 2048, 768, 128, 8, 4, 16), m.MOE_ERR_SHAPE),
+])
+def test_plan_rejects(lib, args, status):
+    plan = m.WorkspacePlan()
+    assert lib.moe_lora_workspace_plan(*args, ctypes.byref(plan)) == status
+    assert lib.moe_lora_workspace_size(*args) == 0
+
+
+def _valid_args(**over):
+    """Arguments that pass every host check except the ones overridden.  The
+    pointers are fake (never dereferenced: each case fails a check first)."""
+    a = m.MoeLoraArgs()
+    a.struct_size = ctypes.sizeof(m.MoeLoraArgs)
+    a.T, a.H, a.I, a.E, a.top_k, a.num_adapters, a.rank = 16, 2048, 768, 128, 8, 4, 16
+    a.scaling = 2.0
+    fake = 1 << 20
+    a.hidden = a.w13 = a.w2 = a.router_logits = a.token_lora_mapping = a.out = fake
+    a.gate_up = m.LoraFactors(fake, fake, 128 * 16 * 2048, 16 * 2048, 128 * 1536 * 16, 1536 * 16)
+    a.down = m.LoraFactors(fake, fake, 128 * 16 * 768, 16 * 768, 128 * 2048 * 16, 2048 * 16)
+    a.workspace = fake
+    a.workspace_bytes = m.moe_lora_workspace_size(16, 2048, 768, 128, 8, 4, 16)
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("over,status", [
+    ({"struct_size": 8}, m.MOE_ERR_UNSUPPORTED),
+    ({"hidden": None}, m.MOE_ERR_NULL),
+    ({"out": None}, m.MOE_ERR_NULL),
+    ({"router_logits": None}, m.MOE_ERR_NULL),
+    ({"workspace": None}, m.MOE_ERR_NULL),
+    ({"token_lora_mapping": None}, m.MOE_ERR_NULL),
+    ({"w13": (1 << 20) + 8}, m.MOE_ERR_ALIGN),
+    ({"workspace": (1 << 20) + 128}, m.MOE_ERR_WORKSPACE),
+    ({"workspace_bytes": 1024}, m.MOE_ERR_WORKSPACE),
+    ({"top_k": 200}, m.MOE_ERR_UNSUPPORTED),
+    ({"top_k": 0}, m.MOE_ERR_SHAPE),
+    ({"tile_n": 48}, m.MOE_ERR_UNSUPPORTED),
+    ({"wait_timeout_ms": -1}, m.MOE_ERR_SHAPE),
+    ({"rank": 20}, m.MOE_ERR_UNSUPPORTED),
+    ({"gate_up": m.LoraFactors(1 << 20, 1 << 20, 4, 0, 0, 0)}, m.MOE_ERR_ALIGN),
+    ({"down": m.LoraFactors(1 << 20, 1 << 20, 8, 8, 24, 0)}, m.MOE_ERR_ALIGN),   # b stride % r
+    ({"down": m.LoraFactors(1 << 20, 1 << 20, -8, 0, 0, 0)}, m.MOE_ERR_SHAPE),
+    ({"down": m.LoraFactors(1 << 20, None, 8, 8, 16, 0)}, m.MOE_ERR_NULL),
+])
+def test_forward_rejects_on_host(lib, over, status):
+    a = _valid_args(**over)
+    assert lib.moe_lora_forward(ctypes.byref(a), None) == status
+
+
+def test_forward_null_args(lib):
+    assert lib.moe_lora_forward(None, None) == m.MOE_ERR_NULL
+
+
+def test_route_and_permute_reject_on_host(lib):
+    fake = 1 << 20
+    assert lib.moe_route_topk(fake, 4, 8, 9, fake, fake, None) == m.MOE_ERR_SHAPE
+    assert lib.moe_route_topk(fake, 4, 2048, 8, fake, fake, None) == m.MOE_ERR_UNSUPPORTED
+    assert lib.moe_route_topk(None, 4, 8, 2, fake, fake, None) == m.MOE_ERR_NULL
+    assert lib.moe_route_topk(None, 0, 8, 2, None, None, None) == m.MOE_OK   # T == 0: nothing to do
+    ws = m.lib().moe_permute_workspace_size(4, 2, 8)
+    assert ws > 0
+    assert lib.moe_permute(fake, 4, 2, 8, None, 0, fake, fake, fake, None, fake + 64, ws, None) == \
+        m.MOE_ERR_WORKSPACE
+    assert lib.moe_permute(fake, 4, 2, 8, None, 0, fake, fake, fake, None, fake, 16, None) == \
+        m.MOE_ERR_WORKSPACE
+    assert lib.moe_permute(fake, 4, 2, 8, fake, 12, fake, fake, fake, fake, fake, ws, None) == \
+        m.MOE_ERR_ALIGN
+    assert lib.moe_permute(fake, 4, 2, 8, None, 0, None, fake, fake, None, fake, ws, None) == \
+        m.MOE_ERR_NULL
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(m, "_lib", None)
+    monkeypatch.setattr(m, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        m.lib()

@@ -1,0 +1,232 @@
+"""CUDA path against the CPU oracle, through the C ABI (needs a GB300).
+
+Routing ids and the permutation are compared bit for bit; routing weights
+within a float32 error bound; the bf16 layer output per element within
+3e-2 + 2e-2*|ref| and in relative Frobenius norm within 1e-2.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from gpu_util import (assert_output_close, bf16_tensor, cached_inputs, check_routing, dev,
+                      make_layer, run_gpu, to_f64, torch_mod, W_RTOL)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import moe_lora_expert_gb300 as m
+    m.lib()
+    yield
+
+
+# ----------------------------------------------------------------- routing
+
+@pytest.mark.parametrize("T,E,k", [(1, 8, 2), (37, 128, 8), (300, 33, 5), (64, 1024, 32),
+                                   (5, 16, 16), (4096, 128, 8), (3, 1, 1)])
+def test_route_topk_matches_oracle(T, E, k):
+    import moe_lora_expert_gb300 as m
+    torch = torch_mod()
+    logits = np.random.default_rng(T * 7 + E).standard_normal((T, E)).astype(np.float32)
+    ids, w = m.moe_route_topk(torch.from_numpy(logits).to(dev()), k)
+    ids_ref, w_ref = oracle.route_topk(logits, k)
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    np.testing.assert_allclose(w.cpu().numpy(), w_ref, rtol=W_RTOL, atol=1e-9)
+
+
+def test_route_topk_ties_and_signed_zero():
+    import moe_lora_expert_gb300 as m
+    torch = torch_mod()
+    logits = np.array([[1.0, 2.0, 2.0, 0.0, 2.0] + [-5.0] * 35,
+                       [0.0] * 40,
+                       [-0.0, 0.0, -1.0, 0.0, -0.0] + [-7.0] * 35], dtype=np.float32)
+    ids, w = m.moe_route_topk(torch.from_numpy(logits).to(dev()), 3)
+    ids_ref, w_ref = oracle.route_topk(logits, 3)
+    assert ids.cpu().numpy().tolist() == ids_ref.tolist() == [[1, 2, 4], [0, 1, 2], [0, 1, 3]]
+    np.testing.assert_allclose(w.cpu().numpy(), w_ref, rtol=W_RTOL)
+
+
+# ----------------------------------------------------------------- permute
+
+@pytest.mark.parametrize("T,k,E,H", [(1, 1, 1, 8), (8, 2, 8, 256), (300, 8, 128, 72),
+                                     (4096, 8, 128, 2048), (1000, 3, 1024, 16), (129, 8, 4, 40)])
+def test_permute_matches_oracle(T, k, E, H):
+    import moe_lora_expert_gb300 as m
+    torch = torch_mod()
+    rng = np.random.default_rng(T + E)
+    ids = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    hidden = workloads.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    off, e2p, p2e, xp, ws = m.moe_permute(torch.from_numpy(ids).to(dev()), E, bf16_tensor(hidden))
+    assert m.moe_read_device_status(ws) == m.MOE_OK
+    off_r, e2p_r, p2e_r = oracle.permute(ids, E)
+    assert np.array_equal(off.cpu().numpy(), off_r)
+    assert np.array_equal(e2p.cpu().numpy(), e2p_r)
+    assert np.array_equal(p2e.cpu().numpy(), p2e_r)
+    xp_bits = xp.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(xp_bits, hidden[p2e_r // k])
+
+
+def test_permute_unrouted_and_invalid_ids():
+    import moe_lora_expert_gb300 as m
+    torch = torch_mod()
+    ids = np.array([[2, -1], [0, 2], [-1, 1], [7, 1], [0, -5]], dtype=np.int32)
+    off, e2p, p2e, _, ws = m.moe_permute(torch.from_numpy(ids).to(dev()), 3)
+    assert m.moe_read_device_status(ws) == m.MOE_ERR_BAD_EXPERT_ID
+    clean = np.where((ids >= 0) & (ids < 3), ids, -1)
+    off_r, e2p_r, p2e_r = oracle.permute(clean, 3)
+    assert np.array_equal(off.cpu().numpy(), off_r)
+    assert np.array_equal(e2p.cpu().numpy(), e2p_r)
+    assert np.array_equal(p2e.cpu().numpy(), p2e_r)
+
+
+# ----------------------------------------------------------------- forward
+
+FULL_SAMPLE = {"prefill_T4096": list(range(0, 4096, 64)) + [4095]}
+
+
+@pytest.mark.parametrize("name", workloads.WORKLOAD_ORDER)
+def test_forward_workload(name):
+    inp = cached_inputs(name)
+    res = run_gpu(inp)
+    assert res["status"] == 0, res["status_str"]
+    check_routing(res, inp)
+    tokens = FULL_SAMPLE.get(name)
+    ref = oracle.forward_inputs(inp, tokens=tokens)
+    got = res["out64"] if tokens is None else res["out64"][tokens]
+    rel = assert_output_close(got, ref["out64"], name)
+    print(f"{name}: relative Frobenius error {rel:.3e}")
+
+
+@pytest.mark.parametrize("tile_n", [16, 32, 64, 128, 256])
+def test_forward_every_tile_width(tile_n):
+    wl = workloads.small_workload("tiles", T=96, H=192, I=136, E=6, top_k=3, num_adapters=3,
+                                  rank=16, map_lo=-1, map_hi=2, seed=31)
+    inp = workloads.make_inputs(wl)
+    res = run_gpu(inp, tile_n=tile_n)
+    assert res["status"] == 0, res["status_str"]
+    check_routing(res, inp)
+    assert_output_close(res["out64"], oracle.forward_inputs(inp)["out64"], f"tile_n={tile_n}")
+
+
+EDGE = [
+    workloads.small_workload("one_token", T=1, H=64, I=64, E=4, top_k=2, rank=8, seed=41),
+    workloads.small_workload("one_expert_k1", T=20, H=128, I=64, E=1, top_k=1, num_adapters=2,
+                             rank=16, seed=42),
+    workloads.small_workload("k_eq_E", T=17, H=64, I=32, E=4, top_k=4, num_adapters=2, rank=8,
+                             seed=43),
+    workloads.small_workload("ragged_dims", T=33, H=200, I=72, E=5, top_k=2, num_adapters=2,
+                             rank=24, seed=44),
+    workloads.small_workload("rank128", T=40, H=256, I=128, E=4, top_k=2, num_adapters=2,
+                             rank=128, seed=45),
+    workloads.small_workload("rank72", T=40, H=256, I=128, E=4, top_k=2, num_adapters=3,
+                             rank=72, seed=46),
+    workloads.small_workload("many_adapters", T=200, H=128, I=64, E=8, top_k=2, num_adapters=64,
+                             rank=8, map_lo=-1, map_hi=63, seed=47),
+    workloads.small_workload("shared_outer", T=64, H=256, I=128, E=8, top_k=4, num_adapters=3,
+                             rank=32, shared_outer=True, bias_sigma=2.0, map_lo=-1, map_hi=2,
+                             seed=48),
+    workloads.small_workload("no_lora", T=50, H=128, I=96, E=6, top_k=2, num_adapters=0, rank=0,
+                             seed=49),
+    workloads.small_workload("hot_expert", T=700, H=128, I=64, E=16, top_k=2, num_adapters=2,
+                             rank=16, bias_sigma=4.0, seed=50),
+    workloads.small_workload("many_chunks", T=1500, H=64, I=64, E=32, top_k=2, num_adapters=2,
+                             rank=8, seed=51),
+]
+
+
+@pytest.mark.parametrize("wl", EDGE, ids=lambda w: w.name)
+def test_forward_edge_cases(wl):
+    inp = workloads.make_inputs(wl)
+    res = run_gpu(inp)
+    assert res["status"] == 0, res["status_str"]
+    check_routing(res, inp)
+    assert_output_close(res["out64"], oracle.forward_inputs(inp)["out64"], wl.name)
+
+
+def test_intermediates_match_oracle():
+    """Activation h and expert output y, row by row, on the tiny layer."""
+    import moe_lora_expert_gb300 as m
+    torch = torch_mod()
+    inp = cached_inputs("tiny_T8")
+    wl = inp.wl
+    res = run_gpu(inp)
+    ref = oracle.forward_inputs(inp, keep_intermediates=True)
+    layer = res["layer"]
+    plan = layer.plan(wl.T)
+    ws = layer._ws
+    n = wl.T * wl.top_k
+
+    def view_bf16(off, cols):
+        return ws[off:off + n * cols * 2].view(torch.bfloat16).reshape(n, cols).float().cpu().numpy()
+
+    h = view_bf16(plan.act, wl.I)
+    y = view_bf16(plan.expert_out, wl.H)
+    for t in range(wl.T):
+        for j in range(wl.top_k):
+            p = res["e2p"][t * wl.top_k + j]
+            g_r, h_r, y_r = ref["intermediates"][(t, j)]
+            assert_output_close(h[p], h_r, f"h[{t},{j}]")
+            assert_output_close(y[p], y_r, f"y[{t},{j}]")
+
+
+def test_no_adapter_tokens_reproduce_plain_moe_bitwise():
+    inp = workloads.make_inputs(workloads.WORKLOADS["tiny_T8"])
+    plain = run_gpu(inp, with_lora=False)["out"]
+    none = run_gpu(inp, mapping=np.full(inp.wl.T, -1, np.int32))["out"]
+    torch = torch_mod()
+    assert torch.equal(plain.view(torch.int16), none.view(torch.int16))
+    mixed = run_gpu(inp)["out"].float()
+    rows = np.where(inp.mapping < 0)[0]
+    assert len(rows) > 0
+    assert torch.equal(mixed[rows], plain.float()[rows])
+
+
+def test_zero_scaling_reproduces_plain_moe():
+    wl = dataclasses.replace(workloads.WORKLOADS["tiny_T8"], scaling=0.0)
+    inp = workloads.make_inputs(wl)
+    torch = torch_mod()
+    a = run_gpu(inp)["out"].float()
+    b = run_gpu(inp, with_lora=False)["out"].float()
+    assert torch.equal(a, b)
+
+
+def test_bad_mapping_is_flagged_and_dropped():
+    import moe_lora_expert_gb300 as m
+    inp = workloads.make_inputs(workloads.WORKLOADS["tiny_T8"])
+    bad = inp.mapping.copy()
+    bad[1], bad[5] = 7, -4
+    res = run_gpu(inp, mapping=bad)
+    assert res["status"] == m.MOE_ERR_BAD_MAPPING
+    clean = bad.copy()
+    clean[1] = clean[5] = -1
+    inp.mapping = clean
+    assert_output_close(res["out64"], oracle.forward_inputs(inp)["out64"], "bad mapping")
+
+
+def test_empty_batch_is_a_noop():
+    import moe_lora_expert_gb300 as m
+    torch = torch_mod()
+    inp = cached_inputs("tiny_T8")
+    layer = make_layer(inp)
+    hidden = torch.empty((0, inp.wl.H), dtype=torch.bfloat16, device=dev())
+    logits = torch.empty((0, inp.wl.E), dtype=torch.float32, device=dev())
+    mapping = torch.empty((0,), dtype=torch.int32, device=dev())
+    out = layer.forward(hidden, logits, mapping)
+    assert out.shape == (0, inp.wl.H)
+    assert layer.device_status() == m.MOE_OK
+
+
+def test_repeated_calls_are_deterministic():
+    inp = cached_inputs("decode_T16")
+    layer = make_layer(inp)
+    torch = torch_mod()
+    a = run_gpu(inp, layer=layer)["out"].clone()
+    b = run_gpu(inp, layer=layer)["out"]
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
