@@ -1,0 +1,457 @@
+#!/usr/bin/env python
+"""Benchmark of the routed BF16 MoE-LoRA layer forward (libmoelora, GB300).
+
+One step = one ``moe_lora_forward`` call over one batch: routing, permute,
+gate_up LoRA shrink, gate_up GEMM (+ LoRA expand, SwiGLU), down LoRA shrink,
+down GEMM (+ LoRA expand), finalize.  Inputs are the seeded synthetic layer of
+``workloads.py`` (default: decode_T16, T=16 tokens of a 30B-A3B-shaped layer,
+H=2048, I=768, E=128, top-8, 4 adapters of rank 16), resident in HBM when the
+timed region starts.  L2 is flushed (256 MiB write) before every step, outside
+the step's events.
+
+Prints one JSON line.  ``--impl reference`` times the CPU oracle instead.
+Multi-GPU (torchrun): every rank runs an independent replica of the same
+workload (the path has no cross-GPU exchange); value = all ranks' tokens /
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-LoRA layer tokens/s at T=16/64/4096; % of HBM/tensor roofline"
+DEFAULT_WORKLOAD = "decode_T16"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--tile-n", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic work of one forward (from the actual routing of the inputs)
+# ---------------------------------------------------------------------------
+
+def algorithmic_work(wl, ids, mapping):
+    """Bytes and FLOPs the forward must move / compute, intermediates excluded.
+
+    Bytes: every touched expert's w13 and w2 once, every touched LoRA factor
+    once (shared factors once per adapter), the hidden input, the output, the
+    router logits and the mapping.  FLOPs: 2 per multiply-add of the two expert
+    GEMMs for every (token, slot) and of the four LoRA products for adapted
+    slots (the shared gate_up shrink once per token).
+    """
+    import numpy as np
+    T, H, I, E, k, A, r = wl.T, wl.H, wl.I, wl.E, wl.top_k, wl.num_adapters, wl.rank
+    n = T * k
+    experts = sorted(set(int(e) for e in ids.ravel()))
+    lora = A > 0 and r > 0
+    adapted = [(t, int(mapping[t])) for t in range(T) if lora and mapping[t] >= 0]
+    pairs = sorted({(a, int(e)) for t, a in adapted for e in ids[t]})
+    adapters = sorted({a for _, a in adapted})
+    w13_b, w2_b = 2 * I * H * 2, H * I * 2
+    gu_A = (len(adapters) if wl.shared_outer else len(pairs)) * r * H * 2
+    gu_B = len(pairs) * 2 * I * r * 2
+    dn_A = len(pairs) * r * I * 2
+    dn_B = (len(adapters) if wl.shared_outer else len(pairs)) * H * r * 2
+    io = T * H * 2 * 2 + T * E * 4 + T * 4
+    n_ad = len(adapted) * k
+    shrink_gu_rows = len(adapted) if wl.shared_outer else n_ad
+    flops_gemm = n * 2 * (2 * I * H + H * I)
+    flops_lora = 2 * r * (shrink_gu_rows * H + n_ad * 2 * I + n_ad * I + n_ad * H)
+    work = {
+        "distinct_experts": len(experts), "lora_pairs": len(pairs),
+        "bytes": len(experts) * (w13_b + w2_b) + gu_A + gu_B + dn_A + dn_B + io,
+        "flops": flops_gemm + flops_lora,
+    }
+    # per-kernel figures for the two expert GEMMs
+    work["gemm_gate_up"] = {
+        "bytes": len(experts) * w13_b + gu_B + n * H * 2 + n_ad * r * 2 + n * I * 2,
+        "flops": n * 2 * 2 * I * H + n_ad * 2 * 2 * I * r,
+    }
+    work["gemm_down"] = {
+        "bytes": len(experts) * w2_b + dn_B + n * I * 2 + n_ad * r * 2 + n * H * 2,
+        "flops": n * 2 * H * I + n_ad * 2 * H * r,
+    }
+    return work
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {k: float(pk[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ["expert_gemm.cu", "ptx.cuh", "kernels.cuh"]:
+        with open(os.path.join(ROOT, "moe_lora_expert_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            doc = json.load(f)
+    except Exception:
+        return None
+    ent = doc.get(kernel, {}).get(workload)
+    if not ent or ent.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (run in a fresh single-threaded interpreter)
+# ---------------------------------------------------------------------------
+
+def cpu_baseline_child(workload, seconds):
+    import numpy as np
+    import oracle
+    import workloads
+    wl = workloads.WORKLOADS[workload]
+    inp = workloads.make_inputs(wl)
+    tokens_done, elapsed, calls = 0, 0.0, 0
+    stride = max(1, wl.T // 4)
+    start_tok = 0
+    while elapsed < seconds:
+        toks = [(start_tok + i * stride) % wl.T for i in range(4)]
+        t0 = time.perf_counter()
+        oracle.forward_inputs(inp, tokens=toks)
+        elapsed += time.perf_counter() - t0
+        tokens_done += len(toks)
+        calls += 1
+        start_tok += 1
+    print(json.dumps({"value": tokens_done / elapsed, "tokens": tokens_done, "seconds": elapsed,
+                      "calls": calls}))
+
+
+def run_cpu_baseline(workload, seconds):
+    env = dict(os.environ)
+    for v in ["OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"]:
+        env[v] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    res = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-child",
+                          "--workload", workload, "--cpu-seconds", str(seconds)],
+                         capture_output=True, text=True, env=env, timeout=600)
+    if res.returncode != 0:
+        return {"error": res.stderr.strip().splitlines()[-1:] or ["failed"]}
+    d = json.loads(res.stdout.strip().splitlines()[-1])
+    return {"value": d["value"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": (f"{d['tokens']} tokens of {workload} in {d['calls']} oracle calls of 4 tokens "
+                       f"({d['seconds']:.1f} s, float64 numpy, 1 BLAS thread)")}
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import moe_lora_expert_gb300 as m
+    import workloads
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = workloads.WORKLOADS[args.workload]
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = run_cpu_baseline(args.workload, args.cpu_seconds)
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    inp = workloads.make_inputs(wl)
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    lora = inp.A_gu is not None
+    layer = m.MoeLoraLayer(bf16(inp.w13), bf16(inp.w2), wl.top_k,
+                           bf16(inp.A_gu) if lora else None, bf16(inp.B_gu) if lora else None,
+                           bf16(inp.A_dn) if lora else None, bf16(inp.B_dn) if lora else None,
+                           scaling=wl.scaling, max_tokens=wl.T)
+    hidden = bf16(inp.hidden)
+    logits = torch.from_numpy(inp.logits).to(dev)
+    mapping = torch.from_numpy(inp.mapping).to(dev) if lora else None
+    out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
+    ids = torch.empty((wl.T, wl.top_k), dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        layer.forward(hidden, logits, mapping, out=out, topk_ids=ids, tile_n=args.tile_n,
+                      stage_events=evs)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st = layer.device_status()
+    if st != m.MOE_OK:
+        raise SystemExit(f"device status after warm-up: {m.status_string(st)}")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(m.MOE_NUM_STAGE_EVENTS)]
+              for _ in range(args.steps)]
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids_vis = [v.strip() for v in visible.split(",") if v.strip()]
+    clocks = ClockSampler(ids_vis[local] if local < len(ids_vis) else local)
+    clocks.start()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        step(events[i])
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+
+    stage_ms = [[ev[j].elapsed_time(ev[j + 1]) for j in range(m.MOE_NUM_STAGE_EVENTS - 1)]
+                for ev in events]
+    step_ms = [sum(s) for s in stage_ms]
+    total_ms = sum(step_ms)
+    if pg:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * wl.T * args.steps / (total_ms / 1e3)
+
+    # ---------------- e2e: host buffers, copies inside the timed region
+    h_hidden = hidden.cpu().pin_memory()
+    h_logits = logits.cpu().pin_memory()
+    h_mapping = mapping.cpu().pin_memory() if lora else None
+    h_out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
+    d_hidden, d_logits = torch.empty_like(hidden), torch.empty_like(logits)
+    d_mapping = torch.empty_like(mapping) if lora else None
+    e2e_steps = max(1, min(args.steps, 200))
+    e_ms = 0.0
+    for i in range(args.warmup + e2e_steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        d_hidden.copy_(h_hidden, non_blocking=True)
+        d_logits.copy_(h_logits, non_blocking=True)
+        if lora:
+            d_mapping.copy_(h_mapping, non_blocking=True)
+        layer.forward(d_hidden, d_logits, d_mapping, out=out, tile_n=args.tile_n)
+        h_out.copy_(out, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        if i >= args.warmup:
+            e_ms += e0.elapsed_time(e1)
+    if pg:
+        t = torch.tensor([e_ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e_ms = float(t.item())
+    h2d = wl.T * wl.H * 2 + wl.T * wl.E * 4 + (wl.T * 4 if lora else 0)
+    e2e = {"value": world * wl.T * e2e_steps / (e_ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": wl.T * wl.H * 2}
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return
+
+    # ---------------- roofline
+    ids_np = ids.cpu().numpy()
+    work = algorithmic_work(wl, ids_np, inp.mapping)
+    peaks, peak_src = load_peaks()
+    med = [statistics.median(s[j] for s in stage_ms) for j in range(len(m.STAGE_NAMES))]
+    stages_us = {nm: round(v * 1e3, 2) for nm, v in zip(m.STAGE_NAMES, med)}
+    top = "gemm_gate_up" if med[3] >= med[5] else "gemm_down"
+    kt_ms = statistics.mean(s[3 if top == "gemm_gate_up" else 5] for s in stage_ms)
+    kw = work[top]
+    t_bytes = kw["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_flops = kw["flops"] / (peaks["bf16_tflops"] * 1e12)
+    if t_bytes >= t_flops:
+        achieved = kw["bytes"] / (kt_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    else:
+        achieved = kw["flops"] / (kt_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4)}
+    roof.update({"traffic": committed_traffic(top, args.workload), "kernel": top,
+                 "kernel_us": round(kt_ms * 1e3, 2), "algorithmic_bytes": kw["bytes"],
+                 "algorithmic_flops": kw["flops"], "peak_source": f"{peak_src} (MEASURED_PEAKS.json)"
+                 if peak_src == "measured" else "fallback"})
+    t_roof = max(work["bytes"] / (peaks["hbm_gbs"] * 1e9), work["flops"] / (peaks["bf16_tflops"] * 1e12))
+    fwd = {"bound": "hbm" if work["bytes"] / (peaks["hbm_gbs"] * 1e9) >= work["flops"] / (peaks["bf16_tflops"] * 1e12) else "tensor",
+           "t_roof_us": round(t_roof * 1e6, 2), "t_us": round(ms_per_step * 1e3, 2),
+           "frac": round(t_roof / (ms_per_step / 1e3), 4), "bytes": work["bytes"], "flops": work["flops"],
+           "distinct_experts": work["distinct_experts"], "lora_pairs": work["lora_pairs"]}
+
+    n_kernels = 1 + 4 + 2 + 1 + (2 if lora else 0)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded normal inputs and weights; no trained weights)",
+        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
+                   "top_k": wl.top_k, "num_adapters": wl.num_adapters, "rank": wl.rank,
+                   "lora_scaling": wl.scaling, "shared_outer": wl.shared_outer,
+                   "tile_n": args.tile_n or "auto",
+                   "l2": "flushed before every step (256 MiB write, outside the step events)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": roof, "forward_roofline": fwd, "stages_us": stages_us,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_kernels * args.steps,
+        "clocks": clk, "wall_s_timed_region": round(wall, 4),
+    }
+    print(json.dumps(line))
+    if pg:
+        pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the CPU oracle as it stands
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import oracle
+    import workloads
+    wl = workloads.WORKLOADS[args.workload]
+    inp = workloads.make_inputs(wl)
+    cores = 1
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        cores = max([d.get("num_threads", 1) for d in info] + [1])
+    except Exception:
+        cores = os.cpu_count() or 1
+    t = 0.0
+    tokens = 0
+    for i in range(args.warmup + args.steps):
+        tok = [i % wl.T]
+        t0 = time.perf_counter()
+        oracle.forward_inputs(inp, tokens=tok)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            t += dt
+            tokens += len(tok)
+    value = tokens / t
+    sample = f"1 token of {wl.name} per step (float64 numpy oracle)"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded normal inputs and weights; no trained weights)",
+            "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
+                       "top_k": wl.top_k, "num_adapters": wl.num_adapters, "rank": wl.rank,
+                       "parallelism": "host CPU"},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    args = parse_args()
+    if args.cpu_baseline_child:
+        cpu_baseline_child(args.workload, args.cpu_seconds)
+        return
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

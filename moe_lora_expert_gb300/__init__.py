@@ -289,6 +289,11 @@ class MoeLoraLayer:
         a.tile_n, a.wait_timeout_ms = int(tile_n), int(wait_timeout_ms)
         self._events_keepalive = None
         if stage_events is not None:
+            if len(stage_events) != MOE_NUM_STAGE_EVENTS:
+                raise ValueError(f"stage_events needs {MOE_NUM_STAGE_EVENTS} events")
+            for e in stage_events:       # torch creates the CUDA event on first record
+                if not e.cuda_event:
+                    e.record()
             arr = (ctypes.c_void_p * MOE_NUM_STAGE_EVENTS)(*[e.cuda_event for e in stage_events])
             self._events_keepalive = arr
             a.stage_events = ctypes.cast(arr, ctypes.c_void_p)

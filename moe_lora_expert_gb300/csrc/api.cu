@@ -156,6 +156,7 @@ int moe_route_topk(const float* logits, int T, int E, int top_k, int32_t* topk_i
   if (top_k > E) return MOE_ERR_SHAPE;
   if (T == 0) return MOE_OK;
   if (logits == nullptr || topk_ids == nullptr || topk_w == nullptr) return MOE_ERR_NULL;
+  (void)cudaGetLastError();  // launch checks below must not report an earlier, unrelated error
   return cuda_status(moe::launch_route_topk(logits, T, E, top_k, topk_ids, topk_w, stream));
 }
 
@@ -178,6 +179,7 @@ int moe_permute(const int32_t* topk_ids, int T, int top_k, int E, const void* hi
   if (gather && (H <= 0 || H % 8 != 0 || !aligned16(hidden) || !aligned16(permuted_hidden)))
     return MOE_ERR_ALIGN;
   int* status = static_cast<int*>(ws);
+  (void)cudaGetLastError();  // launch checks below must not report an earlier, unrelated error
   if (cudaMemsetAsync(status, 0, 16, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (T == 0) return cuda_status(cudaMemsetAsync(expert_offsets, 0, (E + 1) * sizeof(int32_t), stream));
   if (topk_ids == nullptr || expanded_to_permuted == nullptr || permuted_to_expanded == nullptr)
@@ -240,6 +242,26 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
       a->tile_n != 256)
     return MOE_ERR_UNSUPPORTED;
   if (a->wait_timeout_ms < 0) return MOE_ERR_SHAPE;
+  (void)cudaGetLastError();  // launch checks below must not report an earlier, unrelated error
+
+  struct CUevent_st* const* ev = a->stage_events;
+  int ev_next = 0;
+  auto mark = [&]() -> bool {
+    if (ev == nullptr || ev_next >= MOE_NUM_STAGE_EVENTS) return true;
+    return cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[ev_next++]), stream) == cudaSuccess;
+  };
+  auto finish_marks = [&]() -> bool {
+    while (ev != nullptr && ev_next < MOE_NUM_STAGE_EVENTS)
+      if (!mark()) return false;
+    return true;
+  };
+  if (T == 0) {  // nothing to compute; tensor pointers may be NULL
+    if (a->workspace != nullptr) {
+      if ((reinterpret_cast<uintptr_t>(a->workspace) & (kAlign - 1)) != 0) return MOE_ERR_WORKSPACE;
+      if (cudaMemsetAsync(a->workspace, 0, 16, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return finish_marks() ? MOE_OK : MOE_ERR_CUDA;
+  }
 
   if (a->hidden == nullptr || a->w13 == nullptr || a->w2 == nullptr ||
       a->router_logits == nullptr || a->out == nullptr || a->workspace == nullptr)
@@ -271,22 +293,9 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
       static_cast<int64_t>(E) * H >= (int64_t(1) << 31))
     return MOE_ERR_UNSUPPORTED;
 
-  struct CUevent_st* const* ev = a->stage_events;
-  int ev_next = 0;
-  auto mark = [&]() -> bool {
-    if (ev == nullptr || ev_next >= MOE_NUM_STAGE_EVENTS) return true;
-    return cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[ev_next++]), stream) == cudaSuccess;
-  };
-  auto finish_marks = [&]() -> bool {
-    while (ev != nullptr && ev_next < MOE_NUM_STAGE_EVENTS)
-      if (!mark()) return false;
-    return true;
-  };
-
   uint8_t* ws = static_cast<uint8_t*>(a->workspace);
   int* status = reinterpret_cast<int*>(ws + pl.status);
   if (cudaMemsetAsync(status, 0, 16, stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (T == 0) return finish_marks() ? MOE_OK : MOE_ERR_CUDA;
 
   int32_t* topk_ids = a->topk_ids_out ? a->topk_ids_out : reinterpret_cast<int32_t*>(ws + pl.topk_ids);
   float* topk_w = a->topk_w_out ? a->topk_w_out : reinterpret_cast<float*>(ws + pl.topk_w);
