@@ -126,6 +126,40 @@ int moe_permute(const int32_t* topk_ids, int T, int top_k, int E,
                 void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_permute_noalloc -- moe_permute without a caller-provided scratch buffer.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory (for instance a plugin running inside a
+ * framework that owns all device buffers and forbids cudaMalloc, or an
+ * allocator's own start-up code) and so have no spare buffer to pass as
+ * moe_permute's ``ws``.  The results are those of moe_permute with the same
+ * arguments.
+ *
+ * Scratch: one fixed device array inside the library (status word plus the
+ * per-chunk expert counts, about 256 KiB), held by every GPU that loads the
+ * library until the process exits.  Nothing is allocated or freed by a call.
+ * Limit: T * top_k <= MOE_NOALLOC_MAX_SLOTS and E <= MOE_MAX_EXPERTS; larger
+ * sizes return MOE_ERR_UNSUPPORTED before anything is enqueued.
+ * The first call on each device looks up the array's device address on the
+ * current device; make that first call before any stream capture.
+ * Every call on a device uses the same array, and the array keeps the last
+ * call's contents: calls whose work overlaps on the GPU (other streams,
+ * other host threads) race and give undefined results.  Order them on one
+ * stream or with events.
+ *
+ *   status_out: device int32, or NULL.  When non-NULL it receives the device
+ *     status word of this call (MOE_OK, or MOE_ERR_BAD_EXPERT_ID when an id
+ *     outside [-1, E) was seen), in stream order.
+ * Other arguments as for moe_permute.
+ * ------------------------------------------------------------------------- */
+#define MOE_NOALLOC_MAX_SLOTS 65536
+int moe_permute_noalloc(const int32_t* topk_ids, int T, int top_k, int E,
+                        const void* hidden, int H,
+                        int32_t* expert_offsets, int32_t* expanded_to_permuted,
+                        int32_t* permuted_to_expanded, void* permuted_hidden,
+                        int32_t* status_out, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * LoRA factors of one projection (gate_up or down).
  *
  * One rank-r pair per (adapter, expert) (sglang#4 Flow 1(A):

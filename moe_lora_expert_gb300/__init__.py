@@ -36,7 +36,7 @@ STAGE_NAMES = ["route", "permute", "shrink_gate_up", "gemm_gate_up", "shrink_dow
 EXPORTED_SYMBOLS = [
     "moe_status_string", "moe_lora_abi_version", "moe_route_topk", "moe_permute_workspace_size",
     "moe_permute", "moe_lora_workspace_plan", "moe_lora_workspace_size", "moe_lora_forward",
-    "moe_read_device_status",
+    "moe_read_device_status", "moe_permute_noalloc",
 ]
 
 
@@ -104,6 +104,8 @@ def lib() -> ctypes.CDLL:
         L.moe_lora_forward.argtypes = [ctypes.POINTER(MoeLoraArgs), vp]
         L.moe_read_device_status.restype = i32
         L.moe_read_device_status.argtypes = [vp, vp]
+        L.moe_permute_noalloc.restype = i32
+        L.moe_permute_noalloc.argtypes = [vp, i32, i32, i32, vp, i32, vp, vp, vp, vp, vp, vp]
         _lib = L
     return _lib
 
