@@ -66,6 +66,50 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// N-D bf16 tensor (dims innermost first, strides in bytes for dims 1..rank-1),
+// 128-byte swizzle, zero fill out of bounds.
+bool encode_nd(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+               const uint64_t* strides, const uint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5], e[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1;
+    if (i + 1 < rank) st[i] = strides[i];
+  }
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, st, b, e,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// w13 [E, 2I, H] seen so that one K block of feature block fb lands as
+// 4 groups x (16 gate rows, 16 up rows).  With I % 16 == 0 a 5-D view
+// {H, 16 rows, 2 halves, I/16 groups, E} does it in one box; otherwise a 3-D
+// view {H, I, 2E} in four boxes of {64, 16, 2}.  Rows past I fall outside a
+// dimension of either view and are zero-filled.
+bool encode_w13(CUtensorMap* m, const void* w13, int H, int I, int E, bool* single_box) {
+  const uint64_t row = static_cast<uint64_t>(H) * 2;
+  if (I % 16 == 0) {
+    const uint64_t dims[5] = {static_cast<uint64_t>(H), 16, 2, static_cast<uint64_t>(I / 16),
+                              static_cast<uint64_t>(E)};
+    const uint64_t strides[4] = {row, row * I, row * 16, row * 2 * I};
+    const uint32_t box[5] = {64, 16, 2, 4, 1};
+    if (encode_nd(m, w13, 5, dims, strides, box)) {
+      *single_box = true;
+      return true;
+    }
+  }
+  const uint64_t dims[3] = {static_cast<uint64_t>(H), static_cast<uint64_t>(I),
+                            2ull * static_cast<uint64_t>(E)};
+  const uint64_t strides[2] = {row, row * I};
+  const uint32_t box[3] = {64, 16, 2};
+  *single_box = false;
+  return encode_nd(m, w13, 3, dims, strides, box);
+}
+
 // ------------------------------------------------------------ workspace plan
 bool sizes_ok(int T, int H, int I, int E, int top_k, int num_adapters, int rank) {
   return T >= 0 && H > 0 && I > 0 && E > 0 && top_k > 0 && num_adapters >= 0 && rank >= 0;
@@ -322,7 +366,8 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
 
   // TMA descriptors (host-encoded, passed by value as kernel parameters).
   CUtensorMap tm_w13, tm_w2, tm_xp, tm_h, tm_bgu, tm_bdn, tm_u, tm_v;
-  bool enc = encode_2d(&tm_w13, a->w13, H, static_cast<uint64_t>(E) * 2 * I, H * 2ull, 64, 16) &&
+  bool gu_single_box = false;
+  bool enc = encode_w13(&tm_w13, a->w13, H, I, E, &gu_single_box) &&
              encode_2d(&tm_w2, a->w2, I, static_cast<uint64_t>(E) * H, I * 2ull, 64, 128) &&
              encode_2d(&tm_xp, xp, H, n, H * 2ull, 64, bn) &&
              encode_2d(&tm_h, h, I, n, I * 2ull, 64, bn);
@@ -399,6 +444,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.E = E;
   gp.K = H;
   gp.rows_per_expert = 2 * I;
+  gp.gu_single_box = gu_single_box ? 1 : 0;
   gp.n_feat = I;
   gp.feat_blocks = (I + 63) / 64;
   gp.num_adapters = A;
@@ -408,7 +454,8 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.out = h;
   gp.status = status;
   gp.timeout_ns = timeout_ns;
-  if (moe::launch_expert_gemm(moe::kGateUp, bn, tm_w13, tm_xp, tm_bgu, tm_u, gp, sms, stream) !=
+  if (moe::launch_expert_gemm(moe::kGateUp, bn, tm_w13, tm_xp, tm_bgu, tm_u, gp,
+                              sms * moe::gemm_ctas_per_sm(bn), stream) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
   if (!mark()) return MOE_ERR_CUDA;
@@ -431,7 +478,8 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.lb_row_stride_adapter = dn_rs_a;
   gp.lb_row_stride_expert = dn_rs_e;
   gp.out = y;
-  if (moe::launch_expert_gemm(moe::kDown, bn, tm_w2, tm_h, tm_bdn, tm_v, gp, sms, stream) !=
+  if (moe::launch_expert_gemm(moe::kDown, bn, tm_w2, tm_h, tm_bdn, tm_v, gp,
+                              sms * moe::gemm_ctas_per_sm(bn), stream) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
   if (!mark()) return MOE_ERR_CUDA;

@@ -45,10 +45,14 @@ constexpr unsigned kFullMask = 0xFFFFFFFFu;
 
 template <int BN>
 struct GemmCfg {
+  // Narrow (decode) tiles run two CTAs per SM so that two producers keep TMA
+  // loads in flight; wide tiles run one CTA per SM with deeper stages.
+  static constexpr int kCtasPerSm = BN <= 64 ? 2 : 1;
+  static constexpr int kStageBudget = BN <= 64 ? 96 * 1024 : 200 * 1024;
   static constexpr int kABytes = 128 * 64 * 2;   // 128 rows x 64 K of bf16
   static constexpr int kBBytes = BN * 64 * 2;    // BN rows x 64 K of bf16
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStagesRaw = (200 * 1024) / kStageBytes;
+  static constexpr int kStagesRaw = kStageBudget / kStageBytes;
   static constexpr int kStages = kStagesRaw > 16 ? 16 : kStagesRaw;
   static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr int kMetaBytes = 512;                         // barriers, flags
@@ -109,12 +113,35 @@ __device__ __forceinline__ void raise_timeout(int* status, volatile int* abort_f
   *abort_flag = 1;
 }
 
-// A-operand (weight-side) loads for one K block: 128 rows starting at the
-// feature block of ``row_base`` (a weight matrix or a LoRA B factor).
+// Weight-side (A operand) loads of one K block: 128 rows of the feature block.
+// gate_up: the map views w13 so that one box (or four, see the host code)
+// brings gate rows 64 fb + 16q + (0..15) to smem rows 32q + (0..15) and the
+// matching up rows to smem rows 32q + 16 + (0..15), q = 0..3.
 template <int MODE>
-__device__ __forceinline__ void load_a_block(uint8_t* sA, const CUtensorMap* map, uint64_t* bar,
-                                             int kc, int64_t row_base, int fb, int n_feat,
-                                             uint64_t pol) {
+__device__ __forceinline__ void load_weight_block(uint8_t* sA, const CUtensorMap* map,
+                                                  uint64_t* bar, int kc, int e, int fb,
+                                                  int rows_per_expert, int gu_single_box,
+                                                  uint64_t pol) {
+  if (MODE == kGateUp) {
+    if (gu_single_box) {
+      // map dims {H, 16 rows, 2 halves, I/16 groups, E}
+      tma_load_5d(sA, map, bar, kc, 0, 0, fb * 4, e, pol);
+    } else {
+      // map dims {H, I, 2E}, box {64, 16, 2}
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tma_load_3d(sA + q * 4096, map, bar, kc, fb * 64 + q * 16, 2 * e, pol);
+    }
+  } else {
+    tma_load_2d(sA, map, bar, kc, e * rows_per_expert + fb * 128, pol);
+  }
+}
+
+// LoRA B-factor (A operand of the expand) loads: same row arrangement, from
+// the 2-D map over all factor rows (box {64, 16} for gate_up, {64, 128} down).
+template <int MODE>
+__device__ __forceinline__ void load_lora_b_block(uint8_t* sA, const CUtensorMap* map,
+                                                  uint64_t* bar, int kc, int64_t row_base, int fb,
+                                                  int n_feat, uint64_t pol) {
   if (MODE == kGateUp) {
 #pragma unroll
     for (int bx = 0; bx < 8; ++bx) {
@@ -128,7 +155,7 @@ __device__ __forceinline__ void load_a_block(uint8_t* sA, const CUtensorMap* map
 }
 
 template <int BN, int MODE>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                        const __grid_constant__ CUtensorMap tm_lb, const __grid_constant__ CUtensorMap tm_lu,
                        const GemmParams p) {
@@ -214,14 +241,13 @@ __global__ void __launch_bounds__(192, 1)
             uint8_t* sB = sA + C::kABytes;
             mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
             if (b < nk) {
-              load_a_block<MODE>(sA, &tm_w, &full[stage], b * 64,
-                                 static_cast<int64_t>(wk.e) * p.rows_per_expert, wk.fb, p.n_feat,
-                                 pol_w);
+              load_weight_block<MODE>(sA, &tm_w, &full[stage], b * 64, wk.e, wk.fb,
+                                      p.rows_per_expert, p.gu_single_box, pol_w);
               tma_load_2d(sB, &tm_x, &full[stage], b * 64, wk.row0, pol_x);
             } else {
               const int64_t frow = static_cast<int64_t>(adapter) * p.lb_row_stride_adapter +
                                    static_cast<int64_t>(wk.e) * p.lb_row_stride_expert;
-              load_a_block<MODE>(sA, &tm_lb, &full[stage], j * 64, frow, wk.fb, p.n_feat, pol_x);
+              load_lora_b_block<MODE>(sA, &tm_lb, &full[stage], j * 64, frow, wk.fb, p.n_feat, pol_x);
               tma_load_2d(sB, &tm_lu, &full[stage], adapter * p.rank + j * 64, wk.row0, pol_x);
             }
             armed |= 1u << stage;
@@ -369,6 +395,16 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+int gemm_ctas_per_sm(int bn) {
+  switch (bn) {
+    case 16: return GemmCfg<16>::kCtasPerSm;
+    case 32: return GemmCfg<32>::kCtasPerSm;
+    case 64: return GemmCfg<64>::kCtasPerSm;
+    case 128: return GemmCfg<128>::kCtasPerSm;
+    default: return GemmCfg<256>::kCtasPerSm;
   }
 }
 

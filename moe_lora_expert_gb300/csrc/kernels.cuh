@@ -73,6 +73,7 @@ struct GemmParams {
   int E;
   int K;                          // main reduction length (H or I)
   int rows_per_expert;            // rows of the weight per expert (2I or H)
+  int gu_single_box;              // gate_up weight map is the 5-D one-box view
   int n_feat;                     // output features (I for gate_up, H for down)
   int feat_blocks;                // feature blocks per expert
   int num_adapters;               // 0 = no LoRA
@@ -85,6 +86,7 @@ struct GemmParams {
 };
 enum GemmMode { kGateUp = 0, kDown = 1 };
 int gemm_stage_count(int bn);
+int gemm_ctas_per_sm(int bn);
 size_t gemm_smem_bytes(int bn);
 cudaError_t launch_expert_gemm(int mode, int bn, const CUtensorMap& tm_w, const CUtensorMap& tm_x,
                                const CUtensorMap& tm_lb, const CUtensorMap& tm_lu,
