@@ -339,7 +339,10 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
 
   uint8_t* ws = static_cast<uint8_t*>(a->workspace);
   int* status = reinterpret_cast<int*>(ws + pl.status);
-  if (cudaMemsetAsync(status, 0, 16, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  // The one-CTA permute clears the status word itself; otherwise clear it here.
+  const bool small_permute = moe::small_permute_fits(static_cast<int>(n), E);
+  const bool fuse_route = small_permute && T <= 128;
+  if (!small_permute && cudaMemsetAsync(status, 0, 16, stream) != cudaSuccess) return MOE_ERR_CUDA;
 
   int32_t* topk_ids = a->topk_ids_out ? a->topk_ids_out : reinterpret_cast<int32_t*>(ws + pl.topk_ids);
   float* topk_w = a->topk_w_out ? a->topk_w_out : reinterpret_cast<float*>(ws + pl.topk_w);
@@ -393,48 +396,74 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   if (!enc) return MOE_ERR_CUDA;
 
   if (!mark()) return MOE_ERR_CUDA;
-  // 1. routing
-  if (moe::launch_route_topk(a->router_logits, T, E, K, topk_ids, topk_w, stream) != cudaSuccess)
+  // 1-2. routing and permutation (one CTA when it fits)
+  moe::FusedPermuteParams fp{};
+  fp.logits = fuse_route ? a->router_logits : nullptr;
+  fp.topk_ids = topk_ids;
+  fp.topk_w = topk_w;
+  fp.T = T;
+  fp.top_k = K;
+  fp.E = E;
+  fp.mapping = lora ? a->token_lora_mapping : nullptr;
+  fp.num_adapters = A;
+  fp.row_adapter = row_adapter;
+  fp.expert_offsets = offsets;
+  fp.e2p = e2p;
+  fp.p2e = p2e;
+  fp.tile_start = tile_start;
+  fp.status = status;
+  if (!fuse_route &&
+      moe::launch_route_topk(a->router_logits, T, E, K, topk_ids, topk_w, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!mark()) return MOE_ERR_CUDA;
-  // 2. permute + gather
-  PermuteParams pp{};
-  pp.topk_ids = topk_ids;
-  pp.n = static_cast<int>(n);
-  pp.top_k = K;
-  pp.E = E;
-  pp.H = H;
-  pp.hidden = static_cast<const __nv_bfloat16*>(a->hidden);
-  pp.permuted = xp;
-  pp.mapping = lora ? a->token_lora_mapping : nullptr;
-  pp.num_adapters = A;
-  pp.row_adapter = row_adapter;
-  pp.expert_offsets = offsets;
-  pp.e2p = e2p;
-  pp.p2e = p2e;
-  pp.chunk_counts = chunk_counts;
-  pp.tile_start = tile_start;
-  pp.status = status;
-  if (moe::launch_permute(pp, stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (!mark()) return MOE_ERR_CUDA;
-  // 3. gate_up LoRA shrink: U = s * A_gu x (one-hot per adapter)
-  ShrinkParams sp{};
-  if (lora) {
-    sp.X = xp;
-    sp.K = H;
-    sp.A = static_cast<const __nv_bfloat16*>(a->gate_up.A);
-    sp.a_stride_adapter = a->gate_up.a_stride_adapter;
-    sp.a_stride_expert = a->gate_up.a_stride_expert;
-    sp.row_adapter = row_adapter;
-    sp.expert_offsets = offsets;
-    sp.tile_start16 = tile_start + moe::tile_width_index(16) * (E + 1);
-    sp.E = E;
-    sp.num_adapters = A;
-    sp.rank = r;
-    sp.scaling = a->scaling;
-    sp.U = U;
-    if (moe::launch_lora_shrink(sp, static_cast<int>(n), stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (small_permute) {
+    if (moe::launch_small_permute(fp, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+    PermuteParams pp{};
+    pp.topk_ids = topk_ids;
+    pp.n = static_cast<int>(n);
+    pp.top_k = K;
+    pp.E = E;
+    pp.H = H;
+    pp.hidden = nullptr;  // rows are gathered by the next kernel
+    pp.permuted = nullptr;
+    pp.mapping = fp.mapping;
+    pp.num_adapters = A;
+    pp.row_adapter = row_adapter;
+    pp.expert_offsets = offsets;
+    pp.e2p = e2p;
+    pp.p2e = p2e;
+    pp.chunk_counts = chunk_counts;
+    pp.tile_start = tile_start;
+    pp.status = status;
+    if (moe::launch_permute(pp, stream) != cudaSuccess) return MOE_ERR_CUDA;
   }
+  if (!mark()) return MOE_ERR_CUDA;
+  // 3. row gather + gate_up LoRA shrink: xp = hidden[t(p)], U = s * A_gu x
+  //    (one-hot per adapter).  Few tiles (decode): one phase per CTA; many
+  //    tiles: smaller phases so that several CTAs share an SM.
+  const size_t shrink_budget = n <= 16 * static_cast<int64_t>(sms) ? 200 * 1024 : 72 * 1024;
+  ShrinkParams sp{};
+  sp.X = static_cast<const __nv_bfloat16*>(a->hidden);
+  sp.p2e = p2e;
+  sp.top_k = K;
+  sp.K = H;
+  sp.gathered = xp;
+  sp.A = lora ? static_cast<const __nv_bfloat16*>(a->gate_up.A) : nullptr;
+  sp.a_stride_adapter = lora ? a->gate_up.a_stride_adapter : 0;
+  sp.a_stride_expert = lora ? a->gate_up.a_stride_expert : 0;
+  sp.row_adapter = row_adapter;
+  sp.expert_offsets = offsets;
+  sp.tile_start16 = tile_start + moe::tile_width_index(16) * (E + 1);
+  sp.E = E;
+  sp.num_adapters = A;
+  sp.rank = r;
+  sp.scaling = a->scaling;
+  sp.U = lora ? U : nullptr;
+  sp.status = status;
+  sp.timeout_ns = timeout_ns;
+  sp.kc = moe::shrink_chunk(H, r, shrink_budget);
+  if (moe::launch_gather_shrink(sp, static_cast<int>(n), stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (!mark()) return MOE_ERR_CUDA;
   // 4. gate_up GEMM + LoRA expand + SwiGLU -> h
   GemmParams gp{};
@@ -462,12 +491,15 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   // 5. down LoRA shrink: V = s * A_dn h
   if (lora) {
     sp.X = h;
+    sp.p2e = nullptr;
     sp.K = I;
+    sp.gathered = nullptr;
     sp.A = static_cast<const __nv_bfloat16*>(a->down.A);
     sp.a_stride_adapter = a->down.a_stride_adapter;
     sp.a_stride_expert = a->down.a_stride_expert;
     sp.U = V;
-    if (moe::launch_lora_shrink(sp, static_cast<int>(n), stream) != cudaSuccess) return MOE_ERR_CUDA;
+    sp.kc = moe::shrink_chunk(I, r, shrink_budget);
+    if (moe::launch_gather_shrink(sp, static_cast<int>(n), stream) != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (!mark()) return MOE_ERR_CUDA;
   // 6. down GEMM + LoRA expand -> y

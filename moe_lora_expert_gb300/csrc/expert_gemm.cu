@@ -204,10 +204,14 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
+  // Everything above overlaps the previous kernel's tail; the routing tables
+  // it wrote are read only after the wait.
+  pdl_wait();
   for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
     s_off[i] = p.expert_offsets[i];
     s_ts[i] = p.tile_start[i];
   }
+  pdl_launch_dependents();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -436,8 +440,7 @@ static cudaError_t launch_one(const CUtensorMap& tm_w, const CUtensorMap& tm_x,
   const int smem = GemmCfg<BN>::kSmemBytes;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  kern<<<grid, 192, smem, s>>>(tm_w, tm_x, tm_lb, tm_lu, p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(192), smem, s, tm_w, tm_x, tm_lb, tm_lu, p);
 }
 
 cudaError_t launch_expert_gemm(int mode, int bn, const CUtensorMap& tm_w, const CUtensorMap& tm_x,

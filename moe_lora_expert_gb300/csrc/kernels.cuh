@@ -3,10 +3,30 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace moe {
+
+// Launch with programmatic stream serialization: the kernel may start while
+// its predecessor drains, and must call griddepcontrol.wait (pdl_wait)
+// before touching anything the predecessor writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
 
 // Token-tile widths for which the permute scan writes per-expert tile
 // prefixes: tile_start[bn_index][e] = sum_{e' < e} ceil(n_e' / bn).
@@ -43,13 +63,18 @@ constexpr int kPermuteChunk = 1024;
 size_t permute_scratch_bytes(int n, int E);
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s);
 
-// ------------------------------------------------------------ LoRA shrink
-// U[p, a*r + i] = bf16(scaling * sum_k A[a, e(p)][i, k] * X[p, k]) for the
-// row's own adapter a, and 0 in every other column of the row.
+// ------------------------------------------------- gather + LoRA shrink
+// Per 16-row tile of one expert: copy the source rows (gathered[p] = X[src(p)])
+// and/or U[p, a*r + i] = bf16(scaling * sum_k A[a, e(p)][i, k] * X[src(p), k])
+// for the row's own adapter a, 0 in every other column of the row.
 struct ShrinkParams {
-  const __nv_bfloat16* X;       // [n, K]
+  const __nv_bfloat16* X;       // source rows [*, K]
+  const int32_t* p2e;           // src(p) = p2e[p] / top_k; null: src(p) = p
+  int top_k;
   int K;
-  const __nv_bfloat16* A;       // factor base
+  int kc;                       // K elements staged per phase
+  __nv_bfloat16* gathered;      // [n, K] row copy, or null
+  const __nv_bfloat16* A;       // factor base (ignored when rank == 0 or U == null)
   int64_t a_stride_adapter;     // elements
   int64_t a_stride_expert;      // elements (0 = shared)
   const int32_t* row_adapter;   // [n]
@@ -57,11 +82,32 @@ struct ShrinkParams {
   const int32_t* tile_start16;  // [E + 1] prefix of ceil(n_e / 16)
   int E;
   int num_adapters;
-  int rank;
+  int rank;                     // 0: gather only
   float scaling;
-  __nv_bfloat16* U;             // [n, num_adapters * rank]
+  __nv_bfloat16* U;             // [n, num_adapters * rank], or null
+  int* status;
+  uint64_t timeout_ns;
 };
-cudaError_t launch_lora_shrink(const ShrinkParams& p, int n_rows, cudaStream_t s);
+int shrink_chunk(int K, int rank, size_t smem_budget);
+cudaError_t launch_gather_shrink(const ShrinkParams& p, int n_rows, cudaStream_t s);
+
+// ------------------------------------------------- one-CTA permute (fused)
+struct FusedPermuteParams {
+  const float* logits;          // [T, E]: route first; null: read topk_ids
+  int32_t* topk_ids;            // [T*k] written (routing) or read
+  float* topk_w;                // [T*k] written when routing
+  int T, top_k, E;
+  const int32_t* mapping;       // [T] or null
+  int num_adapters;
+  int32_t* row_adapter;         // [n] or null
+  int32_t* expert_offsets;      // [E + 1]
+  int32_t* e2p;                 // [n]
+  int32_t* p2e;                 // [n]
+  int32_t* tile_start;          // [kNumTileWidths, E + 1] or null
+  int* status;                  // cleared by the kernel
+};
+bool small_permute_fits(int n, int E);
+cudaError_t launch_small_permute(const FusedPermuteParams& p, cudaStream_t s);
 
 // ------------------------------------------------------- expert GEMMs
 // Swap-AB grouped GEMM: D[feature, token] = W_e[feature, :] . X[token, :]

@@ -32,15 +32,11 @@ __device__ __forceinline__ float float_from_order_bits(uint32_t o) {
   return __uint_as_float(b);
 }
 
+// Routes one token with a whole warp; lane j < k ends with slot j's expert
+// id and renormalised weight.
 template <int EPL>
-__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
-                                                         int E, int k, int32_t* __restrict__ ids,
-                                                         float* __restrict__ w) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const float* row = logits + static_cast<size_t>(t) * E;
-
+__device__ __forceinline__ void route_token(const float* __restrict__ row, int E, int k, int lane,
+                                            int* out_id, float* out_w) {
   uint64_t key[EPL];
 #pragma unroll
   for (int s = 0; s < EPL; ++s) {
@@ -77,9 +73,23 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   float sum = ex;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+  *out_id = my_id;
+  *out_w = ex / sum;
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
+                                                         int E, int k, int32_t* __restrict__ ids,
+                                                         float* __restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  int id;
+  float wt;
+  route_token<EPL>(logits + static_cast<size_t>(t) * E, E, k, lane, &id, &wt);
   if (lane < k) {
-    ids[static_cast<size_t>(t) * k + lane] = my_id;
-    w[static_cast<size_t>(t) * k + lane] = ex / sum;
+    ids[static_cast<size_t>(t) * k + lane] = id;
+    w[static_cast<size_t>(t) * k + lane] = wt;
   }
 }
 
@@ -248,6 +258,152 @@ cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// ------------------------------------------------- one-CTA permute (fused)
+// For n = T*k slots small enough that the whole counting sort fits in one
+// CTA's shared memory.  Optionally routes the tokens first (one warp per
+// token).  Clears the device status word, then:
+//   pass 1: warp w takes slots [w*seg, (w+1)*seg) in order and gives each
+//           slot its stable rank among earlier slots of the same expert in
+//           the segment (match_any per 32 slots, per-warp expert counters);
+//   pass 2: per expert, an exclusive scan of the 32 warp counters; a block
+//           scan of the expert totals gives the expert offsets and the tile
+//           prefixes;
+//   pass 3: permuted index = offset[e] + warp base + rank; inverse map and
+//           the row's adapter.
+template <int EPL>
+__global__ void __launch_bounds__(1024) small_permute_kernel(const FusedPermuteParams p) {
+  extern __shared__ int4 small_smem[];
+  const int n = p.T * p.top_k, E = p.E, k = p.top_k;
+  const int n2 = (n + 1) & ~1;
+  int16_t* s_ids = reinterpret_cast<int16_t*>(small_smem);
+  int16_t* s_local = s_ids + n2;
+  int* s_cnt = reinterpret_cast<int*>(s_local + n2);
+  int* s_off = s_cnt + 32 * E;
+  __shared__ int warp_sums[32];
+  __shared__ int s_total;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  pdl_wait();
+  if (tid == 0) p.status[0] = 0;
+  for (int i = tid; i < 32 * E; i += blockDim.x) s_cnt[i] = 0;
+  __syncthreads();
+  if (p.logits != nullptr) {
+    for (int t = warp; t < p.T; t += 32) {
+      int id;
+      float wt;
+      route_token<EPL>(p.logits + static_cast<size_t>(t) * E, E, k, lane, &id, &wt);
+      if (lane < k) {
+        p.topk_ids[t * k + lane] = id;
+        p.topk_w[t * k + lane] = wt;
+        s_ids[t * k + lane] = static_cast<int16_t>(id);
+      }
+    }
+  } else {
+    for (int x = tid; x < n; x += blockDim.x)
+      s_ids[x] = static_cast<int16_t>(checked_id(p.topk_ids[x], E, p.status, true));
+  }
+  __syncthreads();
+
+  const int seg = (n + 31) / 32;
+  const int x_begin = warp * seg, x_end = min(x_begin + seg, n);
+  int* cnt = s_cnt + warp * E;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int x0 = x_begin; x0 < x_end; x0 += 32) {
+    const int x = x0 + lane;
+    const bool valid = x < x_end;
+    const int id = valid ? s_ids[x] : -1;
+    const bool routed = id >= 0;
+    const unsigned grp = __match_any_sync(kFull, routed ? id : -2);
+    const int rank = __popc(grp & lt_mask);
+    const int prev = routed ? cnt[id] : 0;
+    __syncwarp();
+    if (routed && rank == 0) cnt[id] = prev + __popc(grp);
+    __syncwarp();
+    if (valid) s_local[x] = static_cast<int16_t>(routed ? prev + rank : -1);
+  }
+  __syncthreads();
+
+  int total = 0;
+  if (tid < E) {
+    for (int w = 0; w < 32; ++w) {
+      const int v = s_cnt[w * E + tid];
+      s_cnt[w * E + tid] = total;
+      total += v;
+    }
+  }
+  const int off = block_exclusive_scan_1024(tid < E ? total : 0, warp_sums, &s_total);
+  if (tid < E) {
+    s_off[tid] = off;
+    p.expert_offsets[tid] = off;
+  }
+  if (tid == 0) {
+    s_off[E] = s_total;
+    p.expert_offsets[E] = s_total;
+  }
+  if (p.tile_start != nullptr) {
+    for (int wi = 0; wi < kNumTileWidths; ++wi) {
+      const int bn = tile_width_of(wi);
+      const int tiles = tid < E ? (total + bn - 1) / bn : 0;
+      const int ts = block_exclusive_scan_1024(tiles, warp_sums, &s_total);
+      if (tid < E) p.tile_start[wi * (E + 1) + tid] = ts;
+      if (tid == 0) p.tile_start[wi * (E + 1) + E] = s_total;
+    }
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+
+  for (int x = tid; x < n; x += blockDim.x) {
+    const int id = s_ids[x];
+    int pidx = -1;
+    if (id >= 0) {
+      pidx = s_off[id] + s_cnt[(x / seg) * E + id] + s_local[x];
+      p.p2e[pidx] = x;
+      if (p.row_adapter != nullptr) {
+        int a = -1;
+        if (p.num_adapters > 0 && p.mapping != nullptr) {
+          a = p.mapping[x / k];
+          if (a < -1 || a >= p.num_adapters) {
+            set_status(p.status, MOE_ERR_BAD_MAPPING);
+            a = -1;
+          }
+        }
+        p.row_adapter[pidx] = a;
+      }
+    }
+    p.e2p[x] = pidx;
+  }
+  for (int x = s_off[E] + tid; x < n; x += blockDim.x) p.p2e[x] = -1;
+}
+
+size_t small_permute_smem(int n, int E) {
+  const size_t n2 = (static_cast<size_t>(n) + 1) & ~static_cast<size_t>(1);
+  return n2 * 2 * 2 + static_cast<size_t>(32) * E * 4 + (static_cast<size_t>(E) + 1) * 4;
+}
+
+bool small_permute_fits(int n, int E) {
+  return n <= 8192 && small_permute_smem(n, E) <= 200 * 1024;
+}
+
+cudaError_t launch_small_permute(const FusedPermuteParams& p, cudaStream_t s) {
+  const int n = p.T * p.top_k;
+  const size_t smem = small_permute_smem(n, p.E);
+  const int epl = (p.E + 31) / 32;
+#define MOE_SMALL_CASE(V)                                                                         \
+  {                                                                                               \
+    cudaError_t err = cudaFuncSetAttribute(small_permute_kernel<V>,                               \
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+    if (err != cudaSuccess) return err;                                                           \
+    return launch_pdl(small_permute_kernel<V>, dim3(1), dim3(1024), smem, s, p);                  \
+  }
+  if (p.logits == nullptr || epl <= 1) MOE_SMALL_CASE(1)
+  if (epl <= 2) MOE_SMALL_CASE(2)
+  if (epl <= 4) MOE_SMALL_CASE(4)
+  if (epl <= 8) MOE_SMALL_CASE(8)
+  if (epl <= 16) MOE_SMALL_CASE(16)
+  MOE_SMALL_CASE(32)
+#undef MOE_SMALL_CASE
+}
+
 // ---------------------------------------------------------------- finalize
 // out[t, :] = sum_j w[t, j] * y[e2p[t*k + j], :], summed in slot order in
 // float32, rounded to bf16 (nearest even).  One thread per 8 columns.
@@ -257,6 +413,8 @@ __global__ void __launch_bounds__(256) finalize_kernel(const __nv_bfloat16* __re
                                                        __nv_bfloat16* __restrict__ out) {
   const int t = blockIdx.x;
   const int c8 = blockIdx.y * blockDim.x + threadIdx.x;
+  pdl_wait();
+  pdl_launch_dependents();
   if (c8 * 8 >= H) return;
   float acc[8];
 #pragma unroll
@@ -285,8 +443,7 @@ cudaError_t launch_finalize(const __nv_bfloat16* y, const int32_t* e2p, const fl
                             int top_k, int H, __nv_bfloat16* out, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const dim3 grid(T, (H / 8 + 255) / 256);
-  finalize_kernel<<<grid, 256, 0, s>>>(y, e2p, w, top_k, H, out);
-  return cudaGetLastError();
+  return launch_pdl(finalize_kernel, grid, dim3(256), 0, s, y, e2p, w, top_k, H, out);
 }
 
 }  // namespace moe
