@@ -15,6 +15,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -362,6 +363,13 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(ws + pl.act);
 
   const int bn = a->tile_n ? a->tile_n : auto_tile_n(static_cast<int>(n), E);
+  // CTAs per cluster sharing a token tile (TMA multicast).  MOE_LORA_CLUSTER
+  // overrides the default for tuning (1, 2 or 4; 4 only with 256-wide tiles).
+  int cl = moe::gemm_cluster_size(bn);
+  if (const char* env = std::getenv("MOE_LORA_CLUSTER")) {
+    const int v = std::atoi(env);
+    if (v == 1 || (v == 2 && bn >= 128) || (v == 4 && bn == 256)) cl = v;
+  }
   const int sms = num_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
   const uint64_t timeout_ns =
@@ -372,8 +380,8 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   bool gu_single_box = false;
   bool enc = encode_w13(&tm_w13, a->w13, H, I, E, &gu_single_box) &&
              encode_2d(&tm_w2, a->w2, I, static_cast<uint64_t>(E) * H, I * 2ull, 64, 128) &&
-             encode_2d(&tm_xp, xp, H, n, H * 2ull, 64, bn) &&
-             encode_2d(&tm_h, h, I, n, I * 2ull, 64, bn);
+             encode_2d(&tm_xp, xp, H, n, H * 2ull, 64, bn / cl) &&
+             encode_2d(&tm_h, h, I, n, I * 2ull, 64, bn / cl);
   int64_t gu_rs_a = 0, gu_rs_e = 0, dn_rs_a = 0, dn_rs_e = 0;
   if (enc && lora) {
     gu_rs_a = a->gate_up.b_stride_adapter / r;
@@ -385,8 +393,8 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
     if (gu_rows >= (1ull << 31) || dn_rows >= (1ull << 31)) return MOE_ERR_UNSUPPORTED;
     enc = encode_2d(&tm_bgu, a->gate_up.B, r, gu_rows, r * 2ull, 64, 16) &&
           encode_2d(&tm_bdn, a->down.B, r, dn_rows, r * 2ull, 64, 128) &&
-          encode_2d(&tm_u, U, static_cast<uint64_t>(A) * r, n, A * r * 2ull, 64, bn) &&
-          encode_2d(&tm_v, V, static_cast<uint64_t>(A) * r, n, A * r * 2ull, 64, bn);
+          encode_2d(&tm_u, U, static_cast<uint64_t>(A) * r, n, A * r * 2ull, 64, bn / cl) &&
+          encode_2d(&tm_v, V, static_cast<uint64_t>(A) * r, n, A * r * 2ull, 64, bn / cl);
   } else {
     tm_bgu = tm_w13;
     tm_bdn = tm_w2;
@@ -483,7 +491,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.out = h;
   gp.status = status;
   gp.timeout_ns = timeout_ns;
-  if (moe::launch_expert_gemm(moe::kGateUp, bn, tm_w13, tm_xp, tm_bgu, tm_u, gp,
+  if (moe::launch_expert_gemm(moe::kGateUp, bn, cl, tm_w13, tm_xp, tm_bgu, tm_u, gp,
                               sms * moe::gemm_ctas_per_sm(bn), stream) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
@@ -510,7 +518,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.lb_row_stride_adapter = dn_rs_a;
   gp.lb_row_stride_expert = dn_rs_e;
   gp.out = y;
-  if (moe::launch_expert_gemm(moe::kDown, bn, tm_w2, tm_h, tm_bdn, tm_v, gp,
+  if (moe::launch_expert_gemm(moe::kDown, bn, cl, tm_w2, tm_h, tm_bdn, tm_v, gp,
                               sms * moe::gemm_ctas_per_sm(bn), stream) !=
       cudaSuccess)
     return MOE_ERR_CUDA;

@@ -64,12 +64,15 @@ struct Work {
   int e, fb, row0, nrows;
 };
 
+// Work unit u = (token tile, feature-block group).  Each CTA of a cluster of
+// CL takes feature block group * CL + its rank, so the CTAs of a cluster work
+// on the same token tile at the same time and can share its loads.
 template <int BN>
-__device__ __forceinline__ Work decode_work(int w, const int* s_off, const int* s_ts, int E,
-                                            int FB) {
+__device__ __forceinline__ Work decode_work(int u, int crank, int CL, const int* s_off,
+                                            const int* s_ts, int E, int FBg) {
   Work wk;
-  const int tile = w / FB;
-  wk.fb = w - tile * FB;
+  const int tile = u / FBg;
+  wk.fb = (u - tile * FBg) * CL + crank;
   int lo = 0, hi = E - 1;
   while (lo < hi) {  // largest e with s_ts[e] <= tile
     const int mid = (lo + hi + 1) >> 1;
@@ -154,7 +157,7 @@ __device__ __forceinline__ void load_lora_b_block(uint8_t* sA, const CUtensorMap
   }
 }
 
-template <int BN, int MODE>
+template <int BN, int MODE, int CL>
 __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                        const __grid_constant__ CUtensorMap tm_lb, const __grid_constant__ CUtensorMap tm_lu,
@@ -182,7 +185,7 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], CL);  // every CTA of the cluster releases the stage
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accf[b], 1);
@@ -215,8 +218,16 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  // Peers multicast into this CTA's barriers: all of them must be initialised.
+  if (CL > 1) cluster_sync_all();
   const uint32_t tmem_base = *tmem_slot;
-  const int total_work = s_ts[p.E] * p.feat_blocks;
+  const int crank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int unit0 = CL > 1 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int unit_step = CL > 1 ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
+  const int FBg = (p.feat_blocks + CL - 1) / CL;
+  const int total_work = s_ts[p.E] * FBg;
+  constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CL) - 1u);
+  constexpr int kPieceRows = BN / CL;              // token rows each CTA loads and multicasts
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
@@ -225,9 +236,9 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
     uint32_t stage = 0, phase = 0;
     uint32_t armed = 0, armed_parity = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total_work && ok; w += gridDim.x) {
+    for (int w = unit0; w < total_work && ok; w += unit_step) {
       if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
-      const Work wk = decode_work<BN>(w, s_off, s_ts, p.E, p.feat_blocks);
+      const Work wk = decode_work<BN>(w, crank, CL, s_off, s_ts, p.E, FBg);
       uint64_t amask = use_lora ? tile_adapter_mask(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
       const int nblocks = nk + __popcll(amask) * lkb;
       int adapter = -1, j = 0;
@@ -247,12 +258,21 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
             if (b < nk) {
               load_weight_block<MODE>(sA, &tm_w, &full[stage], b * 64, wk.e, wk.fb,
                                       p.rows_per_expert, p.gu_single_box, pol_w);
-              tma_load_2d(sB, &tm_x, &full[stage], b * 64, wk.row0, pol_x);
+              if (CL > 1)
+                tma_load_2d_multicast(sB + crank * kPieceRows * 128, &tm_x, &full[stage], b * 64,
+                                      wk.row0 + crank * kPieceRows, kClusterMask, pol_x);
+              else
+                tma_load_2d(sB, &tm_x, &full[stage], b * 64, wk.row0, pol_x);
             } else {
               const int64_t frow = static_cast<int64_t>(adapter) * p.lb_row_stride_adapter +
                                    static_cast<int64_t>(wk.e) * p.lb_row_stride_expert;
               load_lora_b_block<MODE>(sA, &tm_lb, &full[stage], j * 64, frow, wk.fb, p.n_feat, pol_x);
-              tma_load_2d(sB, &tm_lu, &full[stage], adapter * p.rank + j * 64, wk.row0, pol_x);
+              if (CL > 1)
+                tma_load_2d_multicast(sB + crank * kPieceRows * 128, &tm_lu, &full[stage],
+                                      adapter * p.rank + j * 64, wk.row0 + crank * kPieceRows,
+                                      kClusterMask, pol_x);
+              else
+                tma_load_2d(sB, &tm_lu, &full[stage], adapter * p.rank + j * 64, wk.row0, pol_x);
             }
             armed |= 1u << stage;
             armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
@@ -281,9 +301,9 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
     // -------------------------------------------------------- MMA issuer
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total_work && ok; w += gridDim.x) {
+    for (int w = unit0; w < total_work && ok; w += unit_step) {
       if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
-      const Work wk = decode_work<BN>(w, s_off, s_ts, p.E, p.feat_blocks);
+      const Work wk = decode_work<BN>(w, crank, CL, s_off, s_ts, p.E, FBg);
       const uint64_t amask =
           use_lora ? tile_adapter_mask(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
       const int nblocks = nk + __popcll(amask) * lkb;
@@ -314,7 +334,8 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
             for (int ks = 0; ks < ksteps; ++ks)
               tc_mma_bf16(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc,
                           (b > 0 || ks > 0) ? 1u : 0u);
-            tc_commit(&empty[stage]);
+            if (CL > 1) tc_commit_multicast(&empty[stage], kClusterMask);
+            else tc_commit(&empty[stage]);
           } else {
             raise_timeout(p.status, abort_flag);
           }
@@ -342,9 +363,9 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     uint32_t acc = 0, acc_phase = 0;
-    for (int w = blockIdx.x; w < total_work; w += gridDim.x) {
+    for (int w = unit0; w < total_work; w += unit_step) {
       if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
-      const Work wk = decode_work<BN>(w, s_off, s_ts, p.E, p.feat_blocks);
+      const Work wk = decode_work<BN>(w, crank, CL, s_off, s_ts, p.E, FBg);
       const int ncols = ((wk.nrows + 15) / 16) * 16;
       bool ok = true;
       if (lane == 0) {
@@ -396,6 +417,9 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
 
   tc_fence_before_sync();
   __syncthreads();
+  // No CTA leaves while a peer may still signal its barriers or write its
+  // shared memory.
+  if (CL > 1) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, C::kTmemCols);
@@ -432,33 +456,65 @@ size_t gemm_smem_bytes(int bn) {
   }
 }
 
-template <int BN, int MODE>
+template <int BN, int MODE, int CL>
 static cudaError_t launch_one(const CUtensorMap& tm_w, const CUtensorMap& tm_x,
                               const CUtensorMap& tm_lb, const CUtensorMap& tm_lu,
                               const GemmParams& p, int grid, cudaStream_t s) {
-  auto kern = expert_gemm_kernel<BN, MODE>;
+  auto kern = expert_gemm_kernel<BN, MODE, CL>;
   const int smem = GemmCfg<BN>::kSmemBytes;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  return launch_pdl(kern, dim3(grid), dim3(192), smem, s, tm_w, tm_x, tm_lb, tm_lu, p);
+  if (CL == 1) return launch_pdl(kern, dim3(grid), dim3(192), smem, s, tm_w, tm_x, tm_lb, tm_lu, p);
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // The persistent grid is as many clusters as can be resident at once.
+  cfg.gridDim = dim3(CL * 64);
+  int max_clusters = 0;
+  err = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+  if (err != cudaSuccess) return err;
+  int clusters = grid / CL;
+  if (max_clusters > 0 && clusters > max_clusters) clusters = max_clusters;
+  if (clusters < 1) clusters = 1;
+  cfg.gridDim = dim3(clusters * CL);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, tm_w, tm_x, tm_lb, tm_lu, p);
 }
 
-cudaError_t launch_expert_gemm(int mode, int bn, const CUtensorMap& tm_w, const CUtensorMap& tm_x,
-                               const CUtensorMap& tm_lb, const CUtensorMap& tm_lu,
-                               const GemmParams& p, int grid, cudaStream_t s) {
-#define MOE_GEMM_CASE(BNV)                                                          \
-  case BNV:                                                                         \
-    return mode == kGateUp ? launch_one<BNV, kGateUp>(tm_w, tm_x, tm_lb, tm_lu, p, grid, s) \
-                           : launch_one<BNV, kDown>(tm_w, tm_x, tm_lb, tm_lu, p, grid, s);
-  switch (bn) {
-    MOE_GEMM_CASE(16)
-    MOE_GEMM_CASE(32)
-    MOE_GEMM_CASE(64)
-    MOE_GEMM_CASE(128)
-    MOE_GEMM_CASE(256)
-    default: return cudaErrorInvalidValue;
-  }
+// Multicast of the token tile measured no faster than one CTA per tile on
+// prefill_T4096 (646.6 vs 646.0 us with 2; 686.8 with 4), so it is off by
+// default and kept as a tuning option.
+int gemm_cluster_size(int) { return 1; }
+
+cudaError_t launch_expert_gemm(int mode, int bn, int cl, const CUtensorMap& tm_w,
+                               const CUtensorMap& tm_x, const CUtensorMap& tm_lb,
+                               const CUtensorMap& tm_lu, const GemmParams& p, int grid,
+                               cudaStream_t s) {
+#define MOE_GEMM_CASE(BNV, CLV)                                                              \
+  if (bn == BNV && cl == CLV)                                                                \
+    return mode == kGateUp ? launch_one<BNV, kGateUp, CLV>(tm_w, tm_x, tm_lb, tm_lu, p, grid, s) \
+                           : launch_one<BNV, kDown, CLV>(tm_w, tm_x, tm_lb, tm_lu, p, grid, s);
+  MOE_GEMM_CASE(16, 1)
+  MOE_GEMM_CASE(32, 1)
+  MOE_GEMM_CASE(64, 1)
+  MOE_GEMM_CASE(128, 1)
+  MOE_GEMM_CASE(256, 1)
+  MOE_GEMM_CASE(128, 2)
+  MOE_GEMM_CASE(256, 2)
+  MOE_GEMM_CASE(256, 4)
 #undef MOE_GEMM_CASE
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace moe

@@ -134,9 +134,13 @@ enum GemmMode { kGateUp = 0, kDown = 1 };
 int gemm_stage_count(int bn);
 int gemm_ctas_per_sm(int bn);
 size_t gemm_smem_bytes(int bn);
-cudaError_t launch_expert_gemm(int mode, int bn, const CUtensorMap& tm_w, const CUtensorMap& tm_x,
-                               const CUtensorMap& tm_lb, const CUtensorMap& tm_lu,
-                               const GemmParams& p, int grid, cudaStream_t s);
+// cl: CTAs per cluster along the feature blocks (1, or 2/4 for wide token
+// tiles): the cluster's CTAs share each token tile through TMA multicast.
+int gemm_cluster_size(int bn);
+cudaError_t launch_expert_gemm(int mode, int bn, int cl, const CUtensorMap& tm_w,
+                               const CUtensorMap& tm_x, const CUtensorMap& tm_lb,
+                               const CUtensorMap& tm_lu, const GemmParams& p, int grid,
+                               cudaStream_t s);
 
 // --------------------------------------------------------------- finalize
 cudaError_t launch_finalize(const __nv_bfloat16* y, const int32_t* e2p, const float* w, int T,

@@ -230,3 +230,17 @@ def test_repeated_calls_are_deterministic():
     a = run_gpu(inp, layer=layer)["out"].clone()
     b = run_gpu(inp, layer=layer)["out"]
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("cluster", ["1", "2", "4"])
+def test_forward_cluster_sizes(cluster, monkeypatch):
+    """Wide token tiles shared by a cluster of CTAs through TMA multicast; I=136
+    and H=192 leave feature blocks that do not divide by the cluster size."""
+    monkeypatch.setenv("MOE_LORA_CLUSTER", cluster)
+    wl = workloads.small_workload("cluster", T=300, H=192, I=136, E=3, top_k=2, num_adapters=3,
+                                  rank=16, map_lo=-1, map_hi=2, seed=61)
+    inp = workloads.make_inputs(wl)
+    res = run_gpu(inp, tile_n=256)
+    assert res["status"] == 0, res["status_str"]
+    check_routing(res, inp)
+    assert_output_close(res["out64"], oracle.forward_inputs(inp)["out64"], f"cluster={cluster}")
