@@ -92,24 +92,24 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
   for (int i = tid; i < 16 * R; i += kShrinkThreads) s_u[i] = __float2bfloat16_rn(0.f);
   __syncthreads();
 
-  uint64_t amask = 0;
+  // This CTA handles adapter slot ``ad`` of the tile: it computes u for the
+  // tile's rows of that adapter and writes U columns [ad*r, ad*r + r) of
+  // every row of the tile (zero for rows of other adapters).  Slot 0 also
+  // copies the gathered rows.
+  const int ad = static_cast<int>(blockIdx.y);
+  bool present = false;
   if (R > 0 && p.U != nullptr) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-      if (s_adapter[i] >= 0) amask |= 1ull << s_adapter[i];
+    for (int i = 0; i < 16; ++i) present |= (s_adapter[i] == ad);
   }
-  const int n_ad = __popcll(amask);
-  const int passes = (p.gathered != nullptr && n_ad == 0) ? 1 : n_ad;
+  const bool do_gather = p.gathered != nullptr && ad == 0;
+  const int passes = (present || do_gather) ? 1 : 0;
   const int K = p.K;
   uint32_t parity = 0;
   const uint4 zero = make_uint4(0, 0, 0, 0);
 
   for (int pass = 0; pass < passes; ++pass) {
-    int a = -1;
-    if (pass < n_ad) {
-      a = __ffsll(static_cast<long long>(amask)) - 1;
-      amask &= amask - 1;
-    }
+    const int a = present ? ad : -1;
     const __nv_bfloat16* Af =
         a >= 0 ? p.A + a * p.a_stride_adapter + static_cast<int64_t>(e) * p.a_stride_expert : nullptr;
     float acc[NT > 0 ? NT : 1][4];
@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
       }
       mbar_wait(bar, parity, p.timeout_ns);
       parity ^= 1;
-      if (pass == 0 && p.gathered != nullptr) {
+      if (do_gather) {
         const int vpr = cur / 8;
         for (int v = tid; v < nrows * vpr; v += kShrinkThreads) {
           const int row = v / vpr, c = (v - row * vpr) * 8;
@@ -193,17 +193,15 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
   pdl_launch_dependents();
 
   if constexpr (NT > 0) {
-   if (p.U != nullptr) {  // whole rows of U: own adapter's r values, zeros elsewhere
+   if (p.U != nullptr) {  // this adapter's r columns of every row of the tile
     const int ld = p.num_adapters * R;
-    const int vec_per_row = ld / 8;
+    constexpr int vec_per_row = R / 8;
     for (int v = tid; v < nrows * vec_per_row; v += kShrinkThreads) {
       const int row = v / vec_per_row;
-      const int col = (v - row * vec_per_row) * 8;
-      const int a = s_adapter[row];
+      const int c = (v - row * vec_per_row) * 8;
       uint4 val = zero;
-      if (a >= 0 && col >= a * R && col < (a + 1) * R)
-        val = *reinterpret_cast<const uint4*>(s_u + row * R + (col - a * R));
-      *reinterpret_cast<uint4*>(p.U + static_cast<size_t>(row0 + row) * ld + col) = val;
+      if (s_adapter[row] == ad) val = *reinterpret_cast<const uint4*>(s_u + row * R + c);
+      *reinterpret_cast<uint4*>(p.U + static_cast<size_t>(row0 + row) * ld + ad * R + c) = val;
     }
    }
   }
@@ -221,14 +219,15 @@ size_t shrink_launch_smem(const ShrinkParams& p) { return shrink_smem_bytes(p.kc
 cudaError_t launch_gather_shrink(const ShrinkParams& p, int n_rows, cudaStream_t s) {
   if (n_rows == 0) return cudaSuccess;
   const int NT = p.rank / 8;
-  const int grid = (n_rows + 15) / 16 + (p.E < n_rows ? p.E : n_rows);
+  const int tiles = (n_rows + 15) / 16 + (p.E < n_rows ? p.E : n_rows);
+  const dim3 grid(tiles, (NT > 0 && p.U != nullptr) ? p.num_adapters : 1);
   const size_t smem = shrink_smem_bytes(p.kc, p.rank);
 #define MOE_SHRINK_CASE(N)                                                                        \
   case N: {                                                                                       \
     cudaError_t err = cudaFuncSetAttribute(gather_shrink_kernel<N>,                               \
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
     if (err != cudaSuccess) return err;                                                           \
-    return launch_pdl(gather_shrink_kernel<N>, dim3(grid), dim3(kShrinkThreads), smem, s, p);     \
+    return launch_pdl(gather_shrink_kernel<N>, grid, dim3(kShrinkThreads), smem, s, p);           \
   }
   switch (NT) {
     MOE_SHRINK_CASE(0) MOE_SHRINK_CASE(1) MOE_SHRINK_CASE(2) MOE_SHRINK_CASE(3)

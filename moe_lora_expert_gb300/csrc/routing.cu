@@ -123,13 +123,19 @@ __device__ __forceinline__ int checked_id(int id, int E, int* status, bool repor
   return id;
 }
 
-__global__ void __launch_bounds__(32) permute_count_kernel(PermuteParams p) {
-  extern __shared__ int cnt[];
-  const int lane = threadIdx.x;
-  for (int e = lane; e < p.E; e += 32) cnt[e] = 0;
-  __syncwarp();
-  const int base = blockIdx.x * kPermuteChunk;
-  const int end = min(base + kPermuteChunk, p.n);
+// 8 warps per 1024-slot chunk; warp w ranks slots [128w, 128w + 128) of the
+// chunk with its own counters, then the counters are merged by a prefix over
+// the warps, so ranks follow the slot order of the whole chunk.
+constexpr int kCountWarps = 8;
+__global__ void __launch_bounds__(32 * kCountWarps) permute_count_kernel(PermuteParams p) {
+  extern __shared__ int cnt[];  // [kCountWarps][E]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < kCountWarps * p.E; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  const int seg = kPermuteChunk / kCountWarps;
+  const int base = blockIdx.x * kPermuteChunk + warp * seg;
+  const int end = min(base + seg, p.n);
+  int* my = cnt + warp * p.E;
   const unsigned lt_mask = (1u << lane) - 1u;
   for (int x0 = base; x0 < end; x0 += 32) {
     const int x = x0 + lane;
@@ -138,14 +144,29 @@ __global__ void __launch_bounds__(32) permute_count_kernel(PermuteParams p) {
     const bool routed = id >= 0;
     const unsigned group = __match_any_sync(kFull, routed ? id : -2);
     const int rank = __popc(group & lt_mask);
-    const int prev = routed ? cnt[id] : 0;
+    const int prev = routed ? my[id] : 0;
     __syncwarp();
-    if (routed && rank == 0) cnt[id] = prev + __popc(group);
+    if (routed && rank == 0) my[id] = prev + __popc(group);
     __syncwarp();
-    if (valid) p.e2p[x] = routed ? prev + rank : -1;  // rank inside the chunk for now
+    if (valid) p.e2p[x] = routed ? prev + rank : -1;  // rank inside the warp segment for now
   }
-  __syncwarp();
-  for (int e = lane; e < p.E; e += 32) p.chunk_counts[blockIdx.x * p.E + e] = cnt[e];
+  __syncthreads();
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < kCountWarps; ++w) {
+      const int v = cnt[w * p.E + e];
+      cnt[w * p.E + e] = run;
+      run += v;
+    }
+    p.chunk_counts[blockIdx.x * p.E + e] = run;
+  }
+  __syncthreads();
+  if (base < end) {
+    for (int x = base + lane; x < end; x += 32) {
+      const int r = p.e2p[x];
+      if (r >= 0) p.e2p[x] = r + my[checked_id(p.topk_ids[x], p.E, p.status, false)];
+    }
+  }
 }
 
 // Exclusive scan over the block (blockDim.x == 1024).  Returns the exclusive
@@ -203,36 +224,40 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(PermuteParams p, int
   }
 }
 
+// One thread per slot: final permuted index, inverse map, row adapter.
 __global__ void __launch_bounds__(256) permute_scatter_kernel(PermuteParams p) {
+  const int x = blockIdx.x * blockDim.x + threadIdx.x;
+  if (x >= p.n) return;
+  const int id = checked_id(p.topk_ids[x], p.E, p.status, false);
+  int pidx = -1;
+  if (id >= 0) {
+    pidx = p.expert_offsets[id] + p.chunk_counts[(x / kPermuteChunk) * p.E + id] + p.e2p[x];
+    p.p2e[pidx] = x;
+    if (p.row_adapter != nullptr) {
+      int a = -1;
+      if (p.num_adapters > 0 && p.mapping != nullptr) {
+        a = p.mapping[x / p.top_k];
+        if (a < -1 || a >= p.num_adapters) {
+          set_status(p.status, MOE_ERR_BAD_MAPPING);
+          a = -1;
+        }
+      }
+      p.row_adapter[pidx] = a;
+    }
+  }
+  p.e2p[x] = pidx;
+}
+
+// permuted[p] = hidden[x / top_k] for every routed slot x (one warp per slot).
+__global__ void __launch_bounds__(256) permute_gather_kernel(PermuteParams p) {
   const int lane = threadIdx.x & 31;
   const int x = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (x >= p.n) return;
-  int pidx = -1;
-  if (lane == 0) {
-    const int id = checked_id(p.topk_ids[x], p.E, p.status, false);
-    if (id >= 0) {
-      pidx = p.expert_offsets[id] + p.chunk_counts[(x / kPermuteChunk) * p.E + id] + p.e2p[x];
-      p.p2e[pidx] = x;
-      if (p.row_adapter != nullptr) {
-        int a = -1;
-        if (p.num_adapters > 0 && p.mapping != nullptr) {
-          a = p.mapping[x / p.top_k];
-          if (a < -1 || a >= p.num_adapters) {
-            set_status(p.status, MOE_ERR_BAD_MAPPING);
-            a = -1;
-          }
-        }
-        p.row_adapter[pidx] = a;
-      }
-    }
-    p.e2p[x] = pidx;
-  }
-  pidx = __shfl_sync(kFull, pidx, 0);
-  if (pidx < 0 || p.hidden == nullptr || p.permuted == nullptr) return;
+  const int pidx = p.e2p[x];
+  if (pidx < 0) return;
   const uint4* src = reinterpret_cast<const uint4*>(p.hidden + static_cast<size_t>(x / p.top_k) * p.H);
   uint4* dst = reinterpret_cast<uint4*>(p.permuted + static_cast<size_t>(pidx) * p.H);
-  const int nvec = p.H / 8;
-  for (int v = lane; v < nvec; v += 32) dst[v] = __ldg(src + v);
+  for (int v = lane; v < p.H / 8; v += 32) dst[v] = __ldg(src + v);
 }
 
 __global__ void permute_fill_tail_kernel(int32_t* p2e, const int32_t* offsets, int E, int n) {
@@ -251,10 +276,12 @@ size_t permute_scratch_bytes(int n, int E) {
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s) {
   if (p.n == 0) return cudaSuccess;
   const int nchunks = (p.n + kPermuteChunk - 1) / kPermuteChunk;
-  permute_count_kernel<<<nchunks, 32, p.E * sizeof(int), s>>>(p);
+  permute_count_kernel<<<nchunks, 32 * kCountWarps, kCountWarps * p.E * sizeof(int), s>>>(p);
   permute_scan_kernel<<<1, 1024, 0, s>>>(p, nchunks);
-  permute_scatter_kernel<<<(p.n + 7) / 8, 256, 0, s>>>(p);
+  permute_scatter_kernel<<<(p.n + 255) / 256, 256, 0, s>>>(p);
   permute_fill_tail_kernel<<<(p.n + 255) / 256, 256, 0, s>>>(p.p2e, p.expert_offsets, p.E, p.n);
+  if (p.hidden != nullptr && p.permuted != nullptr)
+    permute_gather_kernel<<<(p.n + 7) / 8, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 
