@@ -207,6 +207,7 @@ typedef struct {
  *     0 = chosen from T*top_k/E).
  *   wait_timeout_ms: limit of every device-side pipeline wait (0 = 2000 ms).
  *     A wait that runs out sets MOE_ERR_DEVICE_TIMEOUT and the kernel exits.
+ *   debug_flags: 0, or MOE_DEBUG_* bits (failure-path tests only).
  *   stage_events: NULL, or an array of MOE_NUM_STAGE_EVENTS cudaEvent_t
  *     that are recorded on ``stream`` before the first stage, between
  *     stages and after the last one (unused slots are recorded at the end).
@@ -230,8 +231,15 @@ typedef struct {
   size_t workspace_bytes;
   int tile_n;
   int wait_timeout_ms;
+  uint32_t debug_flags;           /* 0 in normal use; see MOE_DEBUG_* */
   struct CUevent_st* const* stage_events;
 } moe_lora_args_t;
+
+/* Test-only flag for debug_flags: the gate_up GEMM's MMA role first waits on
+ * a barrier that nothing signals, so its wait runs out after wait_timeout_ms;
+ * the kernel then reports MOE_ERR_DEVICE_TIMEOUT, drains its own copies and
+ * MMAs, frees its tensor memory and exits (the output is then garbage). */
+#define MOE_DEBUG_STALL_GATE_UP_MMA 1u
 
 /* Byte offsets of the intermediates inside the workspace (for inspection). */
 typedef struct {

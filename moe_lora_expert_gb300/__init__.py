@@ -30,6 +30,7 @@ MOE_ERR_DEVICE_TIMEOUT = -7
 MOE_ERR_BAD_MAPPING = -8
 MOE_ERR_BAD_EXPERT_ID = -9
 MOE_NUM_STAGE_EVENTS = 8
+MOE_DEBUG_STALL_GATE_UP_MMA = 1
 STAGE_NAMES = ["route", "permute", "shrink_gate_up", "gemm_gate_up", "shrink_down", "gemm_down",
                "finalize"]
 
@@ -65,6 +66,7 @@ class MoeLoraArgs(ctypes.Structure):
                 ("expanded_to_permuted_out", ctypes.c_void_p),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
                 ("tile_n", ctypes.c_int), ("wait_timeout_ms", ctypes.c_int),
+                ("debug_flags", ctypes.c_uint32),
                 ("stage_events", ctypes.c_void_p)]
 
 
@@ -273,7 +275,8 @@ class MoeLoraLayer:
                                        self.rank)
 
     def make_args(self, hidden, router_logits, token_lora_mapping, out, topk_ids=None, topk_w=None,
-                  expanded_to_permuted=None, tile_n=0, wait_timeout_ms=0, stage_events=None):
+                  expanded_to_permuted=None, tile_n=0, wait_timeout_ms=0, stage_events=None,
+                  debug_flags=0):
         T = hidden.shape[0]
         ws = self.workspace(T)
         a = MoeLoraArgs()
@@ -289,6 +292,7 @@ class MoeLoraLayer:
         a.expanded_to_permuted_out = _ptr(expanded_to_permuted)
         a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
         a.tile_n, a.wait_timeout_ms = int(tile_n), int(wait_timeout_ms)
+        a.debug_flags = int(debug_flags)
         self._events_keepalive = None
         if stage_events is not None:
             if len(stage_events) != MOE_NUM_STAGE_EVENTS:
@@ -303,7 +307,7 @@ class MoeLoraLayer:
 
     def forward(self, hidden, router_logits, token_lora_mapping=None, out=None, topk_ids=None,
                 topk_w=None, expanded_to_permuted=None, tile_n=0, wait_timeout_ms=0,
-                stage_events: Optional[Sequence] = None, stream=None):
+                stage_events: Optional[Sequence] = None, stream=None, debug_flags=0):
         torch = _torch()
         T = hidden.shape[0]
         _require(hidden, torch.bfloat16, (T, self.H), "hidden")
@@ -313,7 +317,8 @@ class MoeLoraLayer:
         if out is None:
             out = torch.empty((T, self.H), dtype=torch.bfloat16, device=hidden.device)
         args = self.make_args(hidden, router_logits, token_lora_mapping, out, topk_ids, topk_w,
-                              expanded_to_permuted, tile_n, wait_timeout_ms, stage_events)
+                              expanded_to_permuted, tile_n, wait_timeout_ms, stage_events,
+                              debug_flags)
         _check(moe_lora_forward(args, stream), "moe_lora_forward")
         return out
 

@@ -17,7 +17,9 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "../../include/moe_lora.h"
 #include "kernels.cuh"
@@ -173,6 +175,24 @@ int auto_tile_n(int n_rows, int E) {
 }
 
 }  // namespace
+
+namespace moe {
+
+cudaError_t ensure_smem_limit(const void* func, int bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, int> done;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  std::lock_guard<std::mutex> lock(mu);
+  int& have = done[std::make_pair(dev, func)];
+  if (have >= bytes) return cudaSuccess;
+  err = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (err == cudaSuccess) have = bytes;
+  return err;
+}
+
+}  // namespace moe
 
 extern "C" {
 
@@ -482,6 +502,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.K = H;
   gp.rows_per_expert = 2 * I;
   gp.gu_single_box = gu_single_box ? 1 : 0;
+  gp.debug_stall_mma = (a->debug_flags & MOE_DEBUG_STALL_GATE_UP_MMA) ? 1 : 0;
   gp.n_feat = I;
   gp.feat_blocks = (I + 63) / 64;
   gp.num_adapters = A;
@@ -515,6 +536,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.rows_per_expert = H;
   gp.n_feat = H;
   gp.feat_blocks = (H + 127) / 128;
+  gp.debug_stall_mma = 0;
   gp.lb_row_stride_adapter = dn_rs_a;
   gp.lb_row_stride_expert = dn_rs_e;
   gp.out = y;

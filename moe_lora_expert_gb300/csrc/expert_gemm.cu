@@ -172,7 +172,8 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
   uint64_t* accf = empty + C::kStages;
   uint64_t* acce = accf + 2;
   uint64_t* drain = acce + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* never = drain + 1;  // test hook: a barrier nothing arrives on
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_off = reinterpret_cast<int*>(meta + C::kMetaBytes);
   int* s_ts = s_off + (MOE_MAX_EXPERTS + 1);
@@ -192,6 +193,7 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
       mbar_init(&acce[b], 4);
     }
     mbar_init(drain, 1);
+    mbar_init(never, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -301,6 +303,11 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
     // -------------------------------------------------------- MMA issuer
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
     bool ok = true;
+    if (p.debug_stall_mma) {  // failure-path test: this wait can only run out
+      if (lane == 0 && !wait_or_abort(never, 0, p.timeout_ns, abort_flag))
+        raise_timeout(p.status, abort_flag);
+      ok = false;
+    }
     for (int w = unit0; w < total_work && ok; w += unit_step) {
       if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
       const Work wk = decode_work<BN>(w, crank, CL, s_off, s_ts, p.E, FBg);
@@ -462,7 +469,7 @@ static cudaError_t launch_one(const CUtensorMap& tm_w, const CUtensorMap& tm_x,
                               const GemmParams& p, int grid, cudaStream_t s) {
   auto kern = expert_gemm_kernel<BN, MODE, CL>;
   const int smem = GemmCfg<BN>::kSmemBytes;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
   if (CL == 1) return launch_pdl(kern, dim3(grid), dim3(192), smem, s, tm_w, tm_x, tm_lb, tm_lu, p);
 

@@ -9,6 +9,10 @@
 
 namespace moe {
 
+// Raises a kernel's dynamic shared-memory limit once per device, so that the
+// launch path itself issues only launches (and stays capturable).
+cudaError_t ensure_smem_limit(const void* func, int bytes);
+
 // Launch with programmatic stream serialization: the kernel may start while
 // its predecessor drains, and must call griddepcontrol.wait (pdl_wait)
 // before touching anything the predecessor writes.
@@ -120,6 +124,7 @@ struct GemmParams {
   int K;                          // main reduction length (H or I)
   int rows_per_expert;            // rows of the weight per expert (2I or H)
   int gu_single_box;              // gate_up weight map is the 5-D one-box view
+  int debug_stall_mma;            // test only: MMA role first waits on a barrier nobody signals
   int n_feat;                     // output features (I for gate_up, H for down)
   int feat_blocks;                // feature blocks per expert
   int num_adapters;               // 0 = no LoRA

@@ -224,8 +224,7 @@ cudaError_t launch_gather_shrink(const ShrinkParams& p, int n_rows, cudaStream_t
   const size_t smem = shrink_smem_bytes(p.kc, p.rank);
 #define MOE_SHRINK_CASE(N)                                                                        \
   case N: {                                                                                       \
-    cudaError_t err = cudaFuncSetAttribute(gather_shrink_kernel<N>,                               \
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+    cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(gather_shrink_kernel<N>), (int)smem); \
     if (err != cudaSuccess) return err;                                                           \
     return launch_pdl(gather_shrink_kernel<N>, grid, dim3(kShrinkThreads), smem, s, p);           \
   }

@@ -417,8 +417,7 @@ cudaError_t launch_small_permute(const FusedPermuteParams& p, cudaStream_t s) {
   const int epl = (p.E + 31) / 32;
 #define MOE_SMALL_CASE(V)                                                                         \
   {                                                                                               \
-    cudaError_t err = cudaFuncSetAttribute(small_permute_kernel<V>,                               \
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+    cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(small_permute_kernel<V>), (int)smem); \
     if (err != cudaSuccess) return err;                                                           \
     return launch_pdl(small_permute_kernel<V>, dim3(1), dim3(1024), smem, s, p);                  \
   }

@@ -244,3 +244,50 @@ def test_forward_cluster_sizes(cluster, monkeypatch):
     assert res["status"] == 0, res["status_str"]
     check_routing(res, inp)
     assert_output_close(res["out64"], oracle.forward_inputs(inp)["out64"], f"cluster={cluster}")
+
+
+def test_forward_replays_from_a_cuda_graph():
+    """The forward enqueues only launches and memsets: captured into a CUDA graph
+    and replayed it gives the eager result bit for bit, also after the inputs
+    are overwritten in place between replays."""
+    torch = torch_mod()
+    for name in ["decode_T16", "skewed_T256_shared_outer_r64"]:
+        inp = cached_inputs(name)
+        layer = make_layer(inp)
+        hid = bf16_tensor(inp.hidden)
+        lg = torch.from_numpy(inp.logits).to(dev())
+        mp = torch.from_numpy(inp.mapping).to(dev())
+        eager = layer.forward(hid, lg, mp).clone()
+        out = torch.empty_like(eager)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            layer.forward(hid, lg, mp, out=out)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), eager.view(torch.int16)), name
+        lg.copy_(torch.flip(lg, dims=[0]))
+        hid.copy_(torch.flip(hid, dims=[0]))
+        graph.replay()
+        eager2 = layer.forward(hid, lg, mp)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), eager2.view(torch.int16)), name
+        assert layer.device_status() == 0
+
+
+def test_device_wait_timeout_is_reported_and_recoverable():
+    """A pipeline wait that can only run out (test flag: the gate_up GEMM's MMA
+    role waits on a barrier nobody signals) ends with MOE_ERR_DEVICE_TIMEOUT
+    in the status word; the kernel drains and frees its tensor memory, and the
+    next call on the same workspace is correct again."""
+    import moe_lora_expert_gb300 as m
+    torch = torch_mod()
+    inp = cached_inputs("tiny_T8")
+    layer = make_layer(inp)
+    hid = bf16_tensor(inp.hidden)
+    lg = torch.from_numpy(inp.logits).to(dev())
+    mp = torch.from_numpy(inp.mapping).to(dev())
+    layer.forward(hid, lg, mp, wait_timeout_ms=20, debug_flags=m.MOE_DEBUG_STALL_GATE_UP_MMA)
+    assert layer.device_status() == m.MOE_ERR_DEVICE_TIMEOUT
+    out = layer.forward(hid, lg, mp)
+    assert layer.device_status() == m.MOE_OK
+    assert_output_close(to_f64(out), oracle.forward_inputs(inp)["out64"], "after timeout")
