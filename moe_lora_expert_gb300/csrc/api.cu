@@ -439,6 +439,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   fp.e2p = e2p;
   fp.p2e = p2e;
   fp.tile_start = tile_start;
+  fp.tile_width_mask = (1u << moe::tile_width_index(16)) | (1u << moe::tile_width_index(bn));
   fp.status = status;
   if (!fuse_route &&
       moe::launch_route_topk(a->router_logits, T, E, K, topk_ids, topk_w, stream) != cudaSuccess)

@@ -108,6 +108,7 @@ struct FusedPermuteParams {
   int32_t* e2p;                 // [n]
   int32_t* p2e;                 // [n]
   int32_t* tile_start;          // [kNumTileWidths, E + 1] or null
+  uint32_t tile_width_mask;     // bit i: write the prefix for width 16 << i
   int* status;                  // cleared by the kernel
 };
 bool small_permute_fits(int n, int E);

@@ -369,6 +369,7 @@ __global__ void __launch_bounds__(1024) small_permute_kernel(const FusedPermuteP
   }
   if (p.tile_start != nullptr) {
     for (int wi = 0; wi < kNumTileWidths; ++wi) {
+      if (!((p.tile_width_mask >> wi) & 1u)) continue;
       const int bn = tile_width_of(wi);
       const int tiles = tid < E ? (total + bn - 1) / bn : 0;
       const int ts = block_exclusive_scan_1024(tiles, warp_sums, &s_total);
@@ -432,30 +433,48 @@ cudaError_t launch_small_permute(const FusedPermuteParams& p, cudaStream_t s) {
 
 // ---------------------------------------------------------------- finalize
 // out[t, :] = sum_j w[t, j] * y[e2p[t*k + j], :], summed in slot order in
-// float32, rounded to bf16 (nearest even).  One thread per 8 columns.
+// float32, rounded to bf16 (nearest even).  One CTA per token, one thread per
+// 8 columns; the slot indices and weights are staged in shared memory first
+// so that each thread's k row loads are independent and issue together.
 __global__ void __launch_bounds__(256) finalize_kernel(const __nv_bfloat16* __restrict__ y,
                                                        const int32_t* __restrict__ e2p,
                                                        const float* __restrict__ w, int k, int H,
                                                        __nv_bfloat16* __restrict__ out) {
+  __shared__ int s_p[MOE_MAX_TOP_K];
+  __shared__ float s_w[MOE_MAX_TOP_K];
   const int t = blockIdx.x;
   const int c8 = blockIdx.y * blockDim.x + threadIdx.x;
   pdl_wait();
   pdl_launch_dependents();
+  if (threadIdx.x < k) {
+    s_p[threadIdx.x] = e2p[static_cast<size_t>(t) * k + threadIdx.x];
+    s_w[threadIdx.x] = w[static_cast<size_t>(t) * k + threadIdx.x];
+  }
+  __syncthreads();
   if (c8 * 8 >= H) return;
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  for (int j = 0; j < k; ++j) {
-    const int p = e2p[static_cast<size_t>(t) * k + j];
-    if (p < 0) continue;
-    const float wj = w[static_cast<size_t>(t) * k + j];
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(y + static_cast<size_t>(p) * H) + c8);
-    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+  constexpr int kBatch = 8;
+  for (int j0 = 0; j0 < k; j0 += kBatch) {
+    uint4 v[kBatch];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = __bfloat1622float2(h2[i]);
-      acc[2 * i] = fmaf(wj, f.x, acc[2 * i]);
-      acc[2 * i + 1] = fmaf(wj, f.y, acc[2 * i + 1]);
+    for (int b = 0; b < kBatch; ++b) {
+      const int p = (j0 + b < k) ? s_p[j0 + b] : -1;
+      v[b] = p >= 0 ? __ldg(reinterpret_cast<const uint4*>(y + static_cast<size_t>(p) * H) + c8)
+                    : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      if (j0 + b >= k || s_p[j0 + b] < 0) continue;
+      const float wj = s_w[j0 + b];
+      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v[b]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h2[i]);
+        acc[2 * i] = fmaf(wj, f.x, acc[2 * i]);
+        acc[2 * i + 1] = fmaf(wj, f.y, acc[2 * i + 1]);
+      }
     }
   }
   uint4 o;
