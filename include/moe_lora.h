@@ -208,6 +208,15 @@ typedef struct {
  *   wait_timeout_ms: limit of every device-side pipeline wait (0 = 2000 ms).
  *     A wait that runs out sets MOE_ERR_DEVICE_TIMEOUT and the kernel exits.
  *   debug_flags: 0, or MOE_DEBUG_* bits (failure-path tests only).
+ *   adapter_scaling: NULL (every adapter uses ``scaling``) or a HOST array of
+ *     num_adapters LoRA scales (e.g. alpha_a / r_a per adapter).  The values
+ *     are read during the call and travel with the launches, so a captured
+ *     CUDA graph keeps the values of the capture.
+ *   Per-adapter ranks: pad each adapter's factors with zero rows (A) and zero
+ *     columns (B) to the common ``rank``; the padding contributes exactly 0.
+ *   Separate gate and up LoRAs (A_g [r,H], B_g [I,r], A_u [r,H], B_u [I,r]):
+ *     pass them as the rank-2r gate_up pair A = [A_g; A_u],
+ *     B = [[B_g, 0], [0, B_u]], which gives the same two deltas.
  *   stage_events: NULL, or an array of MOE_NUM_STAGE_EVENTS cudaEvent_t
  *     that are recorded on ``stream`` before the first stage, between
  *     stages and after the last one (unused slots are recorded at the end).
@@ -233,6 +242,7 @@ typedef struct {
   int wait_timeout_ms;
   uint32_t debug_flags;           /* 0 in normal use; see MOE_DEBUG_* */
   struct CUevent_st* const* stage_events;
+  const float* adapter_scaling;   /* HOST array [num_adapters] or NULL */
 } moe_lora_args_t;
 
 /* Test-only flag for debug_flags: the gate_up GEMM's MMA role first waits on

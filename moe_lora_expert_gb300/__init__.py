@@ -67,7 +67,8 @@ class MoeLoraArgs(ctypes.Structure):
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
                 ("tile_n", ctypes.c_int), ("wait_timeout_ms", ctypes.c_int),
                 ("debug_flags", ctypes.c_uint32),
-                ("stage_events", ctypes.c_void_p)]
+                ("stage_events", ctypes.c_void_p),
+                ("adapter_scaling", ctypes.c_void_p)]
 
 
 class WorkspacePlan(ctypes.Structure):
@@ -228,7 +229,7 @@ class MoeLoraLayer:
     """
 
     def __init__(self, w13, w2, top_k: int, A_gu=None, B_gu=None, A_dn=None, B_dn=None,
-                 scaling: float = 1.0, max_tokens: int = 0):
+                 scaling: float = 1.0, max_tokens: int = 0, adapter_scaling=None):
         torch = _torch()
         self.E, twoI, self.H = w13.shape
         self.I = twoI // 2
@@ -257,6 +258,11 @@ class MoeLoraLayer:
             self.dn = LoraFactors(None, None, 0, 0, 0, 0)
         self._ws = None
         self._ws_T = -1
+        self._scales = None
+        if adapter_scaling is not None:
+            if len(adapter_scaling) != self.num_adapters:
+                raise ValueError("adapter_scaling needs one value per adapter")
+            self._scales = (ctypes.c_float * max(1, self.num_adapters))(*[float(v) for v in adapter_scaling])
         if max_tokens > 0:
             self.workspace(max_tokens)
 
@@ -293,6 +299,7 @@ class MoeLoraLayer:
         a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
         a.tile_n, a.wait_timeout_ms = int(tile_n), int(wait_timeout_ms)
         a.debug_flags = int(debug_flags)
+        a.adapter_scaling = ctypes.cast(self._scales, ctypes.c_void_p) if self._scales is not None else None
         self._events_keepalive = None
         if stage_events is not None:
             if len(stage_events) != MOE_NUM_STAGE_EVENTS:

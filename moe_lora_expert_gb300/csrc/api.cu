@@ -487,7 +487,8 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   sp.E = E;
   sp.num_adapters = A;
   sp.rank = r;
-  sp.scaling = a->scaling;
+  for (int i = 0; i < MOE_MAX_ADAPTERS; ++i)
+    sp.scaling[i] = (a->adapter_scaling != nullptr && i < A) ? a->adapter_scaling[i] : a->scaling;
   sp.U = lora ? U : nullptr;
   sp.status = status;
   sp.timeout_ns = timeout_ns;

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/moe_lora.h"
+
 namespace moe {
 
 // Raises a kernel's dynamic shared-memory limit once per device, so that the
@@ -87,7 +89,7 @@ struct ShrinkParams {
   int E;
   int num_adapters;
   int rank;                     // 0: gather only
-  float scaling;
+  float scaling[MOE_MAX_ADAPTERS];  // per adapter
   __nv_bfloat16* U;             // [n, num_adapters * rank], or null
   int* status;
   uint64_t timeout_ns;

@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
         float sum = 0.f;
 #pragma unroll
         for (int w = 0; w < 8; ++w) sum += s_red[w * 16 * R + i];
-        s_u[i] = __float2bfloat16_rn(p.scaling * sum);
+        s_u[i] = __float2bfloat16_rn(p.scaling[a] * sum);
       }
       __syncthreads();
      }

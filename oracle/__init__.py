@@ -6,4 +6,5 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 from .moe_lora_oracle import (  # noqa: F401
     bf16_bits_to_f64, f64_to_bf16_bits, route_topk, permute, silu, expert_slot,
     LoraFactors, moe_lora_forward, factors_from_inputs, forward_inputs,
+    expert_slot_general, decode_adapter, moe_lora_forward_general,
 )

@@ -313,3 +313,82 @@ def forward_inputs(inp, tokens=None, keep_intermediates=False, with_lora=True):
     wl = inp.wl
     return moe_lora_forward(inp.hidden, inp.logits, inp.w13, inp.w2, inp.mapping, wl.top_k,
                             wl.scaling, gu, dn, tokens=tokens, keep_intermediates=keep_intermediates)
+
+
+# ---------------------------------------------------------------------------
+# General adapters: separate or fused gate/up LoRA, own rank and scale per
+# adapter.  Real PEFT adapters carry one LoRA pair per projection (gate_proj,
+# up_proj, down_proj) with scale alpha / r.  The pages' fused gate_up delta is
+# the special case of one pair on the fused projection (readings R4, R5).
+# ---------------------------------------------------------------------------
+
+def expert_slot_general(x, w13_e, w2_e, adapter, expert):
+    """One (token, expert) evaluation with a general adapter (or None).
+
+    ``adapter`` is a dict of float64 arrays indexed by expert:
+      'scaling': s,
+      either 'gate_up': (A [E, r, H], B [E, 2I, r])
+      or 'gate': (A [E, r, H], B [E, I, r]) and 'up': (A, B) of the same shapes,
+      'down': (A [E, r, I], B [E, H, r]).
+    gate = w13[e][:I] x + s B_g (A_g x);  up = w13[e][I:] x + s B_u (A_u x)
+    y = w2[e] h + s B_dn (A_dn h),  h = silu(gate) * up.
+    """
+    I = w2_e.shape[1]
+    g = w13_e @ x
+    if adapter is not None:
+        s = adapter["scaling"]
+        if "gate_up" in adapter:
+            A, B = adapter["gate_up"]
+            g = g + s * (B[expert] @ (A[expert] @ x))
+        else:
+            Ag, Bg = adapter["gate"]
+            Au, Bu = adapter["up"]
+            g = g + s * np.concatenate([Bg[expert] @ (Ag[expert] @ x), Bu[expert] @ (Au[expert] @ x)])
+    h = silu(g[:I]) * g[I:]
+    y = w2_e @ h
+    if adapter is not None:
+        Ad, Bd = adapter["down"]
+        y = y + adapter["scaling"] * (Bd[expert] @ (Ad[expert] @ h))
+    return y
+
+
+def decode_adapter(bits_adapter):
+    """bf16-bit arrays of one adapter -> float64 (same structure)."""
+    out = {"scaling": float(bits_adapter["scaling"])}
+    for key in ("gate_up", "gate", "up", "down"):
+        if key in bits_adapter:
+            A, B = bits_adapter[key]
+            out[key] = (bf16_bits_to_f64(A), bf16_bits_to_f64(B))
+    return out
+
+
+def moe_lora_forward_general(hidden_bits, logits, w13_bits, w2_bits, mapping, top_k, adapters,
+                             tokens=None):
+    """Layer forward with general adapters (list indexed by adapter slot).
+
+    Routing and the weighted sum are those of ``moe_lora_forward``; each slot
+    is ``expert_slot_general``.  Returns (out64 [n, H], out_bf16).
+    """
+    T, H = np.asarray(hidden_bits).shape
+    ids, w = route_topk(logits, top_k)
+    tokens = list(range(T)) if tokens is None else list(tokens)
+    dec = [decode_adapter(a) for a in adapters]
+    by_expert = {}
+    for t in tokens:
+        for j in range(top_k):
+            by_expert.setdefault(int(ids[t, j]), []).append((t, j))
+    y_slot = {}
+    for e in sorted(by_expert):
+        w13_e = bf16_bits_to_f64(w13_bits[e])
+        w2_e = bf16_bits_to_f64(w2_bits[e])
+        for (t, j) in by_expert[e]:
+            a = int(mapping[t])
+            y_slot[(t, j)] = expert_slot_general(bf16_bits_to_f64(hidden_bits[t]), w13_e, w2_e,
+                                                 dec[a] if a >= 0 else None, e)
+    out = np.zeros((len(tokens), H))
+    for i, t in enumerate(tokens):
+        acc = np.zeros(H)
+        for j in range(top_k):
+            acc = acc + w[t, j] * y_slot[(t, j)]
+        out[i] = acc
+    return out, f64_to_bf16_bits(out)

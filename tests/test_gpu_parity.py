@@ -291,3 +291,33 @@ def test_device_wait_timeout_is_reported_and_recoverable():
     out = layer.forward(hid, lg, mp)
     assert layer.device_status() == m.MOE_OK
     assert_output_close(to_f64(out), oracle.forward_inputs(inp)["out64"], "after timeout")
+
+
+@pytest.mark.parametrize("shape", ["small", "decode_T16"])
+def test_peft_adapters_separate_gate_up_mixed_ranks_and_scales(shape):
+    """Separate gate/up pairs, per-adapter ranks and scales, packed into the
+    fused layout (block-diagonal, zero-padded) and run through the kernels,
+    against the oracle's direct per-projection formulation."""
+    import moe_lora_expert_gb300 as m
+    from moe_lora_expert_gb300 import adapters as pk
+    torch = torch_mod()
+    specs = [("separate", 8, 16.0), ("fused", 16, 32.0), ("separate", 16, 8.0), ("fused", 8, 8.0)]
+    if shape == "small":
+        wl = workloads.small_workload("peft_gpu", T=40, H=128, I=64, E=6, top_k=2, num_adapters=4,
+                                      rank=8, map_lo=-1, map_hi=3, seed=81)
+    else:
+        wl = workloads.WORKLOADS["decode_T16"]
+    inp = workloads.make_inputs(wl) if shape == "small" else cached_inputs("decode_T16")
+    ads = workloads.make_peft_adapters(wl, specs, seed=82)
+    ads_t = [{"scaling": ad["scaling"], **{k: (bf16_tensor(v[0]), bf16_tensor(v[1]))
+                                           for k, v in ad.items() if k != "scaling"}} for ad in ads]
+    A_gu, B_gu, A_dn, B_dn, scales = pk.pack_adapters(ads_t, wl.E, wl.H, wl.I)
+    layer = m.MoeLoraLayer(bf16_tensor(inp.w13), bf16_tensor(inp.w2), wl.top_k, A_gu, B_gu, A_dn,
+                           B_dn, scaling=1.0, adapter_scaling=scales)
+    mapping = inp.mapping.clip(-1, 3).astype(np.int32)
+    out = layer.forward(bf16_tensor(inp.hidden), torch.from_numpy(inp.logits).to(dev()),
+                        torch.from_numpy(mapping).to(dev()))
+    assert layer.device_status() == 0
+    ref, _ = oracle.moe_lora_forward_general(inp.hidden, inp.logits, inp.w13, inp.w2, mapping,
+                                             wl.top_k, ads)
+    assert_output_close(to_f64(out), ref, f"peft {shape}")

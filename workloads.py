@@ -153,3 +153,28 @@ def small_workload(name="custom", T=8, H=64, I=32, E=4, top_k=2, num_adapters=2,
     """A workload of arbitrary (small) shape, for edge cases and brute-force checks."""
     return Workload(name, T, H, I, E, top_k, num_adapters, rank, scaling, map_lo, map_hi,
                     shared_outer, bias_sigma, seed)
+
+
+def make_peft_adapters(wl: Workload, specs, seed: int = 7):
+    """Draw PEFT-style adapters for the layer shape of ``wl``.
+
+    ``specs`` is a list, one entry per adapter slot, of (kind, rank, alpha):
+    kind "separate" draws one LoRA pair per projection (gate, up, down);
+    kind "fused" draws one pair on the fused gate_up projection and one on
+    down.  Factors ~ N(0, 0.02) -> bf16 bits; scaling = alpha / rank.
+    Order: for each adapter in turn, its gate/up (or gate_up) A then B, then
+    down A then B.
+    """
+    rng = np.random.default_rng(seed)
+    H, I, E = wl.H, wl.I, wl.E
+    out = []
+    for kind, r, alpha in specs:
+        ad = {"scaling": float(alpha) / float(r)}
+        if kind == "separate":
+            ad["gate"] = (_normal_bf16(rng, (E, r, H), 0.02), _normal_bf16(rng, (E, I, r), 0.02))
+            ad["up"] = (_normal_bf16(rng, (E, r, H), 0.02), _normal_bf16(rng, (E, I, r), 0.02))
+        else:
+            ad["gate_up"] = (_normal_bf16(rng, (E, r, H), 0.02), _normal_bf16(rng, (E, 2 * I, r), 0.02))
+        ad["down"] = (_normal_bf16(rng, (E, r, I), 0.02), _normal_bf16(rng, (E, H, r), 0.02))
+        out.append(ad)
+    return out
