@@ -493,6 +493,11 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   sp.status = status;
   sp.timeout_ns = timeout_ns;
   sp.kc = moe::shrink_chunk(H, r, shrink_budget);
+  // A shared gate_up A factor makes u a function of the token alone.
+  sp.per_token = (lora && a->gate_up.a_stride_expert == 0) ? 1 : 0;
+  sp.T = T;
+  sp.e2p = e2p;
+  sp.mapping = lora ? a->token_lora_mapping : nullptr;
   if (moe::launch_gather_shrink(sp, static_cast<int>(n), stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (!mark()) return MOE_ERR_CUDA;
   // 4. gate_up GEMM + LoRA expand + SwiGLU -> h
@@ -530,6 +535,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
     sp.a_stride_expert = a->down.a_stride_expert;
     sp.U = V;
     sp.kc = moe::shrink_chunk(I, r, shrink_budget);
+    sp.per_token = 0;
     if (moe::launch_gather_shrink(sp, static_cast<int>(n), stream) != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (!mark()) return MOE_ERR_CUDA;

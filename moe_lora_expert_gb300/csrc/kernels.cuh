@@ -93,6 +93,13 @@ struct ShrinkParams {
   __nv_bfloat16* U;             // [n, num_adapters * rank], or null
   int* status;
   uint64_t timeout_ns;
+  // Per-token mode (gate_up A shared by all experts, so u depends on the
+  // token only): tiles of 16 tokens; rows are hidden rows; results and
+  // gathered copies go to every permuted row e2p[t*top_k + j] of the token.
+  int per_token;
+  int T;
+  const int32_t* e2p;           // [T * top_k]
+  const int32_t* mapping;       // [T]
 };
 int shrink_chunk(int K, int rank, size_t smem_budget);
 cudaError_t launch_gather_shrink(const ShrinkParams& p, int n_rows, cudaStream_t s);

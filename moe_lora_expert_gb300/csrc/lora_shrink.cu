@@ -62,9 +62,13 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
   pdl_wait();
   if (tid == 0) {
     const int tile = blockIdx.x;
-    const int total = p.tile_start16[p.E];
+    const int total = p.per_token ? (p.T + 15) / 16 : p.tile_start16[p.E];
     int e = -1, row0 = 0, nrows = 0;
-    if (tile < total) {
+    if (p.per_token && tile < total) {
+      e = 0;  // the factor does not depend on the expert
+      row0 = tile * 16;
+      nrows = min(16, p.T - row0);
+    } else if (tile < total) {
       int lo = 0, hi = p.E - 1;
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -86,8 +90,17 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
   if (e < 0) return;
   if (tid < 16) {
     const bool in = tid < nrows;
-    s_adapter[tid] = (in && R > 0) ? p.row_adapter[row0 + tid] : -1;
-    s_src[tid] = in ? (p.p2e != nullptr ? p.p2e[row0 + tid] / p.top_k : row0 + tid) : 0;
+    int a = -1;
+    if (in && R > 0) {
+      if (p.per_token) {  // same rule as the permute: out-of-range mappings mean "none"
+        a = p.mapping[row0 + tid];
+        if (a < -1 || a >= p.num_adapters) a = -1;
+      } else {
+        a = p.row_adapter[row0 + tid];
+      }
+    }
+    s_adapter[tid] = a;
+    s_src[tid] = in ? ((p.p2e != nullptr && !p.per_token) ? p.p2e[row0 + tid] / p.top_k : row0 + tid) : 0;
   }
   for (int i = tid; i < 16 * R; i += kShrinkThreads) s_u[i] = __float2bfloat16_rn(0.f);
   __syncthreads();
@@ -142,9 +155,12 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
       parity ^= 1;
       if (do_gather) {
         const int vpr = cur / 8;
-        for (int v = tid; v < nrows * vpr; v += kShrinkThreads) {
-          const int row = v / vpr, c = (v - row * vpr) * 8;
-          *reinterpret_cast<uint4*>(p.gathered + static_cast<size_t>(row0 + row) * K + kc0 + c) =
+        const int copies = p.per_token ? p.top_k : 1;  // every permuted row of the token
+        for (int v = tid; v < nrows * copies * vpr; v += kShrinkThreads) {
+          const int rc = v / vpr, c = (v - rc * vpr) * 8;
+          const int row = rc / copies, j = rc - row * copies;
+          const int dst = p.per_token ? p.e2p[(row0 + row) * p.top_k + j] : row0 + row;
+          *reinterpret_cast<uint4*>(p.gathered + static_cast<size_t>(dst) * K + kc0 + c) =
               *reinterpret_cast<const uint4*>(Xs + row * pitch + c);
         }
       }
@@ -196,12 +212,15 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
    if (p.U != nullptr) {  // this adapter's r columns of every row of the tile
     const int ld = p.num_adapters * R;
     constexpr int vec_per_row = R / 8;
-    for (int v = tid; v < nrows * vec_per_row; v += kShrinkThreads) {
-      const int row = v / vec_per_row;
-      const int c = (v - row * vec_per_row) * 8;
+    const int copies = p.per_token ? p.top_k : 1;  // every permuted row of the token
+    for (int v = tid; v < nrows * copies * vec_per_row; v += kShrinkThreads) {
+      const int rc = v / vec_per_row;
+      const int c = (v - rc * vec_per_row) * 8;
+      const int row = rc / copies, j = rc - row * copies;
+      const int dst = p.per_token ? p.e2p[(row0 + row) * p.top_k + j] : row0 + row;
       uint4 val = zero;
       if (s_adapter[row] == ad) val = *reinterpret_cast<const uint4*>(s_u + row * R + c);
-      *reinterpret_cast<uint4*>(p.U + static_cast<size_t>(row0 + row) * ld + ad * R + c) = val;
+      *reinterpret_cast<uint4*>(p.U + static_cast<size_t>(dst) * ld + ad * R + c) = val;
     }
    }
   }
@@ -219,7 +238,7 @@ size_t shrink_launch_smem(const ShrinkParams& p) { return shrink_smem_bytes(p.kc
 cudaError_t launch_gather_shrink(const ShrinkParams& p, int n_rows, cudaStream_t s) {
   if (n_rows == 0) return cudaSuccess;
   const int NT = p.rank / 8;
-  const int tiles = (n_rows + 15) / 16 + (p.E < n_rows ? p.E : n_rows);
+  const int tiles = p.per_token ? (p.T + 15) / 16 : (n_rows + 15) / 16 + (p.E < n_rows ? p.E : n_rows);
   const dim3 grid(tiles, (NT > 0 && p.U != nullptr) ? p.num_adapters : 1);
   const size_t smem = shrink_smem_bytes(p.kc, p.rank);
 #define MOE_SHRINK_CASE(N)                                                                        \
