@@ -105,6 +105,24 @@ def kernels_per_forward(wl):
     return ((0 if fuse_route else 1) + (1 if small else 4) + 1 + 1 + (1 if lora else 0) + 1 + 1)
 
 
+def max_over_ranks(value_ms, dist=None, device=None):
+    """Largest per-rank time (ms) across the process group (identity without one)."""
+    if dist is None:
+        return float(value_ms)
+    import torch
+    t = torch.tensor([float(value_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_step, steps, world, total_ms_per_rank, dist=None, device=None):
+    """Whole-job tokens/s of ``world`` replicas: every rank processes
+    ``tokens_per_step`` tokens per step; the job takes as long as its slowest
+    rank.  Returns (tokens_per_s, slowest_rank_total_ms)."""
+    slowest = max_over_ranks(total_ms_per_rank, dist, device)
+    return world * tokens_per_step * steps / (slowest / 1e3), slowest
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -323,13 +341,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     stage_ms = [[ev[j].elapsed_time(ev[j + 1]) for j in range(m.MOE_NUM_STAGE_EVENTS - 1)]
                 for ev in events]
-    total_ms = sum(step_ms)
-    if pg:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    value, total_ms = job_throughput(wl.T, args.steps, world, sum(step_ms), pg, dev)
     ms_per_step = total_ms / args.steps
-    value = world * wl.T * args.steps / (total_ms / 1e3)
 
     # ---------------- e2e: host buffers, copies inside the timed region
     h_hidden = hidden.cpu().pin_memory()
@@ -354,10 +367,7 @@ def run_ours(args):
         e1.synchronize()
         if i >= args.warmup:
             e_ms += e0.elapsed_time(e1)
-    if pg:
-        t = torch.tensor([e_ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e_ms = float(t.item())
+    e_ms = max_over_ranks(e_ms, pg, dev)
     h2d = wl.T * wl.H * 2 + wl.T * wl.E * 4 + (wl.T * 4 if lora else 0)
     e2e = {"value": world * wl.T * e2e_steps / (e_ms / 1e3), "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": wl.T * wl.H * 2}
