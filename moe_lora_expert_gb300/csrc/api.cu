@@ -519,6 +519,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.out = h;
   gp.status = status;
   gp.timeout_ns = timeout_ns;
+  gp.tables_ready = 1;  // launched right after the gate_up shrink (n > 0 here)
   if (moe::launch_expert_gemm(moe::kGateUp, bn, cl, tm_w13, tm_xp, tm_bgu, tm_u, gp,
                               sms * moe::gemm_ctas_per_sm(bn), stream) !=
       cudaSuccess)
@@ -548,6 +549,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.lb_row_stride_adapter = dn_rs_a;
   gp.lb_row_stride_expert = dn_rs_e;
   gp.out = y;
+  gp.tables_ready = lora ? 1 : 0;  // else the gate_up GEMM precedes this launch
   if (moe::launch_expert_gemm(moe::kDown, bn, cl, tm_w2, tm_h, tm_bdn, tm_v, gp,
                               sms * moe::gemm_ctas_per_sm(bn), stream) !=
       cudaSuccess)

@@ -90,7 +90,7 @@ __device__ __forceinline__ uint64_t tile_adapter_mask(const int32_t* row_adapter
                                                       int nrows, int lane) {
   uint64_t m = 0;
   for (int i = lane; i < nrows; i += 32) {
-    const int a = row_adapter[row0 + i];
+    const int a = __ldcg(row_adapter + row0 + i);
     if (a >= 0) m |= 1ull << a;
   }
   const uint32_t lo = __reduce_or_sync(kFullMask, static_cast<uint32_t>(m));
@@ -209,12 +209,17 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
-  // Everything above overlaps the previous kernel's tail; the routing tables
-  // it wrote are read only after the wait.
-  pdl_wait();
+  // Programmatic dependent launch: this grid may start while the previous
+  // kernel drains.  When that kernel is the shrink (tables_ready), it waited
+  // for its own predecessor before letting this grid launch, so the routing
+  // tables the permute wrote are complete: they are read now (L2 loads, no
+  // stale L1 line possible), the weight stream starts at once, and only the
+  // token-side loads, which read what the shrink wrote, wait (producer warp,
+  // below).  Otherwise every thread waits here first.
+  if (!p.tables_ready) pdl_wait();
   for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
-    s_off[i] = p.expert_offsets[i];
-    s_ts[i] = p.tile_start[i];
+    s_off[i] = __ldcg(p.expert_offsets + i);
+    s_ts[i] = __ldcg(p.tile_start + i);
   }
   pdl_launch_dependents();
   tc_fence_before_sync();
@@ -238,6 +243,26 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
     uint32_t stage = 0, phase = 0;
     uint32_t armed = 0, armed_parity = 0;
     bool ok = true;
+    // Token-side loads of the first ring pass are held back until the
+    // previous kernel has completed (griddepcontrol.wait).
+    bool waited = !p.tables_ready;
+    int n_pend = 0;
+    const CUtensorMap* pend_map[C::kStages];
+    int pend_c0[C::kStages], pend_c1[C::kStages], pend_stage[C::kStages];
+    auto issue_token_load = [&](const CUtensorMap* map, int st, int c0, int c1) {
+      uint8_t* sB = smem + st * C::kStageBytes + C::kABytes;
+      if (CL > 1)
+        tma_load_2d_multicast(sB + crank * kPieceRows * 128, map, &full[st], c0,
+                              c1 + crank * kPieceRows, kClusterMask, pol_x);
+      else
+        tma_load_2d(sB, map, &full[st], c0, c1, pol_x);
+    };
+    auto release_pending = [&]() {
+      pdl_wait();
+      waited = true;
+      for (int i = 0; i < n_pend; ++i) issue_token_load(pend_map[i], pend_stage[i], pend_c0[i], pend_c1[i]);
+      n_pend = 0;
+    };
     for (int w = unit0; w < total_work && ok; w += unit_step) {
       if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
       const Work wk = decode_work<BN>(w, crank, CL, s_off, s_ts, p.E, FBg);
@@ -257,24 +282,29 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
             uint8_t* sA = smem + stage * C::kStageBytes;
             uint8_t* sB = sA + C::kABytes;
             mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+            (void)sB;
+            const CUtensorMap* tmap;
+            int tc0;
             if (b < nk) {
               load_weight_block<MODE>(sA, &tm_w, &full[stage], b * 64, wk.e, wk.fb,
                                       p.rows_per_expert, p.gu_single_box, pol_w);
-              if (CL > 1)
-                tma_load_2d_multicast(sB + crank * kPieceRows * 128, &tm_x, &full[stage], b * 64,
-                                      wk.row0 + crank * kPieceRows, kClusterMask, pol_x);
-              else
-                tma_load_2d(sB, &tm_x, &full[stage], b * 64, wk.row0, pol_x);
+              tmap = &tm_x;
+              tc0 = b * 64;
             } else {
               const int64_t frow = static_cast<int64_t>(adapter) * p.lb_row_stride_adapter +
                                    static_cast<int64_t>(wk.e) * p.lb_row_stride_expert;
               load_lora_b_block<MODE>(sA, &tm_lb, &full[stage], j * 64, frow, wk.fb, p.n_feat, pol_x);
-              if (CL > 1)
-                tma_load_2d_multicast(sB + crank * kPieceRows * 128, &tm_lu, &full[stage],
-                                      adapter * p.rank + j * 64, wk.row0 + crank * kPieceRows,
-                                      kClusterMask, pol_x);
-              else
-                tma_load_2d(sB, &tm_lu, &full[stage], adapter * p.rank + j * 64, wk.row0, pol_x);
+              tmap = &tm_lu;
+              tc0 = adapter * p.rank + j * 64;
+            }
+            if (waited) {
+              issue_token_load(tmap, stage, tc0, wk.row0);
+            } else {
+              pend_map[n_pend] = tmap;
+              pend_c0[n_pend] = tc0;
+              pend_c1[n_pend] = wk.row0;
+              pend_stage[n_pend] = stage;
+              if (++n_pend == C::kStages) release_pending();
             }
             armed |= 1u << stage;
             armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
@@ -291,6 +321,7 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
         }
       }
     }
+    if (lane == 0 && !waited) release_pending();
     // Every load issued must have landed before the CTA leaves.
     if (lane == 0) {
       for (int s = 0; s < C::kStages; ++s)

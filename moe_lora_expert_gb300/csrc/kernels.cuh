@@ -144,6 +144,11 @@ struct GemmParams {
   __nv_bfloat16* out;             // [n, n_feat]
   int* status;
   uint64_t timeout_ns;
+  // 1 when the kernel launched just before this one is the shrink, which
+  // calls griddepcontrol.wait before it lets dependents launch: the routing
+  // tables are then complete when this grid starts, and the weight stream
+  // may begin before this grid's own wait.  0: everything waits first.
+  int tables_ready;
 };
 enum GemmMode { kGateUp = 0, kDown = 1 };
 int gemm_stage_count(int bn);
