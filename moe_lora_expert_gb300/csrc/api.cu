@@ -390,6 +390,11 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
     const int v = std::atoi(env);
     if (v == 1 || (v == 2 && bn >= 128) || (v == 4 && bn == 256)) cl = v;
   }
+  // CTA pairs sharing one M = 256 MMA (wide tiles, no multicast cluster).
+  // MOE_LORA_PAIR=0/1 overrides the default for tuning (128- or 256-wide tiles).
+  bool pair = cl == 1 && moe::gemm_use_pair(bn);
+  if (const char* env = std::getenv("MOE_LORA_PAIR")) pair = cl == 1 && std::atoi(env) != 0 && bn >= 128;
+  if (pair) cl = 2;  // a pair is a cluster of two; each CTA loads bn / 2 token rows
   const int sms = num_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
   const uint64_t timeout_ns =
@@ -520,7 +525,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.status = status;
   gp.timeout_ns = timeout_ns;
   gp.tables_ready = 1;  // launched right after the gate_up shrink (n > 0 here)
-  if (moe::launch_expert_gemm(moe::kGateUp, bn, cl, tm_w13, tm_xp, tm_bgu, tm_u, gp,
+  if (moe::launch_expert_gemm(moe::kGateUp, bn, cl, pair, tm_w13, tm_xp, tm_bgu, tm_u, gp,
                               sms * moe::gemm_ctas_per_sm(bn), stream) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
@@ -550,7 +555,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.lb_row_stride_expert = dn_rs_e;
   gp.out = y;
   gp.tables_ready = lora ? 1 : 0;  // else the gate_up GEMM precedes this launch
-  if (moe::launch_expert_gemm(moe::kDown, bn, cl, tm_w2, tm_h, tm_bdn, tm_v, gp,
+  if (moe::launch_expert_gemm(moe::kDown, bn, cl, pair, tm_w2, tm_h, tm_bdn, tm_v, gp,
                               sms * moe::gemm_ctas_per_sm(bn), stream) !=
       cudaSuccess)
     return MOE_ERR_CUDA;

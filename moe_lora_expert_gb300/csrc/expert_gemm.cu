@@ -43,14 +43,15 @@ namespace moe {
 
 constexpr unsigned kFullMask = 0xFFFFFFFFu;
 
-template <int BN>
+template <int BN, bool PAIR = false>
 struct GemmCfg {
   // Narrow (decode) tiles run two CTAs per SM so that two producers keep TMA
   // loads in flight; wide tiles run one CTA per SM with deeper stages.
   static constexpr int kCtasPerSm = BN <= 64 ? 2 : 1;
   static constexpr int kStageBudget = BN <= 64 ? 96 * 1024 : 200 * 1024;
   static constexpr int kABytes = 128 * 64 * 2;   // 128 rows x 64 K of bf16
-  static constexpr int kBBytes = BN * 64 * 2;    // BN rows x 64 K of bf16
+  // A CTA of a pair holds half of the token tile.
+  static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * 64 * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStagesRaw = kStageBudget / kStageBytes;
   static constexpr int kStages = kStagesRaw > 16 ? 16 : kStagesRaw;
@@ -99,13 +100,16 @@ __device__ __forceinline__ uint64_t tile_adapter_mask(const int32_t* row_adapter
 }
 
 // Bounded wait that also gives up as soon as another role raised the abort flag.
+// CLUSTER: acquire at cluster scope (arrivals come from the peer CTA too).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
                                               volatile int* abort_flag) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  auto probe = [&]() { return CLUSTER ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity); };
+  if (probe()) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_try_wait(a, parity)) return true;
+    if (probe()) return true;
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > limit_ns) return false;
   }
@@ -120,49 +124,71 @@ __device__ __forceinline__ void raise_timeout(int* status, volatile int* abort_f
 // gate_up: the map views w13 so that one box (or four, see the host code)
 // brings gate rows 64 fb + 16q + (0..15) to smem rows 32q + (0..15) and the
 // matching up rows to smem rows 32q + 16 + (0..15), q = 0..3.
-template <int MODE>
+// PAIR: the bytes complete on the pair leader's barrier, ``cbar`` (a
+// shared::cluster address); otherwise on this CTA's ``bar``.
+template <bool PAIR>
+__device__ __forceinline__ void load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, uint32_t cbar,
+                                        int c0, int c1, uint64_t pol) {
+  if constexpr (PAIR) tma_load_2d_pair(dst, map, cbar, c0, c1, pol);
+  else tma_load_2d(dst, map, bar, c0, c1, pol);
+}
+
+template <int MODE, bool PAIR>
 __device__ __forceinline__ void load_weight_block(uint8_t* sA, const CUtensorMap* map,
-                                                  uint64_t* bar, int kc, int e, int fb,
+                                                  uint64_t* bar, uint32_t cbar, int kc, int e, int fb,
                                                   int rows_per_expert, int gu_single_box,
                                                   uint64_t pol) {
   if (MODE == kGateUp) {
     if (gu_single_box) {
       // map dims {H, 16 rows, 2 halves, I/16 groups, E}
-      tma_load_5d(sA, map, bar, kc, 0, 0, fb * 4, e, pol);
+      if constexpr (PAIR) tma_load_5d_pair(sA, map, cbar, kc, 0, 0, fb * 4, e, pol);
+      else tma_load_5d(sA, map, bar, kc, 0, 0, fb * 4, e, pol);
     } else {
       // map dims {H, I, 2E}, box {64, 16, 2}
 #pragma unroll
-      for (int q = 0; q < 4; ++q) tma_load_3d(sA + q * 4096, map, bar, kc, fb * 64 + q * 16, 2 * e, pol);
+      for (int q = 0; q < 4; ++q) {
+        if constexpr (PAIR) tma_load_3d_pair(sA + q * 4096, map, cbar, kc, fb * 64 + q * 16, 2 * e, pol);
+        else tma_load_3d(sA + q * 4096, map, bar, kc, fb * 64 + q * 16, 2 * e, pol);
+      }
     }
   } else {
-    tma_load_2d(sA, map, bar, kc, e * rows_per_expert + fb * 128, pol);
+    load_2d<PAIR>(sA, map, bar, cbar, kc, e * rows_per_expert + fb * 128, pol);
   }
 }
 
 // LoRA B-factor (A operand of the expand) loads: same row arrangement, from
 // the 2-D map over all factor rows (box {64, 16} for gate_up, {64, 128} down).
-template <int MODE>
+template <int MODE, bool PAIR>
 __device__ __forceinline__ void load_lora_b_block(uint8_t* sA, const CUtensorMap* map,
-                                                  uint64_t* bar, int kc, int64_t row_base, int fb,
-                                                  int n_feat, uint64_t pol) {
+                                                  uint64_t* bar, uint32_t cbar, int kc, int64_t row_base,
+                                                  int fb, int n_feat, uint64_t pol) {
   if (MODE == kGateUp) {
 #pragma unroll
     for (int bx = 0; bx < 8; ++bx) {
       const int q = bx >> 1, up = bx & 1;
       const int64_t row = row_base + static_cast<int64_t>(up) * n_feat + fb * 64 + q * 16;
-      tma_load_2d(sA + bx * 2048, map, bar, kc, static_cast<int>(row), pol);
+      load_2d<PAIR>(sA + bx * 2048, map, bar, cbar, kc, static_cast<int>(row), pol);
     }
   } else {
-    tma_load_2d(sA, map, bar, kc, static_cast<int>(row_base + fb * 128), pol);
+    load_2d<PAIR>(sA, map, bar, cbar, kc, static_cast<int>(row_base + fb * 128), pol);
   }
 }
 
-template <int BN, int MODE, int CL>
+// PAIR (CL == 2): the two CTAs of the cluster take adjacent feature blocks
+// of the same token tile and share one M = 256 MMA (cta_group::2).  Each
+// loads its 128 weight rows and half of the token rows; all those bytes
+// complete on the even CTA's barrier, whose MMA warp alone issues the MMAs
+// and commits to both CTAs' barriers.  Each CTA's TMEM receives its own
+// feature block for the whole token tile, so the epilogue is unchanged; the
+// epilogue warps of both CTAs release the even CTA's accumulator barrier.
+template <int BN, int MODE, int CL, bool PAIR>
 __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                        const __grid_constant__ CUtensorMap tm_lb, const __grid_constant__ CUtensorMap tm_lu,
                        const GemmParams p) {
-  using C = GemmCfg<BN>;
+  static_assert(!PAIR || CL == 2, "a pair is a cluster of two");
+  using C = GemmCfg<BN, PAIR>;
+  constexpr bool kMulticast = CL > 1 && !PAIR;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -186,11 +212,13 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], CL);  // every CTA of the cluster releases the stage
+      // multicast: every CTA of the cluster releases the stage; pair: the
+      // leader's commit arrives once in each CTA
+      mbar_init(&empty[s], kMulticast ? CL : 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accf[b], 1);
-      mbar_init(&acce[b], 4);
+      mbar_init(&acce[b], PAIR ? 8 : 4);  // epilogue warps (of both CTAs of a pair)
     }
     mbar_init(drain, 1);
     mbar_init(never, 1);
@@ -206,8 +234,13 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
     }
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {  // collective with the peer's warp 1
+      tmem_alloc_pair(tmem_slot, C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, C::kTmemCols);
+      tmem_relinquish();
+    }
   }
   // Programmatic dependent launch: this grid may start while the previous
   // kernel drains.  When that kernel is the shrink (tables_ready), it waited
@@ -235,6 +268,7 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
   const int total_work = s_ts[p.E] * FBg;
   constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CL) - 1u);
   constexpr int kPieceRows = BN / CL;              // token rows each CTA loads and multicasts
+  const bool leader = !PAIR || crank == 0;
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
@@ -249,9 +283,12 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
     int n_pend = 0;
     const CUtensorMap* pend_map[C::kStages];
     int pend_c0[C::kStages], pend_c1[C::kStages], pend_stage[C::kStages];
+    // Pair: c1 already names this CTA's half of the token tile.
     auto issue_token_load = [&](const CUtensorMap* map, int st, int c0, int c1) {
       uint8_t* sB = smem + st * C::kStageBytes + C::kABytes;
-      if (CL > 1)
+      if constexpr (PAIR)
+        tma_load_2d_pair(sB, map, mapa_shared(smem_u32(&full[st]), 0), c0, c1, pol_x);
+      else if constexpr (kMulticast)
         tma_load_2d_multicast(sB + crank * kPieceRows * 128, map, &full[st], c0,
                               c1 + crank * kPieceRows, kClusterMask, pol_x);
       else
@@ -268,6 +305,8 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
       const Work wk = decode_work<BN>(w, crank, CL, s_off, s_ts, p.E, FBg);
       uint64_t amask = use_lora ? tile_adapter_mask(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
       const int nblocks = nk + __popcll(amask) * lkb;
+      // first token row this CTA loads: a pair splits the MMA's N in halves
+      const int trow = PAIR ? wk.row0 + crank * (((wk.nrows + 31) / 32) * 16) : wk.row0;
       int adapter = -1, j = 0;
       for (int b = 0; b < nblocks; ++b) {
         if (b >= nk) {  // next LoRA block: adapters in ascending order, lkb blocks each
@@ -277,32 +316,33 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
           }
         }
         if (lane == 0) {
-          ok = wait_or_abort(&empty[stage], phase ^ 1, p.timeout_ns, abort_flag);
+          ok = wait_or_abort<PAIR>(&empty[stage], phase ^ 1, p.timeout_ns, abort_flag);
           if (ok) {
             uint8_t* sA = smem + stage * C::kStageBytes;
-            uint8_t* sB = sA + C::kABytes;
-            mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-            (void)sB;
+            // the pair leader counts the bytes of both CTAs
+            if (leader) mbar_arrive_expect_tx(&full[stage], (PAIR ? 2 : 1) * C::kStageBytes);
+            const uint32_t cbar = PAIR ? mapa_shared(smem_u32(&full[stage]), 0) : 0u;
             const CUtensorMap* tmap;
             int tc0;
             if (b < nk) {
-              load_weight_block<MODE>(sA, &tm_w, &full[stage], b * 64, wk.e, wk.fb,
-                                      p.rows_per_expert, p.gu_single_box, pol_w);
+              load_weight_block<MODE, PAIR>(sA, &tm_w, &full[stage], cbar, b * 64, wk.e, wk.fb,
+                                            p.rows_per_expert, p.gu_single_box, pol_w);
               tmap = &tm_x;
               tc0 = b * 64;
             } else {
               const int64_t frow = static_cast<int64_t>(adapter) * p.lb_row_stride_adapter +
                                    static_cast<int64_t>(wk.e) * p.lb_row_stride_expert;
-              load_lora_b_block<MODE>(sA, &tm_lb, &full[stage], j * 64, frow, wk.fb, p.n_feat, pol_x);
+              load_lora_b_block<MODE, PAIR>(sA, &tm_lb, &full[stage], cbar, j * 64, frow, wk.fb,
+                                            p.n_feat, pol_x);
               tmap = &tm_lu;
               tc0 = adapter * p.rank + j * 64;
             }
             if (waited) {
-              issue_token_load(tmap, stage, tc0, wk.row0);
+              issue_token_load(tmap, stage, tc0, trow);
             } else {
               pend_map[n_pend] = tmap;
               pend_c0[n_pend] = tc0;
-              pend_c1[n_pend] = wk.row0;
+              pend_c1[n_pend] = trow;
               pend_stage[n_pend] = stage;
               if (++n_pend == C::kStages) release_pending();
             }
@@ -322,19 +362,26 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
       }
     }
     if (lane == 0 && !waited) release_pending();
-    // Every load issued must have landed before the CTA leaves.
+    // Every load issued must have landed before the CTA leaves.  A pair's
+    // odd CTA cannot wait on the leader's barriers: it waits until the MMA
+    // released each stage it filled last (the data had landed by then).
+    // After an abort nothing may consume the stages any more; loads in
+    // flight land within microseconds, so a short wait suffices then.
     if (lane == 0) {
+      const uint64_t lim = *abort_flag ? 1000000ull : p.timeout_ns;
       for (int s = 0; s < C::kStages; ++s)
-        if (armed & (1u << s))
-          if (!mbar_wait(&full[s], (armed_parity >> s) & 1u, p.timeout_ns))
+        if (armed & (1u << s)) {
+          uint64_t* bar = leader ? &full[s] : &empty[s];
+          if (!mbar_wait(bar, (armed_parity >> s) & 1u, lim))
             set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
+        }
     }
     __syncwarp();
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-    bool ok = true;
-    if (p.debug_stall_mma) {  // failure-path test: this wait can only run out
+    bool ok = leader;  // a pair's odd CTA issues no MMA
+    if (p.debug_stall_mma && leader) {  // failure-path test: this wait can only run out
       if (lane == 0 && !wait_or_abort(never, 0, p.timeout_ns, abort_flag))
         raise_timeout(p.status, abort_flag);
       ok = false;
@@ -345,10 +392,11 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
       const uint64_t amask =
           use_lora ? tile_adapter_mask(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
       const int nblocks = nk + __popcll(amask) * lkb;
-      const int ncols = ((wk.nrows + 15) / 16) * 16;
-      const uint32_t idesc = make_idesc_bf16(128, ncols);
+      // a pair's N is split in halves of 16-row multiples
+      const int ncols = PAIR ? ((wk.nrows + 31) / 32) * 32 : ((wk.nrows + 15) / 16) * 16;
+      const uint32_t idesc = make_idesc_bf16(PAIR ? 256 : 128, ncols);
       if (lane == 0) {
-        ok = wait_or_abort(&acce[acc], acc_phase ^ 1, p.timeout_ns, abort_flag);
+        ok = wait_or_abort<PAIR>(&acce[acc], acc_phase ^ 1, p.timeout_ns, abort_flag);
         if (!ok) raise_timeout(p.status, abort_flag);
       }
       ok = __shfl_sync(kFullMask, ok, 0);
@@ -358,7 +406,7 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
       int j = 0;
       for (int b = 0; b < nblocks; ++b) {
         if (lane == 0) {
-          ok = wait_or_abort(&full[stage], phase, p.timeout_ns, abort_flag);
+          ok = wait_or_abort<PAIR>(&full[stage], phase, p.timeout_ns, abort_flag);
           if (ok) {
             tc_fence_after_sync();
             const uint32_t a_addr = smem_u32(smem + stage * C::kStageBytes);
@@ -369,10 +417,16 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
               const int rem = p.rank - j * 64;
               ksteps = rem >= 64 ? 4 : (rem + 15) / 16;
             }
-            for (int ks = 0; ks < ksteps; ++ks)
-              tc_mma_bf16(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc,
-                          (b > 0 || ks > 0) ? 1u : 0u);
-            if (CL > 1) tc_commit_multicast(&empty[stage], kClusterMask);
+            for (int ks = 0; ks < ksteps; ++ks) {
+              if constexpr (PAIR)
+                tc_mma_bf16_pair(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc,
+                                 (b > 0 || ks > 0) ? 1u : 0u);
+              else
+                tc_mma_bf16(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc,
+                            (b > 0 || ks > 0) ? 1u : 0u);
+            }
+            if constexpr (PAIR) tc_commit_pair(&empty[stage], 0x3);
+            else if constexpr (kMulticast) tc_commit_multicast(&empty[stage], kClusterMask);
             else tc_commit(&empty[stage]);
           } else {
             raise_timeout(p.status, abort_flag);
@@ -387,13 +441,17 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
         }
       }
       if (!ok) break;
-      if (lane == 0) tc_commit(&accf[acc]);
+      if (lane == 0) {
+        if constexpr (PAIR) tc_commit_pair(&accf[acc], 0x3);
+        else tc_commit(&accf[acc]);
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
     // Every MMA issued must be complete before TMEM is released.
-    if (lane == 0) {
-      tc_commit(drain);
+    if (lane == 0 && leader) {
+      if constexpr (PAIR) tc_commit_pair(drain, 0x1);
+      else tc_commit(drain);
       if (!mbar_wait(drain, 0, p.timeout_ns)) set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
     }
     __syncwarp();
@@ -404,10 +462,10 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
     for (int w = unit0; w < total_work; w += unit_step) {
       if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
       const Work wk = decode_work<BN>(w, crank, CL, s_off, s_ts, p.E, FBg);
-      const int ncols = ((wk.nrows + 15) / 16) * 16;
+      const int ncols = PAIR ? ((wk.nrows + 31) / 32) * 32 : ((wk.nrows + 15) / 16) * 16;
       bool ok = true;
       if (lane == 0) {
-        ok = wait_or_abort(&accf[acc], acc_phase, p.timeout_ns, abort_flag);
+        ok = wait_or_abort<PAIR>(&accf[acc], acc_phase, p.timeout_ns, abort_flag);
         if (!ok) raise_timeout(p.status, abort_flag);
       }
       ok = __shfl_sync(kFullMask, ok, 0);
@@ -447,7 +505,10 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
       }
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acce[acc]);
+      if (lane == 0) {
+        if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_u32(&acce[acc]), 0));
+        else mbar_arrive(&acce[acc]);
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
@@ -460,7 +521,8 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
   if (CL > 1) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, C::kTmemCols);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, C::kTmemCols);  // collective with the peer
+    else tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
 
@@ -474,32 +536,32 @@ int gemm_ctas_per_sm(int bn) {
   }
 }
 
-int gemm_stage_count(int bn) {
+int gemm_stage_count(int bn, bool pair) {
   switch (bn) {
     case 16: return GemmCfg<16>::kStages;
     case 32: return GemmCfg<32>::kStages;
     case 64: return GemmCfg<64>::kStages;
-    case 128: return GemmCfg<128>::kStages;
-    default: return GemmCfg<256>::kStages;
+    case 128: return pair ? GemmCfg<128, true>::kStages : GemmCfg<128>::kStages;
+    default: return pair ? GemmCfg<256, true>::kStages : GemmCfg<256>::kStages;
   }
 }
 
-size_t gemm_smem_bytes(int bn) {
+size_t gemm_smem_bytes(int bn, bool pair) {
   switch (bn) {
     case 16: return GemmCfg<16>::kSmemBytes;
     case 32: return GemmCfg<32>::kSmemBytes;
     case 64: return GemmCfg<64>::kSmemBytes;
-    case 128: return GemmCfg<128>::kSmemBytes;
-    default: return GemmCfg<256>::kSmemBytes;
+    case 128: return pair ? GemmCfg<128, true>::kSmemBytes : GemmCfg<128>::kSmemBytes;
+    default: return pair ? GemmCfg<256, true>::kSmemBytes : GemmCfg<256>::kSmemBytes;
   }
 }
 
-template <int BN, int MODE, int CL>
+template <int BN, int MODE, int CL, bool PAIR>
 static cudaError_t launch_one(const CUtensorMap& tm_w, const CUtensorMap& tm_x,
                               const CUtensorMap& tm_lb, const CUtensorMap& tm_lu,
                               const GemmParams& p, int grid, cudaStream_t s) {
-  auto kern = expert_gemm_kernel<BN, MODE, CL>;
-  const int smem = GemmCfg<BN>::kSmemBytes;
+  auto kern = expert_gemm_kernel<BN, MODE, CL, PAIR>;
+  const int smem = GemmCfg<BN, PAIR>::kSmemBytes;
   cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
   if (CL == 1) return launch_pdl(kern, dim3(grid), dim3(192), smem, s, tm_w, tm_x, tm_lb, tm_lu, p);
@@ -535,22 +597,29 @@ static cudaError_t launch_one(const CUtensorMap& tm_w, const CUtensorMap& tm_x,
 // default and kept as a tuning option.
 int gemm_cluster_size(int) { return 1; }
 
-cudaError_t launch_expert_gemm(int mode, int bn, int cl, const CUtensorMap& tm_w,
+// Wide token tiles run as CTA pairs (cta_group::2): each SM then lands half
+// of the token tile per stage, which leaves room for deeper stages.
+bool gemm_use_pair(int bn) { return bn == 256; }
+
+cudaError_t launch_expert_gemm(int mode, int bn, int cl, bool pair, const CUtensorMap& tm_w,
                                const CUtensorMap& tm_x, const CUtensorMap& tm_lb,
                                const CUtensorMap& tm_lu, const GemmParams& p, int grid,
                                cudaStream_t s) {
-#define MOE_GEMM_CASE(BNV, CLV)                                                              \
-  if (bn == BNV && cl == CLV)                                                                \
-    return mode == kGateUp ? launch_one<BNV, kGateUp, CLV>(tm_w, tm_x, tm_lb, tm_lu, p, grid, s) \
-                           : launch_one<BNV, kDown, CLV>(tm_w, tm_x, tm_lb, tm_lu, p, grid, s);
-  MOE_GEMM_CASE(16, 1)
-  MOE_GEMM_CASE(32, 1)
-  MOE_GEMM_CASE(64, 1)
-  MOE_GEMM_CASE(128, 1)
-  MOE_GEMM_CASE(256, 1)
-  MOE_GEMM_CASE(128, 2)
-  MOE_GEMM_CASE(256, 2)
-  MOE_GEMM_CASE(256, 4)
+#define MOE_GEMM_CASE(BNV, CLV, PV)                                                               \
+  if (bn == BNV && cl == CLV && pair == PV)                                                       \
+    return mode == kGateUp                                                                        \
+               ? launch_one<BNV, kGateUp, CLV, PV>(tm_w, tm_x, tm_lb, tm_lu, p, grid, s)          \
+               : launch_one<BNV, kDown, CLV, PV>(tm_w, tm_x, tm_lb, tm_lu, p, grid, s);
+  MOE_GEMM_CASE(16, 1, false)
+  MOE_GEMM_CASE(32, 1, false)
+  MOE_GEMM_CASE(64, 1, false)
+  MOE_GEMM_CASE(128, 1, false)
+  MOE_GEMM_CASE(256, 1, false)
+  MOE_GEMM_CASE(128, 2, false)
+  MOE_GEMM_CASE(256, 2, false)
+  MOE_GEMM_CASE(256, 4, false)
+  MOE_GEMM_CASE(128, 2, true)
+  MOE_GEMM_CASE(256, 2, true)
 #undef MOE_GEMM_CASE
   return cudaErrorInvalidValue;
 }

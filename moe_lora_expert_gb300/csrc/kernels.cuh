@@ -151,13 +151,15 @@ struct GemmParams {
   int tables_ready;
 };
 enum GemmMode { kGateUp = 0, kDown = 1 };
-int gemm_stage_count(int bn);
+int gemm_stage_count(int bn, bool pair);
 int gemm_ctas_per_sm(int bn);
-size_t gemm_smem_bytes(int bn);
+size_t gemm_smem_bytes(int bn, bool pair);
 // cl: CTAs per cluster along the feature blocks (1, or 2/4 for wide token
 // tiles): the cluster's CTAs share each token tile through TMA multicast.
 int gemm_cluster_size(int bn);
-cudaError_t launch_expert_gemm(int mode, int bn, int cl, const CUtensorMap& tm_w,
+// pair: clusters of two CTAs sharing one M = 256 MMA (cta_group::2); cl = 2.
+bool gemm_use_pair(int bn);
+cudaError_t launch_expert_gemm(int mode, int bn, int cl, bool pair, const CUtensorMap& tm_w,
                                const CUtensorMap& tm_x, const CUtensorMap& tm_lb,
                                const CUtensorMap& tm_lu, const GemmParams& p, int grid,
                                cudaStream_t s);

@@ -237,6 +237,7 @@ def test_forward_cluster_sizes(cluster, monkeypatch):
     """Wide token tiles shared by a cluster of CTAs through TMA multicast; I=136
     and H=192 leave feature blocks that do not divide by the cluster size."""
     monkeypatch.setenv("MOE_LORA_CLUSTER", cluster)
+    monkeypatch.setenv("MOE_LORA_PAIR", "0")
     wl = workloads.small_workload("cluster", T=300, H=192, I=136, E=3, top_k=2, num_adapters=3,
                                   rank=16, map_lo=-1, map_hi=2, seed=61)
     inp = workloads.make_inputs(wl)
@@ -244,6 +245,34 @@ def test_forward_cluster_sizes(cluster, monkeypatch):
     assert res["status"] == 0, res["status_str"]
     check_routing(res, inp)
     assert_output_close(res["out64"], oracle.forward_inputs(inp)["out64"], f"cluster={cluster}")
+
+
+@pytest.mark.parametrize("with_lora", [True, False])
+@pytest.mark.parametrize("tile_n", [128, 256])
+def test_forward_cta_pairs(tile_n, with_lora, monkeypatch):
+    """Wide token tiles on CTA pairs that share one M = 256 MMA (cta_group::2).
+    I=136 gives an odd number of gate_up feature blocks (the last pair's second
+    CTA has none); T=700 over 3 experts gives full and partial tiles, some
+    with no valid row in the second CTA's half; without LoRA the down GEMM
+    follows the gate_up GEMM directly."""
+    monkeypatch.setenv("MOE_LORA_PAIR", "1")
+    cases = [
+        workloads.small_workload("pair_odd", T=300, H=192, I=136, E=3, top_k=2, num_adapters=3,
+                                 rank=16, map_lo=-1, map_hi=2, seed=61),
+        workloads.small_workload("pair_tiles", T=700, H=256, I=192, E=3, top_k=2, num_adapters=2,
+                                 rank=32, map_lo=-1, map_hi=1, seed=67),
+        # tiles of a few rows (the second CTA's half is empty) and a single
+        # feature block in both GEMMs (the second CTA has none)
+        workloads.small_workload("pair_tiny", T=20, H=128, I=64, E=8, top_k=2, num_adapters=2,
+                                 rank=8, map_lo=-1, map_hi=1, seed=71),
+    ]
+    for wl in cases:
+        inp = workloads.make_inputs(wl)
+        res = run_gpu(inp, tile_n=tile_n, with_lora=with_lora)
+        assert res["status"] == 0, res["status_str"]
+        check_routing(res, inp)
+        ref = oracle.forward_inputs(inp, with_lora=with_lora)["out64"]
+        assert_output_close(res["out64"], ref, f"{wl.name} tile_n={tile_n} lora={with_lora}")
 
 
 def test_forward_replays_from_a_cuda_graph():
