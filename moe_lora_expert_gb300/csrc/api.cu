@@ -444,7 +444,8 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   fp.e2p = e2p;
   fp.p2e = p2e;
   fp.tile_start = tile_start;
-  fp.tile_width_mask = (1u << moe::tile_width_index(16)) | (1u << moe::tile_width_index(bn));
+  fp.tile_width_mask = (1u << moe::tile_width_index(16)) | (1u << moe::tile_width_index(128)) |
+                       (1u << moe::tile_width_index(bn));
   fp.status = status;
   if (!fuse_route &&
       moe::launch_route_topk(a->router_logits, T, E, K, topk_ids, topk_w, stream) != cudaSuccess)
@@ -503,7 +504,14 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   sp.T = T;
   sp.e2p = e2p;
   sp.mapping = lora ? a->token_lora_mapping : nullptr;
-  if (moe::launch_gather_shrink(sp, static_cast<int>(n), stream) != cudaSuccess) return MOE_ERR_CUDA;
+  // Many rows: 128-row tiles streamed through a cp.async pipeline (the
+  // per-token mode keeps the 16-token kernel).
+  const bool row_blocks = n > 16 * static_cast<int64_t>(sms);
+  sp.tile_start128 = tile_start + moe::tile_width_index(128) * (E + 1);
+  if ((row_blocks && !sp.per_token ? moe::launch_rows_shrink(sp, static_cast<int>(n), stream)
+                                   : moe::launch_gather_shrink(sp, static_cast<int>(n), stream)) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
   if (!mark()) return MOE_ERR_CUDA;
   // 4. gate_up GEMM + LoRA expand + SwiGLU -> h
   GemmParams gp{};
@@ -542,7 +550,9 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
     sp.U = V;
     sp.kc = moe::shrink_chunk(I, r, shrink_budget);
     sp.per_token = 0;
-    if (moe::launch_gather_shrink(sp, static_cast<int>(n), stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if ((row_blocks ? moe::launch_rows_shrink(sp, static_cast<int>(n), stream)
+                    : moe::launch_gather_shrink(sp, static_cast<int>(n), stream)) != cudaSuccess)
+      return MOE_ERR_CUDA;
   }
   if (!mark()) return MOE_ERR_CUDA;
   // 6. down GEMM + LoRA expand -> y

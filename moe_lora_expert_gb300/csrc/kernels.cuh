@@ -100,9 +100,13 @@ struct ShrinkParams {
   int T;
   const int32_t* e2p;           // [T * top_k]
   const int32_t* mapping;       // [T]
+  const int32_t* tile_start128; // [E + 1] prefix of ceil(n_e / 128) (row-block kernel)
 };
 int shrink_chunk(int K, int rank, size_t smem_budget);
 cudaError_t launch_gather_shrink(const ShrinkParams& p, int n_rows, cudaStream_t s);
+// Many rows: 128-row tiles of one expert, K streamed through a cp.async
+// pipeline.  Not for the per-token mode.  Uses p.tile_start128.
+cudaError_t launch_rows_shrink(const ShrinkParams& p, int n_rows, cudaStream_t s);
 
 // ------------------------------------------------- one-CTA permute (fused)
 struct FusedPermuteParams {

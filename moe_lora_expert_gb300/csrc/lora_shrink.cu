@@ -258,4 +258,232 @@ cudaError_t launch_gather_shrink(const ShrinkParams& p, int n_rows, cudaStream_t
 #undef MOE_SHRINK_CASE
 }
 
+// ------------------------------------------------------ row-block variant
+// For many rows (prefill).  One CTA per (128-row tile of one expert, adapter
+// slot a).  The CTA takes the tile's rows of adapter a (slot 0 with a gather
+// to do: all rows, for the copy) and streams K in 64-element chunks through
+// a kRowStages-deep cp.async pipeline; warp w owns compacted rows
+// [16w, 16w + 16) and keeps their u in registers for the whole K, so no
+// cross-warp reduction is needed.  Every thread copies the same 16-byte
+// column of the same four rows in every chunk, so its addresses are worked
+// out once.  Shared tiles store each 128-byte row as
+// eight 16-byte chunks, chunk j at position j ^ 4 (row & 1): the 8 lanes of
+// a quarter-warp read rows g, g' of both parities and four chunks each, and
+// land in 8 distinct bank groups.
+constexpr int kRowStages = 3;
+constexpr int kRowTile = 128;
+
+__host__ __device__ inline size_t rows_shrink_smem_bytes(int rank) {
+  return static_cast<size_t>(kRowStages) * (kRowTile + rank) * 128 +
+         static_cast<size_t>(kRowTile) * rank * 2;
+}
+
+__device__ __forceinline__ int swz16(int row, int j) { return (j ^ ((row & 1) << 2)) * 16; }
+
+template <int NT>
+__global__ void __launch_bounds__(kShrinkThreads) rows_shrink_kernel(const ShrinkParams p) {
+  constexpr int R = 8 * NT;
+  constexpr int kXStage = kRowTile * 128;
+  constexpr int kStage = kXStage + R * 128;
+  extern __shared__ int4 rows_smem[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>(rows_smem);
+  __nv_bfloat16* s_u = reinterpret_cast<__nv_bfloat16*>(stages + kRowStages * kStage);  // [128][R]
+  __shared__ int s_rows[kRowTile];  // tile row of compacted row i
+  __shared__ int s_adp[kRowTile];   // adapter of tile row i
+  __shared__ int s_warp_cnt[kShrinkThreads / 32];
+  __shared__ int s_info[4];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int a = static_cast<int>(blockIdx.y);
+
+  pdl_wait();
+  if (tid == 0) {
+    const int tile = blockIdx.x;
+    int e = -1, row0 = 0, nrows = 0;
+    if (tile < p.tile_start128[p.E]) {
+      int lo = 0, hi = p.E - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.tile_start128[mid] <= tile) lo = mid;
+        else hi = mid - 1;
+      }
+      e = lo;
+      row0 = p.expert_offsets[lo] + (tile - p.tile_start128[lo]) * kRowTile;
+      nrows = min(kRowTile, p.expert_offsets[lo + 1] - row0);
+    }
+    s_info[0] = e;
+    s_info[1] = row0;
+    s_info[2] = nrows;
+  }
+  __syncthreads();
+  const int e = s_info[0], row0 = s_info[1], nrows = s_info[2];
+  if (e < 0) return;
+  const bool lora = NT > 0 && p.U != nullptr;
+  const bool do_gather = p.gathered != nullptr && a == 0;
+
+  // Compact the rows this CTA loads, in tile order (block-wide ballot scan).
+  bool take = false;
+  if (tid < kRowTile) {
+    const int ad = (tid < nrows && lora) ? p.row_adapter[row0 + tid] : -1;
+    s_adp[tid] = ad;
+    take = tid < nrows && (do_gather || ad == a);
+  }
+  const unsigned bal = __ballot_sync(0xFFFFFFFFu, take);
+  if (lane == 0) s_warp_cnt[warp] = __popc(bal);
+  __syncthreads();
+  int before = 0, m = 0;
+  for (int w = 0; w < kShrinkThreads / 32; ++w) {
+    const int c = s_warp_cnt[w];
+    if (w < warp) before += c;
+    m += c;
+  }
+  if (take) s_rows[before + __popc(bal & ((1u << lane) - 1u))] = tid;
+  __syncthreads();
+
+  const int K = p.K;
+  const int nchunks = (K + 63) / 64;
+  const __nv_bfloat16* Af =
+      lora ? p.A + a * p.a_stride_adapter + static_cast<int64_t>(e) * p.a_stride_expert : nullptr;
+  const bool compute = lora && m > 0;
+
+  // This thread's share of every chunk: column jc of compacted rows
+  // (tid >> 3) + 32 q, and column jc of factor row tid >> 3.
+  const int jc = tid & 7;
+  const __nv_bfloat16* xsrc[4];
+  __nv_bfloat16* gdst[4];
+  uint32_t xoff[4];
+  bool xval[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int i = (tid >> 3) + 32 * q;
+    xval[q] = i < m;
+    const int tr = xval[q] ? s_rows[i] : 0;
+    const int src = p.p2e != nullptr ? p.p2e[row0 + tr] / p.top_k : row0 + tr;
+    xsrc[q] = p.X + static_cast<size_t>(src) * K + jc * 8;
+    gdst[q] = do_gather ? p.gathered + static_cast<size_t>(row0 + tr) * K + jc * 8 : nullptr;
+    xoff[q] = static_cast<uint32_t>(i * 128 + swz16(i, jc));
+  }
+  const int fr = tid >> 3;
+  const bool fval = compute && fr < R;
+  const __nv_bfloat16* fsrc = fval ? Af + static_cast<size_t>(fr) * K + jc * 8 : p.X;
+  const uint32_t foff = static_cast<uint32_t>(kXStage + fr * 128 + swz16(fr, jc));
+
+  auto load_chunk = [&](int c, int st) {
+    uint8_t* sx = stages + st * kStage;
+    const int k0 = c * 64;
+    const bool kval = k0 + jc * 8 < K;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) cp_async_16(sx + xoff[q], xsrc[q] + (kval ? k0 : 0), xval[q] && kval);
+    if (fval) cp_async_16(sx + foff, fsrc + (kval ? k0 : 0), kval);
+  };
+
+  float acc[NT > 0 ? NT : 1][4];
+#pragma unroll
+  for (int nt = 0; nt < (NT > 0 ? NT : 1); ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+
+  if (m > 0 && (compute || do_gather)) {
+#pragma unroll
+    for (int st = 0; st < kRowStages - 1; ++st) {
+      if (st < nchunks) load_chunk(st, st);
+      cp_async_commit();
+    }
+    for (int c = 0; c < nchunks; ++c) {
+      cp_async_wait<kRowStages - 2>();
+      __syncthreads();  // chunk c visible to all; stage (c - 1) % S free again
+      {
+        const int cn = c + kRowStages - 1;
+        if (cn < nchunks) load_chunk(cn, cn % kRowStages);
+        cp_async_commit();
+      }
+      const uint8_t* sx = stages + (c % kRowStages) * kStage;
+      const int k0 = c * 64;
+      if (do_gather && k0 + jc * 8 < K) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (xval[q]) *reinterpret_cast<uint4*>(gdst[q] + k0) = *reinterpret_cast<const uint4*>(sx + xoff[q]);
+      }
+      if constexpr (NT > 0) {
+        if (compute && warp * 16 < m) {
+          const uint8_t* sf = sx + kXStage;
+          const int ra = warp * 16 + g, rb = ra + 8;
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2) {
+            const int j = c2 * 4 + t4;
+            const uint4 xa = *reinterpret_cast<const uint4*>(sx + ra * 128 + swz16(ra, j));
+            const uint4 xb = *reinterpret_cast<const uint4*>(sx + rb * 128 + swz16(rb, j));
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const int f = nt * 8 + g;
+              const uint4 fv = *reinterpret_cast<const uint4*>(sf + f * 128 + swz16(f, j));
+              mma_m16n8k16_bf16(acc[nt], xa.x, xb.x, xa.y, xb.y, fv.x, fv.y);
+              mma_m16n8k16_bf16(acc[nt], xa.z, xb.z, xa.w, xb.w, fv.z, fv.w);
+            }
+          }
+        }
+      }
+    }
+    cp_async_wait<0>();
+  }
+  pdl_launch_dependents();
+
+  if constexpr (NT > 0) {
+    if (p.U != nullptr) {
+      // u of the compacted rows into s_u[tile row] (rows of adapter a only);
+      // then columns [a r, a r + r) of every row of the tile: u or 0.
+      for (int i = tid; i < kRowTile * R; i += kShrinkThreads) s_u[i] = __float2bfloat16_rn(0.f);
+      __syncthreads();
+      if (compute && warp * 16 < m) {
+        const float sc = p.scaling[a];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int col = nt * 8 + 2 * t4;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int ci = warp * 16 + g + 8 * h;
+            if (ci < m) {
+              const int tr = s_rows[ci];
+              if (s_adp[tr] == a) {
+                s_u[tr * R + col] = __float2bfloat16_rn(sc * acc[nt][2 * h]);
+                s_u[tr * R + col + 1] = __float2bfloat16_rn(sc * acc[nt][2 * h + 1]);
+              }
+            }
+          }
+        }
+      }
+      __syncthreads();
+      const int ld = p.num_adapters * R;
+      constexpr int vpr = R / 8;
+      for (int v = tid; v < nrows * vpr; v += kShrinkThreads) {
+        const int row = v / vpr, c = (v - row * vpr) * 8;
+        *reinterpret_cast<uint4*>(p.U + static_cast<size_t>(row0 + row) * ld + a * R + c) =
+            *reinterpret_cast<const uint4*>(s_u + row * R + c);
+      }
+    }
+  }
+}
+
+cudaError_t launch_rows_shrink(const ShrinkParams& p, int n_rows, cudaStream_t s) {
+  if (n_rows == 0) return cudaSuccess;
+  const int NT = p.rank / 8;
+  const int tiles = (n_rows + kRowTile - 1) / kRowTile + (p.E < n_rows ? p.E : n_rows);
+  const dim3 grid(tiles, (NT > 0 && p.U != nullptr) ? p.num_adapters : 1);
+  const size_t smem = rows_shrink_smem_bytes(p.U != nullptr ? p.rank : 0);
+#define MOE_ROWS_CASE(N)                                                                          \
+  case N: {                                                                                       \
+    cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(rows_shrink_kernel<N>), (int)smem); \
+    if (err != cudaSuccess) return err;                                                           \
+    return launch_pdl(rows_shrink_kernel<N>, grid, dim3(kShrinkThreads), smem, s, p);             \
+  }
+  switch (p.U != nullptr ? NT : 0) {
+    MOE_ROWS_CASE(0) MOE_ROWS_CASE(1) MOE_ROWS_CASE(2) MOE_ROWS_CASE(3)
+    MOE_ROWS_CASE(4) MOE_ROWS_CASE(5) MOE_ROWS_CASE(6) MOE_ROWS_CASE(7)
+    MOE_ROWS_CASE(8) MOE_ROWS_CASE(9) MOE_ROWS_CASE(10) MOE_ROWS_CASE(11)
+    MOE_ROWS_CASE(12) MOE_ROWS_CASE(13) MOE_ROWS_CASE(14) MOE_ROWS_CASE(15)
+    MOE_ROWS_CASE(16)
+    default: return cudaErrorInvalidValue;
+  }
+#undef MOE_ROWS_CASE
+}
+
 }  // namespace moe

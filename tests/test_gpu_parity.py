@@ -275,6 +275,22 @@ def test_forward_cta_pairs(tile_n, with_lora, monkeypatch):
         assert_output_close(res["out64"], ref, f"{wl.name} tile_n={tile_n} lora={with_lora}")
 
 
+@pytest.mark.parametrize("with_lora", [True, False])
+def test_forward_many_rows_row_block_shrink(with_lora):
+    """T*k = 4000 rows (more than 16 per SM) takes the 128-row-tile shrink with
+    its cp.async pipeline: H=200 and I=72 leave partial 64-column chunks in
+    both shrinks, three adapters and unadapted rows share tiles, rank 24."""
+    wl = workloads.small_workload("rows", T=1000, H=200, I=72, E=5, top_k=4, num_adapters=3,
+                                  rank=24, map_lo=-1, map_hi=2, seed=81)
+    inp = workloads.make_inputs(wl)
+    res = run_gpu(inp, with_lora=with_lora)
+    assert res["status"] == 0, res["status_str"]
+    check_routing(res, inp)
+    tokens = np.arange(0, wl.T, 7)
+    ref = oracle.forward_inputs(inp, tokens=tokens, with_lora=with_lora)["out64"]
+    assert_output_close(res["out64"][tokens], ref, f"rows lora={with_lora}")
+
+
 def test_forward_replays_from_a_cuda_graph():
     """The forward enqueues only launches and memsets: captured into a CUDA graph
     and replayed it gives the eager result bit for bit, also after the inputs
