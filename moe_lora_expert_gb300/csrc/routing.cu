@@ -5,6 +5,8 @@
 // "finalize" of the launcher row in the "Files changed" table of
 // "[WIP][LoRA] BF16 support for the experimental_sgl_trtllm MoE-LoRA path &
 // lora expert_outer_shared" (yushengsu-thu/sglang#4).
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -204,10 +206,18 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(PermuteParams p, int
   const int e = threadIdx.x;
   int total = 0;
   if (e < p.E) {
-    for (int c = 0; c < nchunks; ++c) {
-      const int v = p.chunk_counts[c * p.E + e];
-      p.chunk_counts[c * p.E + e] = total;
-      total += v;
+    // Loads in batches, so that the chain of chunks costs one memory round
+    // trip per 16 chunks instead of one per chunk.
+    constexpr int kBatch = 16;
+    for (int c0 = 0; c0 < nchunks; c0 += kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) v[i] = c0 + i < nchunks ? p.chunk_counts[(c0 + i) * p.E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        if (c0 + i < nchunks) p.chunk_counts[(c0 + i) * p.E + e] = total;
+        total += v[i];
+      }
     }
   }
   const int off = block_exclusive_scan_1024(e < p.E ? total : 0, warp_sums, &s_total);
@@ -229,6 +239,8 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(PermuteParams p) {
   const int x = blockIdx.x * blockDim.x + threadIdx.x;
   if (x >= p.n) return;
   const int id = checked_id(p.topk_ids[x], p.E, p.status, false);
+  // Slots past the routed rows (dropped ids) have no source row.
+  if (x >= p.expert_offsets[p.E]) p.p2e[x] = -1;
   int pidx = -1;
   if (id >= 0) {
     pidx = p.expert_offsets[id] + p.chunk_counts[(x / kPermuteChunk) * p.E + id] + p.e2p[x];
@@ -260,11 +272,6 @@ __global__ void __launch_bounds__(256) permute_gather_kernel(PermuteParams p) {
   for (int v = lane; v < p.H / 8; v += 32) dst[v] = __ldg(src + v);
 }
 
-__global__ void permute_fill_tail_kernel(int32_t* p2e, const int32_t* offsets, int E, int n) {
-  const int x = blockIdx.x * blockDim.x + threadIdx.x;
-  if (x < n && x >= offsets[E]) p2e[x] = -1;
-}
-
 size_t permute_scratch_bytes(int n, int E) {
   const size_t nchunks = (static_cast<size_t>(n) + kPermuteChunk - 1) / kPermuteChunk;
   const size_t a = (nchunks * E * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
@@ -279,7 +286,6 @@ cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s) {
   permute_count_kernel<<<nchunks, 32 * kCountWarps, kCountWarps * p.E * sizeof(int), s>>>(p);
   permute_scan_kernel<<<1, 1024, 0, s>>>(p, nchunks);
   permute_scatter_kernel<<<(p.n + 255) / 256, 256, 0, s>>>(p);
-  permute_fill_tail_kernel<<<(p.n + 255) / 256, 256, 0, s>>>(p.p2e, p.expert_offsets, p.E, p.n);
   if (p.hidden != nullptr && p.permuted != nullptr)
     permute_gather_kernel<<<(p.n + 7) / 8, 256, 0, s>>>(p);
   return cudaGetLastError();
@@ -436,59 +442,94 @@ cudaError_t launch_small_permute(const FusedPermuteParams& p, cudaStream_t s) {
 // float32, rounded to bf16 (nearest even).  One CTA per token, one thread per
 // 8 columns; the slot indices and weights are staged in shared memory first
 // so that each thread's k row loads are independent and issue together.
+// out[t] = sum_j w[t, j] y[e2p[t k + j]], slots in order j = 0..k-1, fp32
+// accumulation.  Persistent: CTA b takes tokens b, b + gridDim.x, ...; each
+// thread owns 8 consecutive columns of one token and loads the next token's
+// slot indices and weights while this token's rows are in flight.  KMAX
+// (>= k) bounds the unrolled slot loops so the indices stay in registers.
+template <int KMAX>
 __global__ void __launch_bounds__(256) finalize_kernel(const __nv_bfloat16* __restrict__ y,
                                                        const int32_t* __restrict__ e2p,
-                                                       const float* __restrict__ w, int k, int H,
-                                                       __nv_bfloat16* __restrict__ out) {
-  __shared__ int s_p[MOE_MAX_TOP_K];
-  __shared__ float s_w[MOE_MAX_TOP_K];
-  const int t = blockIdx.x;
+                                                       const float* __restrict__ w, int T, int k,
+                                                       int H, __nv_bfloat16* __restrict__ out) {
   const int c8 = blockIdx.y * blockDim.x + threadIdx.x;
   pdl_wait();
   pdl_launch_dependents();
-  if (threadIdx.x < k) {
-    s_p[threadIdx.x] = e2p[static_cast<size_t>(t) * k + threadIdx.x];
-    s_w[threadIdx.x] = w[static_cast<size_t>(t) * k + threadIdx.x];
-  }
-  __syncthreads();
   if (c8 * 8 >= H) return;
-  float acc[8];
+  int p_cur[KMAX], p_nxt[KMAX];
+  float w_cur[KMAX], w_nxt[KMAX];
+  auto load_idx = [&](int tok, int (&pp)[KMAX], float (&ww)[KMAX]) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  constexpr int kBatch = 8;
-  for (int j0 = 0; j0 < k; j0 += kBatch) {
-    uint4 v[kBatch];
-#pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      const int p = (j0 + b < k) ? s_p[j0 + b] : -1;
-      v[b] = p >= 0 ? __ldg(reinterpret_cast<const uint4*>(y + static_cast<size_t>(p) * H) + c8)
-                    : make_uint4(0, 0, 0, 0);
+    for (int j = 0; j < KMAX; ++j) {
+      pp[j] = j < k ? __ldg(e2p + static_cast<size_t>(tok) * k + j) : -1;
+      ww[j] = j < k ? __ldg(w + static_cast<size_t>(tok) * k + j) : 0.f;
     }
+  };
+  int t = blockIdx.x;
+  if (t < T) load_idx(t, p_cur, w_cur);
+  for (; t < T; t += gridDim.x) {
+    uint4 v[KMAX];
 #pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      if (j0 + b >= k || s_p[j0 + b] < 0) continue;
-      const float wj = s_w[j0 + b];
-      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v[b]);
+    for (int j = 0; j < KMAX; ++j)
+      v[j] = p_cur[j] >= 0 ? __ldg(reinterpret_cast<const uint4*>(y + static_cast<size_t>(p_cur[j]) * H) + c8)
+                           : make_uint4(0, 0, 0, 0);
+    // the next token's indices while the rows are in flight
+    const int tn = t + static_cast<int>(gridDim.x);
+    if (tn < T) load_idx(tn, p_nxt, w_nxt);
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (p_cur[j] < 0) continue;
+      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v[j]);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float2 f = __bfloat1622float2(h2[i]);
-        acc[2 * i] = fmaf(wj, f.x, acc[2 * i]);
-        acc[2 * i + 1] = fmaf(wj, f.y, acc[2 * i + 1]);
+        acc[2 * i] = fmaf(w_cur[j], f.x, acc[2 * i]);
+        acc[2 * i + 1] = fmaf(w_cur[j], f.y, acc[2 * i + 1]);
       }
     }
-  }
-  uint4 o;
-  __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o);
+    uint4 o;
+    __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) o2[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-  reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H)[c8] = o;
+    for (int i = 0; i < 4; ++i) o2[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H)[c8] = o;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      p_cur[j] = p_nxt[j];
+      w_cur[j] = w_nxt[j];
+    }
+  }
+}
+
+template <int KMAX>
+static cudaError_t launch_finalize_k(const __nv_bfloat16* y, const int32_t* e2p, const float* w,
+                                     int T, int top_k, int H, __nv_bfloat16* out, cudaStream_t s) {
+  constexpr int kMaxDevices = 64;
+  static int ctas[kMaxDevices] = {};  // resident CTAs of the persistent grid, per device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (ctas[dev] == 0) {
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, finalize_kernel<KMAX>, 256, 0) !=
+            cudaSuccess)
+      return cudaErrorUnknown;
+    ctas[dev] = std::max(1, sms * per_sm);
+  }
+  const int ycols = (H / 8 + 255) / 256;
+  const int tok_ctas = std::max(1, std::min(T, ctas[dev] / ycols));
+  return launch_pdl(finalize_kernel<KMAX>, dim3(tok_ctas, ycols), dim3(256), 0, s, y, e2p, w, T,
+                    top_k, H, out);
 }
 
 cudaError_t launch_finalize(const __nv_bfloat16* y, const int32_t* e2p, const float* w, int T,
                             int top_k, int H, __nv_bfloat16* out, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const dim3 grid(T, (H / 8 + 255) / 256);
-  return launch_pdl(finalize_kernel, grid, dim3(256), 0, s, y, e2p, w, top_k, H, out);
+  if (top_k <= 8) return launch_finalize_k<8>(y, e2p, w, T, top_k, H, out, s);
+  if (top_k <= 16) return launch_finalize_k<16>(y, e2p, w, T, top_k, H, out, s);
+  return launch_finalize_k<MOE_MAX_TOP_K>(y, e2p, w, T, top_k, H, out, s);
 }
 
 }  // namespace moe
