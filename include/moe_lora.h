@@ -220,6 +220,21 @@ typedef struct {
  *   stage_events: NULL, or an array of MOE_NUM_STAGE_EVENTS cudaEvent_t
  *     that are recorded on ``stream`` before the first stage, between
  *     stages and after the last one (unused slots are recorded at the end).
+ *   Expert parallelism (the local_expert_offset / local_num_experts
+ *   arguments of trtllm_bf16_routed_moe_lora in "[WIP][LoRA] BF16 support for
+ *   the experimental_sgl_trtllm MoE-LoRA path & lora expert_outer_shared"):
+ *     num_router_experts: experts the router scores (router_logits is then
+ *       [T, num_router_experts]); 0 = E, no sharding.
+ *     local_expert_offset: this call holds experts [offset, offset + E) of
+ *       them; w13, w2 and the LoRA factors are indexed by the local expert.
+ *     Routing is global (topk_ids_out holds global ids); slots routed to
+ *     experts of other shards are skipped (expanded_to_permuted = -1), so
+ *     ``out`` is this shard's partial sum and the sum of ``out`` over a
+ *     partition of the experts is the layer output (the caller all-reduces).
+ *     Requires E <= num_router_experts <= MOE_MAX_EXPERTS and
+ *     0 <= offset <= num_router_experts - E, else MOE_ERR_SHAPE.  Callers
+ *     built against the header without these two fields pass the smaller
+ *     struct_size and get no sharding.
  * ------------------------------------------------------------------------- */
 typedef struct {
   uint32_t struct_size;           /* sizeof(moe_lora_args_t) */
@@ -243,6 +258,8 @@ typedef struct {
   uint32_t debug_flags;           /* 0 in normal use; see MOE_DEBUG_* */
   struct CUevent_st* const* stage_events;
   const float* adapter_scaling;   /* HOST array [num_adapters] or NULL */
+  int local_expert_offset;        /* expert parallelism; 0 without sharding */
+  int num_router_experts;         /* 0 = E */
 } moe_lora_args_t;
 
 /* Test-only flag for debug_flags: the gate_up GEMM's MMA role first waits on

@@ -68,7 +68,8 @@ class MoeLoraArgs(ctypes.Structure):
                 ("tile_n", ctypes.c_int), ("wait_timeout_ms", ctypes.c_int),
                 ("debug_flags", ctypes.c_uint32),
                 ("stage_events", ctypes.c_void_p),
-                ("adapter_scaling", ctypes.c_void_p)]
+                ("adapter_scaling", ctypes.c_void_p),
+                ("local_expert_offset", ctypes.c_int), ("num_router_experts", ctypes.c_int)]
 
 
 class WorkspacePlan(ctypes.Structure):
@@ -226,12 +227,20 @@ class MoeLoraLayer:
     w13 [E, 2I, H] bf16, w2 [E, H, I] bf16.  LoRA factors (bf16, optional):
     A_gu [A, E, r, H] or shared [A, r, H]; B_gu [A, E, 2I, r];
     A_dn [A, E, r, I]; B_dn [A, E, H, r] or shared [A, H, r].
+
+    Expert parallelism: ``num_router_experts`` > E makes this layer one shard
+    holding experts [local_expert_offset, local_expert_offset + E) of a router
+    over num_router_experts experts (router_logits [T, num_router_experts]);
+    its forward returns the shard's partial sum (see ``ep``).
     """
 
     def __init__(self, w13, w2, top_k: int, A_gu=None, B_gu=None, A_dn=None, B_dn=None,
-                 scaling: float = 1.0, max_tokens: int = 0, adapter_scaling=None):
+                 scaling: float = 1.0, max_tokens: int = 0, adapter_scaling=None,
+                 local_expert_offset: int = 0, num_router_experts: int = 0):
         torch = _torch()
         self.E, twoI, self.H = w13.shape
+        self.local_expert_offset = int(local_expert_offset)
+        self.num_router_experts = int(num_router_experts) or self.E
         self.I = twoI // 2
         _require(w13, torch.bfloat16, (self.E, 2 * self.I, self.H), "w13")
         _require(w2, torch.bfloat16, (self.E, self.H, self.I), "w2")
@@ -299,6 +308,7 @@ class MoeLoraLayer:
         a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
         a.tile_n, a.wait_timeout_ms = int(tile_n), int(wait_timeout_ms)
         a.debug_flags = int(debug_flags)
+        a.local_expert_offset, a.num_router_experts = self.local_expert_offset, self.num_router_experts
         a.adapter_scaling = ctypes.cast(self._scales, ctypes.c_void_p) if self._scales is not None else None
         self._events_keepalive = None
         if stage_events is not None:
@@ -318,7 +328,7 @@ class MoeLoraLayer:
         torch = _torch()
         T = hidden.shape[0]
         _require(hidden, torch.bfloat16, (T, self.H), "hidden")
-        _require(router_logits, torch.float32, (T, self.E), "router_logits")
+        _require(router_logits, torch.float32, (T, self.num_router_experts), "router_logits")
         if token_lora_mapping is not None:
             _require(token_lora_mapping, torch.int32, (T,), "token_lora_mapping")
         if out is None:

@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstddef>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -295,11 +296,17 @@ int moe_read_device_status(const void* workspace, moe_stream_t stream) {
 
 int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   if (a == nullptr) return MOE_ERR_NULL;
-  if (a->struct_size < sizeof(moe_lora_args_t)) return MOE_ERR_UNSUPPORTED;
+  // Structures from before the expert-parallel fields end at adapter_scaling.
+  constexpr size_t kSizeNoShard = offsetof(moe_lora_args_t, local_expert_offset);
+  if (a->struct_size < kSizeNoShard) return MOE_ERR_UNSUPPORTED;
+  const bool has_shard = a->struct_size >= sizeof(moe_lora_args_t);
   const int T = a->T, H = a->H, I = a->I, E = a->E, K = a->top_k;
+  const int shard_off = has_shard ? a->local_expert_offset : 0;
+  const int R = (has_shard && a->num_router_experts != 0) ? a->num_router_experts : E;
   if (!sizes_ok(T, H, I, E, K, a->num_adapters, a->rank)) return MOE_ERR_SHAPE;
   int st = limits_status(H, I, E, K, a->num_adapters, a->rank);
   if (st != MOE_OK) return st;
+  if (R < E || R > MOE_MAX_EXPERTS || K > R || shard_off < 0 || shard_off > R - E) return MOE_ERR_SHAPE;
   const bool lora = a->num_adapters > 0 && a->rank > 0;
   const int A = lora ? a->num_adapters : 0;
   const int r = lora ? a->rank : 0;
@@ -382,7 +389,10 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   __nv_bfloat16* V = reinterpret_cast<__nv_bfloat16*>(ws + pl.lora_v);
   __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(ws + pl.act);
 
-  const int bn = a->tile_n ? a->tile_n : auto_tile_n(static_cast<int>(n), E);
+  // Rows this shard expects (all of them without sharding): the tile width
+  // and the shrink variant follow the rows per local expert.
+  const int64_t n_local = n * E / R;
+  const int bn = a->tile_n ? a->tile_n : auto_tile_n(static_cast<int>(n_local), E);
   // CTAs per cluster sharing a token tile (TMA multicast).  MOE_LORA_CLUSTER
   // overrides the default for tuning (1, 2 or 4; 4 only with 256-wide tiles).
   int cl = moe::gemm_cluster_size(bn);
@@ -447,8 +457,10 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   fp.tile_width_mask = (1u << moe::tile_width_index(16)) | (1u << moe::tile_width_index(128)) |
                        (1u << moe::tile_width_index(bn));
   fp.status = status;
+  fp.id_offset = shard_off;
+  fp.id_limit = R;
   if (!fuse_route &&
-      moe::launch_route_topk(a->router_logits, T, E, K, topk_ids, topk_w, stream) != cudaSuccess)
+      moe::launch_route_topk(a->router_logits, T, R, K, topk_ids, topk_w, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!mark()) return MOE_ERR_CUDA;
   if (small_permute) {
@@ -471,13 +483,15 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
     pp.chunk_counts = chunk_counts;
     pp.tile_start = tile_start;
     pp.status = status;
+    pp.id_offset = shard_off;
+    pp.id_limit = R;
     if (moe::launch_permute(pp, stream) != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (!mark()) return MOE_ERR_CUDA;
   // 3. row gather + gate_up LoRA shrink: xp = hidden[t(p)], U = s * A_gu x
   //    (one-hot per adapter).  Few tiles (decode): one phase per CTA; many
   //    tiles: smaller phases so that several CTAs share an SM.
-  const size_t shrink_budget = n <= 16 * static_cast<int64_t>(sms) ? 200 * 1024 : 72 * 1024;
+  const size_t shrink_budget = n_local <= 16 * static_cast<int64_t>(sms) ? 200 * 1024 : 72 * 1024;
   ShrinkParams sp{};
   sp.X = static_cast<const __nv_bfloat16*>(a->hidden);
   sp.p2e = p2e;
@@ -506,7 +520,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   sp.mapping = lora ? a->token_lora_mapping : nullptr;
   // Many rows: 128-row tiles streamed through a cp.async pipeline (the
   // per-token mode keeps the 16-token kernel).
-  const bool row_blocks = n > 16 * static_cast<int64_t>(sms);
+  const bool row_blocks = n_local > 16 * static_cast<int64_t>(sms);
   sp.tile_start128 = tile_start + moe::tile_width_index(128) * (E + 1);
   if ((row_blocks && !sp.per_token ? moe::launch_rows_shrink(sp, static_cast<int>(n), stream)
                                    : moe::launch_gather_shrink(sp, static_cast<int>(n), stream)) !=

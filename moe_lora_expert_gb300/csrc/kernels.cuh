@@ -64,6 +64,11 @@ struct PermuteParams {
   int32_t* chunk_counts;        // [nchunks, E]
   int32_t* tile_start;          // [kNumTileWidths, E + 1] or null
   int* status;
+  // Expert parallelism: ids are global in [0, id_limit); this call holds
+  // experts [id_offset, id_offset + E); other ids are dropped.  Without
+  // sharding id_offset = 0, id_limit = E.
+  int id_offset;
+  int id_limit;
 };
 constexpr int kPermuteChunk = 1024;
 size_t permute_scratch_bytes(int n, int E);
@@ -123,6 +128,8 @@ struct FusedPermuteParams {
   int32_t* tile_start;          // [kNumTileWidths, E + 1] or null
   uint32_t tile_width_mask;     // bit i: write the prefix for width 16 << i
   int* status;                  // cleared by the kernel
+  int id_offset;                // as in PermuteParams; logits are [T, id_limit]
+  int id_limit;
 };
 bool small_permute_fits(int n, int E);
 cudaError_t launch_small_permute(const FusedPermuteParams& p, cudaStream_t s);

@@ -160,6 +160,7 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
           const int rc = v / vpr, c = (v - rc * vpr) * 8;
           const int row = rc / copies, j = rc - row * copies;
           const int dst = p.per_token ? p.e2p[(row0 + row) * p.top_k + j] : row0 + row;
+          if (dst < 0) continue;  // slot not routed here (dropped id, another shard's expert)
           *reinterpret_cast<uint4*>(p.gathered + static_cast<size_t>(dst) * K + kc0 + c) =
               *reinterpret_cast<const uint4*>(Xs + row * pitch + c);
         }
@@ -218,6 +219,7 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
       const int c = (v - rc * vec_per_row) * 8;
       const int row = rc / copies, j = rc - row * copies;
       const int dst = p.per_token ? p.e2p[(row0 + row) * p.top_k + j] : row0 + row;
+      if (dst < 0) continue;  // slot not routed here
       uint4 val = zero;
       if (s_adapter[row] == ad) val = *reinterpret_cast<const uint4*>(s_u + row * R + c);
       *reinterpret_cast<uint4*>(p.U + static_cast<size_t>(dst) * ld + ad * R + c) = val;

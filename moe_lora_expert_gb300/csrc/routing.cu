@@ -125,6 +125,18 @@ __device__ __forceinline__ int checked_id(int id, int E, int* status, bool repor
   return id;
 }
 
+// Expert parallelism: a routed id is global in [0, id_limit); this call holds
+// experts [id_offset, id_offset + E).  Returns the local expert, or -1 for a
+// slot that is not routed, or routed to another shard's expert (dropped
+// without error).  Ids outside [-1, id_limit) are reported as bad.
+__device__ __forceinline__ int local_id(int id, int id_offset, int E, int id_limit, int* status,
+                                        bool report) {
+  const int g = checked_id(id, id_limit, status, report);
+  if (g < 0) return -1;
+  const int e = g - id_offset;
+  return (e >= 0 && e < E) ? e : -1;
+}
+
 // 8 warps per 1024-slot chunk; warp w ranks slots [128w, 128w + 128) of the
 // chunk with its own counters, then the counters are merged by a prefix over
 // the warps, so ranks follow the slot order of the whole chunk.
@@ -142,7 +154,7 @@ __global__ void __launch_bounds__(32 * kCountWarps) permute_count_kernel(Permute
   for (int x0 = base; x0 < end; x0 += 32) {
     const int x = x0 + lane;
     const bool valid = x < end;
-    const int id = valid ? checked_id(p.topk_ids[x], p.E, p.status, true) : -1;
+    const int id = valid ? local_id(p.topk_ids[x], p.id_offset, p.E, p.id_limit, p.status, true) : -1;
     const bool routed = id >= 0;
     const unsigned group = __match_any_sync(kFull, routed ? id : -2);
     const int rank = __popc(group & lt_mask);
@@ -166,7 +178,7 @@ __global__ void __launch_bounds__(32 * kCountWarps) permute_count_kernel(Permute
   if (base < end) {
     for (int x = base + lane; x < end; x += 32) {
       const int r = p.e2p[x];
-      if (r >= 0) p.e2p[x] = r + my[checked_id(p.topk_ids[x], p.E, p.status, false)];
+      if (r >= 0) p.e2p[x] = r + my[local_id(p.topk_ids[x], p.id_offset, p.E, p.id_limit, p.status, false)];
     }
   }
 }
@@ -238,7 +250,7 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(PermuteParams p, int
 __global__ void __launch_bounds__(256) permute_scatter_kernel(PermuteParams p) {
   const int x = blockIdx.x * blockDim.x + threadIdx.x;
   if (x >= p.n) return;
-  const int id = checked_id(p.topk_ids[x], p.E, p.status, false);
+  const int id = local_id(p.topk_ids[x], p.id_offset, p.E, p.id_limit, p.status, false);
   // Slots past the routed rows (dropped ids) have no source row.
   if (x >= p.expert_offsets[p.E]) p.p2e[x] = -1;
   int pidx = -1;
@@ -280,7 +292,9 @@ size_t permute_scratch_bytes(int n, int E) {
   return a + b;
 }
 
-cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s) {
+cudaError_t launch_permute(const PermuteParams& pin, cudaStream_t s) {
+  PermuteParams p = pin;
+  if (p.id_limit <= 0) p.id_limit = p.E;  // no sharding
   if (p.n == 0) return cudaSuccess;
   const int nchunks = (p.n + kPermuteChunk - 1) / kPermuteChunk;
   permute_count_kernel<<<nchunks, 32 * kCountWarps, kCountWarps * p.E * sizeof(int), s>>>(p);
@@ -324,16 +338,17 @@ __global__ void __launch_bounds__(1024) small_permute_kernel(const FusedPermuteP
     for (int t = warp; t < p.T; t += 32) {
       int id;
       float wt;
-      route_token<EPL>(p.logits + static_cast<size_t>(t) * E, E, k, lane, &id, &wt);
+      route_token<EPL>(p.logits + static_cast<size_t>(t) * p.id_limit, p.id_limit, k, lane, &id, &wt);
       if (lane < k) {
-        p.topk_ids[t * k + lane] = id;
+        p.topk_ids[t * k + lane] = id;  // global id
         p.topk_w[t * k + lane] = wt;
-        s_ids[t * k + lane] = static_cast<int16_t>(id);
+        const int e = id - p.id_offset;
+        s_ids[t * k + lane] = static_cast<int16_t>(e >= 0 && e < E ? e : -1);
       }
     }
   } else {
     for (int x = tid; x < n; x += blockDim.x)
-      s_ids[x] = static_cast<int16_t>(checked_id(p.topk_ids[x], E, p.status, true));
+      s_ids[x] = static_cast<int16_t>(local_id(p.topk_ids[x], p.id_offset, E, p.id_limit, p.status, true));
   }
   __syncthreads();
 
@@ -418,10 +433,12 @@ bool small_permute_fits(int n, int E) {
   return n <= 8192 && small_permute_smem(n, E) <= 200 * 1024;
 }
 
-cudaError_t launch_small_permute(const FusedPermuteParams& p, cudaStream_t s) {
+cudaError_t launch_small_permute(const FusedPermuteParams& pin, cudaStream_t s) {
+  FusedPermuteParams p = pin;
+  if (p.id_limit <= 0) p.id_limit = p.E;  // no sharding
   const int n = p.T * p.top_k;
   const size_t smem = small_permute_smem(n, p.E);
-  const int epl = (p.E + 31) / 32;
+  const int epl = (p.id_limit + 31) / 32;  // routing scores all id_limit experts
 #define MOE_SMALL_CASE(V)                                                                         \
   {                                                                                               \
     cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(small_permute_kernel<V>), (int)smem); \
@@ -438,10 +455,6 @@ cudaError_t launch_small_permute(const FusedPermuteParams& p, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------- finalize
-// out[t, :] = sum_j w[t, j] * y[e2p[t*k + j], :], summed in slot order in
-// float32, rounded to bf16 (nearest even).  One CTA per token, one thread per
-// 8 columns; the slot indices and weights are staged in shared memory first
-// so that each thread's k row loads are independent and issue together.
 // out[t] = sum_j w[t, j] y[e2p[t k + j]], slots in order j = 0..k-1, fp32
 // accumulation.  Persistent: CTA b takes tokens b, b + gridDim.x, ...; each
 // thread owns 8 consecutive columns of one token and loads the next token's

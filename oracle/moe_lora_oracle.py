@@ -240,8 +240,18 @@ def expert_slot(x, w13_e, w2_e, lora_gu: Optional[LoraFactors], lora_dn: Optiona
 
 def moe_lora_forward(hidden_bits, logits, w13_bits, w2_bits, mapping, top_k, scaling=2.0,
                      lora_gu: Optional[LoraFactors] = None, lora_dn: Optional[LoraFactors] = None,
-                     tokens: Optional[Sequence[int]] = None, keep_intermediates=False):
+                     tokens: Optional[Sequence[int]] = None, keep_intermediates=False,
+                     local_expert_offset: int = 0):
     """The whole layer forward for the listed tokens (default: all).
+
+    Expert parallelism (the local_expert_offset / local_num_experts arguments
+    of trtllm_bf16_routed_moe_lora, sglang PR #28953 summary page; the slots
+    of other ranks' experts carry permuted index -1 there): the router scores
+    all logits.shape[1] experts, while w13_bits, w2_bits and the LoRA factors
+    hold only experts [local_expert_offset, local_expert_offset + E) and are
+    indexed by the local expert.  Slots routed elsewhere contribute nothing,
+    so ``out`` is this shard's part of the sum that the downstream all-reduce
+    completes (Flow 1(A), "downstream all_reduce (in qwen3_moe)").
 
     Routing is computed for every token (it is cheap); the expert work and
     the output only for ``tokens``.  The expert loop visits the experts one
@@ -265,11 +275,13 @@ def moe_lora_forward(hidden_bits, logits, w13_bits, w2_bits, mapping, top_k, sca
     out = np.zeros((len(tokens), H), dtype=np.float64)
     inter = {}
 
-    # slots grouped by expert: expert -> [(token, slot)]
+    # slots grouped by local expert: expert -> [(token, slot)]
     by_expert = {}
     for t in tokens:
         for j in range(top_k):
-            by_expert.setdefault(int(ids[t, j]), []).append((t, j))
+            e = int(ids[t, j]) - local_expert_offset
+            if 0 <= e < E:
+                by_expert.setdefault(e, []).append((t, j))
 
     # y for every slot first; the weighted sum then runs in slot order.
     y_slot = {}
@@ -288,7 +300,8 @@ def moe_lora_forward(hidden_bits, logits, w13_bits, w2_bits, mapping, top_k, sca
     for t in tokens:
         acc = np.zeros(H, dtype=np.float64)
         for j in range(top_k):
-            acc = acc + w[t, j] * y_slot[(t, j)]
+            if (t, j) in y_slot:          # slots of other shards are skipped
+                acc = acc + w[t, j] * y_slot[(t, j)]
         out[row_of[t]] = acc
 
     res = {"ids": ids, "w": w, "tokens": tokens, "out64": out, "out_bf16": f64_to_bf16_bits(out)}
@@ -307,12 +320,15 @@ def factors_from_inputs(inp):
     return gu, dn
 
 
-def forward_inputs(inp, tokens=None, keep_intermediates=False, with_lora=True):
-    """Run ``moe_lora_forward`` on a ``workloads.LayerInputs``."""
+def forward_inputs(inp, tokens=None, keep_intermediates=False, with_lora=True,
+                   local_expert_offset=0):
+    """Run ``moe_lora_forward`` on a ``workloads.LayerInputs`` (for a shard of
+    the experts: the sliced inputs and the shard's first expert)."""
     gu, dn = factors_from_inputs(inp) if with_lora else (None, None)
     wl = inp.wl
     return moe_lora_forward(inp.hidden, inp.logits, inp.w13, inp.w2, inp.mapping, wl.top_k,
-                            wl.scaling, gu, dn, tokens=tokens, keep_intermediates=keep_intermediates)
+                            wl.scaling, gu, dn, tokens=tokens, keep_intermediates=keep_intermediates,
+                            local_expert_offset=local_expert_offset)
 
 
 # ---------------------------------------------------------------------------

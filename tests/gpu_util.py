@@ -39,14 +39,16 @@ def cached_inputs(name):
     return workloads.make_inputs(workloads.WORKLOADS[name])
 
 
-def make_layer(inp, with_lora=True):
+def make_layer(inp, with_lora=True, **shard):
+    """``shard``: local_expert_offset / num_router_experts for an expert shard."""
     import moe_lora_expert_gb300 as m
     wl = inp.wl
     if with_lora and inp.A_gu is not None:
         return m.MoeLoraLayer(bf16_tensor(inp.w13), bf16_tensor(inp.w2), wl.top_k,
                               bf16_tensor(inp.A_gu), bf16_tensor(inp.B_gu), bf16_tensor(inp.A_dn),
-                              bf16_tensor(inp.B_dn), scaling=wl.scaling)
-    return m.MoeLoraLayer(bf16_tensor(inp.w13), bf16_tensor(inp.w2), wl.top_k, scaling=wl.scaling)
+                              bf16_tensor(inp.B_dn), scaling=wl.scaling, **shard)
+    return m.MoeLoraLayer(bf16_tensor(inp.w13), bf16_tensor(inp.w2), wl.top_k, scaling=wl.scaling,
+                          **shard)
 
 
 def run_gpu(inp, layer=None, tile_n=0, with_lora=True, mapping=None):
@@ -86,11 +88,19 @@ def assert_output_close(got, ref, label=""):
     return rel
 
 
-def check_routing(res, inp):
-    """ids and the permutation bit-exact; weights within W_RTOL."""
+def check_routing(res, inp, shard=None):
+    """ids and the permutation bit-exact; weights within W_RTOL.  ``shard`` =
+    (offset, count) of an expert shard: the ids stay global, the permutation
+    is over the shard's experts, other slots dropped (-1)."""
     ids_ref, w_ref = oracle.route_topk(inp.logits, inp.wl.top_k)
     assert np.array_equal(res["ids"], ids_ref), "routing ids differ from the oracle"
     np.testing.assert_allclose(res["w"], w_ref, rtol=W_RTOL, atol=1e-9)
-    _, e2p_ref, _ = oracle.permute(ids_ref, inp.wl.E)
+    if shard is None:
+        _, e2p_ref, _ = oracle.permute(ids_ref, inp.wl.E)
+    else:
+        off, cnt = shard
+        local = ids_ref - off
+        local = np.where((local >= 0) & (local < cnt), local, -1).astype(np.int32)
+        _, e2p_ref, _ = oracle.permute(local, cnt)
     assert np.array_equal(res["e2p"], e2p_ref), "expanded_to_permuted differs from the oracle"
     return ids_ref

@@ -152,6 +152,18 @@ def _valid_args(**over):
     ({"down": m.LoraFactors(1 << 20, 1 << 20, 8, 8, 24, 0)}, m.MOE_ERR_ALIGN),   # b stride % r
     ({"down": m.LoraFactors(1 << 20, 1 << 20, -8, 0, 0, 0)}, m.MOE_ERR_SHAPE),
     ({"down": m.LoraFactors(1 << 20, None, 8, 8, 16, 0)}, m.MOE_ERR_NULL),
+    # expert parallelism: shard outside the router's experts, router too wide
+    ({"num_router_experts": 256, "local_expert_offset": 129}, m.MOE_ERR_SHAPE),
+    ({"num_router_experts": 256, "local_expert_offset": -1}, m.MOE_ERR_SHAPE),
+    ({"num_router_experts": 64}, m.MOE_ERR_SHAPE),                     # fewer than E
+    ({"num_router_experts": 2048, "local_expert_offset": 0}, m.MOE_ERR_SHAPE),
+    ({"local_expert_offset": 1}, m.MOE_ERR_SHAPE),                     # no room without a router width
+    # a valid shard passes the shard checks (then fails on the fake workspace size)
+    ({"num_router_experts": 256, "local_expert_offset": 128, "workspace_bytes": 1024},
+     m.MOE_ERR_WORKSPACE),
+    # a structure from before the shard fields: no sharding, checks go on
+    ({"struct_size": ctypes.sizeof(m.MoeLoraArgs) - 8, "hidden": None}, m.MOE_ERR_NULL),
+    ({"struct_size": ctypes.sizeof(m.MoeLoraArgs) - 12}, m.MOE_ERR_UNSUPPORTED),
 ])
 def test_forward_rejects_on_host(lib, over, status):
     a = _valid_args(**over)

@@ -155,6 +155,31 @@ def small_workload(name="custom", T=8, H=64, I=32, E=4, top_k=2, num_adapters=2,
                     shared_outer, bias_sigma, seed)
 
 
+def shard_experts(inp: "LayerInputs", offset: int, count: int) -> "LayerInputs":
+    """The inputs of one expert-parallel shard: experts [offset, offset + count).
+
+    Weights and per-expert LoRA factors are sliced along the expert axis (a
+    shared factor is kept whole); the router logits keep all experts, since
+    routing is global.  ``wl.E`` becomes ``count``, the number of local
+    experts.
+    """
+    sl = slice(offset, offset + count)
+    shared = inp.wl.shared_outer
+
+    def cut(x, keep_whole=False):
+        if x is None:
+            return None
+        return np.ascontiguousarray(x if keep_whole else x[:, sl])
+
+    return LayerInputs(
+        wl=dataclasses.replace(inp.wl, E=count),
+        logits=inp.logits, hidden=inp.hidden,
+        w13=np.ascontiguousarray(inp.w13[sl]), w2=np.ascontiguousarray(inp.w2[sl]),
+        A_gu=cut(inp.A_gu, keep_whole=shared), B_gu=cut(inp.B_gu),
+        A_dn=cut(inp.A_dn), B_dn=cut(inp.B_dn, keep_whole=shared),
+        mapping=inp.mapping)
+
+
 def make_peft_adapters(wl: Workload, specs, seed: int = 7):
     """Draw PEFT-style adapters for the layer shape of ``wl``.
 
