@@ -372,6 +372,46 @@ def run_ours(args):
     e2e = {"value": world * wl.T * e2e_steps / (e_ms / 1e3), "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": wl.T * wl.H * 2}
 
+    # ---------------- the same steps replayed from CUDA graphs: the forward
+    # alone, and the whole host-to-host step (copies + forward + copy back)
+    def e2e_step():
+        d_hidden.copy_(h_hidden, non_blocking=True)
+        d_logits.copy_(h_logits, non_blocking=True)
+        if lora:
+            d_mapping.copy_(h_mapping, non_blocking=True)
+        layer.forward(d_hidden, d_logits, d_mapping, out=out, tile_n=args.tile_n)
+        h_out.copy_(out, non_blocking=True)
+
+    def replay_ms(g, n):
+        total = 0.0
+        for i in range(args.warmup + n):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            e1.synchronize()
+            if i >= args.warmup:
+                total += e0.elapsed_time(e1)
+        return total
+
+    g_fwd, g_e2e = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g_fwd):
+        step()
+    with torch.cuda.graph(g_e2e):
+        e2e_step()
+    torch.cuda.synchronize()
+    gf_ms = max_over_ranks(replay_ms(g_fwd, e2e_steps), pg, dev)
+    ge_ms = max_over_ranks(replay_ms(g_e2e, e2e_steps), pg, dev)
+    st = layer.device_status()
+    if st != m.MOE_OK:
+        raise SystemExit(f"device status after graph replays: {m.status_string(st)}")
+    graph = {"forward_us_per_step": round(gf_ms / e2e_steps * 1e3, 2),
+             "forward_value": round(world * wl.T * e2e_steps / (gf_ms / 1e3), 1),
+             "e2e_value": round(world * wl.T * e2e_steps / (ge_ms / 1e3), 1), "unit": "tokens/s",
+             "note": "one CUDA graph per step, replayed; e2e_value includes the host copies"}
+
     if rank != 0:
         if pg:
             pg.destroy_process_group()
@@ -419,7 +459,7 @@ def run_ours(args):
                    "l2": "flushed before every step (256 MiB write, outside the step events)",
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": roof, "forward_roofline": fwd, "stages_us": stages_us,
-        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_kernels * args.steps,
+        "cpu_baseline": cpu, "e2e": e2e, "graph": graph, "gpu_launches": n_kernels * args.steps,
         "clocks": clk, "wall_s_timed_region": round(wall, 4),
     }
     print(json.dumps(line))
