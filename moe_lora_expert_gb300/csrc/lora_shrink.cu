@@ -55,14 +55,20 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
   __shared__ int s_src[16];
   __shared__ int s_info[3];
   __shared__ int s_ok;
+  __shared__ int s_ts[MOE_MAX_EXPERTS + 1];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
 
   pdl_wait();
+  // The tile prefix comes to shared memory in one coalesced pass, so that
+  // the search below costs no chain of global round trips.
+  if (!p.per_token)
+    for (int i = tid; i <= p.E; i += kShrinkThreads) s_ts[i] = p.tile_start16[i];
+  __syncthreads();
   if (tid == 0) {
     const int tile = blockIdx.x;
-    const int total = p.per_token ? (p.T + 15) / 16 : p.tile_start16[p.E];
+    const int total = p.per_token ? (p.T + 15) / 16 : s_ts[p.E];
     int e = -1, row0 = 0, nrows = 0;
     if (p.per_token && tile < total) {
       e = 0;  // the factor does not depend on the expert
@@ -72,11 +78,11 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
       int lo = 0, hi = p.E - 1;
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (p.tile_start16[mid] <= tile) lo = mid;
+        if (s_ts[mid] <= tile) lo = mid;
         else hi = mid - 1;
       }
       e = lo;
-      row0 = p.expert_offsets[lo] + (tile - p.tile_start16[lo]) * 16;
+      row0 = p.expert_offsets[lo] + (tile - s_ts[lo]) * 16;
       nrows = min(16, p.expert_offsets[lo + 1] - row0);
     }
     s_info[0] = e;
@@ -294,24 +300,27 @@ __global__ void __launch_bounds__(kShrinkThreads) rows_shrink_kernel(const Shrin
   __shared__ int s_adp[kRowTile];   // adapter of tile row i
   __shared__ int s_warp_cnt[kShrinkThreads / 32];
   __shared__ int s_info[4];
+  __shared__ int s_ts[MOE_MAX_EXPERTS + 1];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int a = static_cast<int>(blockIdx.y);
 
   pdl_wait();
+  for (int i = tid; i <= p.E; i += kShrinkThreads) s_ts[i] = p.tile_start128[i];
+  __syncthreads();
   if (tid == 0) {
     const int tile = blockIdx.x;
     int e = -1, row0 = 0, nrows = 0;
-    if (tile < p.tile_start128[p.E]) {
+    if (tile < s_ts[p.E]) {
       int lo = 0, hi = p.E - 1;
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (p.tile_start128[mid] <= tile) lo = mid;
+        if (s_ts[mid] <= tile) lo = mid;
         else hi = mid - 1;
       }
       e = lo;
-      row0 = p.expert_offsets[lo] + (tile - p.tile_start128[lo]) * kRowTile;
+      row0 = p.expert_offsets[lo] + (tile - s_ts[lo]) * kRowTile;
       nrows = min(kRowTile, p.expert_offsets[lo + 1] - row0);
     }
     s_info[0] = e;

@@ -138,7 +138,25 @@ EDGE = [
                              rank=16, bias_sigma=4.0, seed=50),
     workloads.small_workload("many_chunks", T=1500, H=64, I=64, E=32, top_k=2, num_adapters=2,
                              rank=8, seed=51),
+    # the ABI's maximum expert count and top-k (one-CTA permute, 32-slot finalize)
+    workloads.small_workload("max_experts_top32", T=40, H=64, I=64, E=1024, top_k=32,
+                             num_adapters=2, rank=8, map_lo=-1, map_hi=1, seed=52),
 ]
+
+
+def test_forward_max_experts_many_rows():
+    """1024 experts and 24000 rows: the multi-kernel permute with its largest
+    counter arrays and the 128-row-tile shrink over 1024 experts; the oracle
+    checks every 11th token."""
+    wl = workloads.small_workload("max_experts_rows", T=3000, H=64, I=64, E=1024, top_k=8,
+                                  num_adapters=3, rank=16, map_lo=-1, map_hi=2, seed=53)
+    inp = workloads.make_inputs(wl)
+    res = run_gpu(inp)
+    assert res["status"] == 0, res["status_str"]
+    check_routing(res, inp)
+    tokens = np.arange(0, wl.T, 11)
+    assert_output_close(res["out64"][tokens], oracle.forward_inputs(inp, tokens=tokens)["out64"],
+                        wl.name)
 
 
 @pytest.mark.parametrize("wl", EDGE, ids=lambda w: w.name)
