@@ -383,6 +383,8 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   const size_t nchunks = (static_cast<size_t>(n) + moe::kPermuteChunk - 1) / moe::kPermuteChunk;
   int32_t* tile_start = reinterpret_cast<int32_t*>(
       ws + pl.permute_scratch + align_up(nchunks * E * sizeof(int32_t)));
+  uint64_t* gmask = reinterpret_cast<uint64_t*>(
+      reinterpret_cast<uint8_t*>(tile_start) + align_up(moe::kNumTileWidths * (E + 1) * sizeof(int32_t)));
   __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(ws + pl.permuted_hidden);
   __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(ws + pl.expert_out);
   __nv_bfloat16* U = reinterpret_cast<__nv_bfloat16*>(ws + pl.lora_u);
@@ -457,6 +459,10 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   fp.tile_width_mask = (1u << moe::tile_width_index(16)) | (1u << moe::tile_width_index(128)) |
                        (1u << moe::tile_width_index(bn));
   fp.status = status;
+  // Per 16-row tile, the adapters of its GEMM tile: lets the 16-row shrink
+  // skip (tile, adapter) pairs without work.
+  fp.gmask = (lora && small_permute) ? gmask : nullptr;
+  fp.gemm_bn = bn;
   fp.id_offset = shard_off;
   fp.id_limit = R;
   if (!fuse_route &&
@@ -522,6 +528,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   // per-token mode keeps the 16-token kernel).
   const bool row_blocks = n_local > 16 * static_cast<int64_t>(sms);
   sp.tile_start128 = tile_start + moe::tile_width_index(128) * (E + 1);
+  sp.gmask = fp.gmask;
   if ((row_blocks && !sp.per_token ? moe::launch_rows_shrink(sp, static_cast<int>(n), stream)
                                    : moe::launch_gather_shrink(sp, static_cast<int>(n), stream)) !=
       cudaSuccess)

@@ -71,7 +71,10 @@ struct PermuteParams {
   int id_limit;
 };
 constexpr int kPermuteChunk = 1024;
+// Counting-sort scratch: chunk counts [nchunks, E], the tile prefixes
+// [kNumTileWidths, E + 1], then the 16-row-tile adapter masks (gmask_bytes).
 size_t permute_scratch_bytes(int n, int E);
+size_t gmask_bytes(int n, int E);
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s);
 
 // ------------------------------------------------- gather + LoRA shrink
@@ -106,6 +109,11 @@ struct ShrinkParams {
   const int32_t* e2p;           // [T * top_k]
   const int32_t* mapping;       // [T]
   const int32_t* tile_start128; // [E + 1] prefix of ceil(n_e / 128) (row-block kernel)
+  // Or null.  gmask[t]: adapters present in the expert-GEMM token tile that
+  // contains 16-row tile t.  The CTA of (t, adapter a) exits at once when a is
+  // absent there (no GEMM tile reads a's columns of these rows), unless it
+  // owes the row gather (adapter slot 0).
+  const uint64_t* gmask;
 };
 int shrink_chunk(int K, int rank, size_t smem_budget);
 cudaError_t launch_gather_shrink(const ShrinkParams& p, int n_rows, cudaStream_t s);
@@ -130,6 +138,11 @@ struct FusedPermuteParams {
   int* status;                  // cleared by the kernel
   int id_offset;                // as in PermuteParams; logits are [T, id_limit]
   int id_limit;
+  // Or null: per 16-row tile, the adapter mask of the enclosing gemm_bn-wide
+  // GEMM tile (see ShrinkParams::gmask); needs row_adapter and the 16-wide
+  // tile prefix (tile_width_mask bit 0).
+  uint64_t* gmask;
+  int gemm_bn;
 };
 bool small_permute_fits(int n, int E);
 cudaError_t launch_small_permute(const FusedPermuteParams& p, cudaStream_t s);

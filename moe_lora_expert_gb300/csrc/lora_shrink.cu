@@ -61,6 +61,19 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
   const int g = lane >> 2, t4 = lane & 3;
 
   pdl_wait();
+  if (p.gmask != nullptr && !p.per_token) {
+    // One round trip decides whether this (tile, adapter slot) has work.
+    if (tid == 0) {
+      const int tile = blockIdx.x;
+      const int count = p.tile_start16[p.E];
+      const uint64_t m = p.gmask[tile];
+      const int ad = static_cast<int>(blockIdx.y);
+      const bool needed = ((m >> ad) & 1ull) != 0 || (p.gathered != nullptr && ad == 0);
+      s_ok = (tile < count && needed) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!s_ok) return;
+  }
   // The tile prefix comes to shared memory in one coalesced pass, so that
   // the search below costs no chain of global round trips.
   if (!p.per_token)

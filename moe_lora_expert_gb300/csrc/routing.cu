@@ -289,7 +289,12 @@ size_t permute_scratch_bytes(int n, int E) {
   const size_t a = (nchunks * E * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
   const size_t b = (static_cast<size_t>(kNumTileWidths) * (E + 1) * sizeof(int32_t) + 255) &
                    ~static_cast<size_t>(255);
-  return a + b;
+  return a + b + gmask_bytes(n, E);
+}
+
+size_t gmask_bytes(int n, int E) {
+  const size_t tiles16 = (static_cast<size_t>(n) + 15) / 16 + E + 1;
+  return (tiles16 * sizeof(uint64_t) + 255) & ~static_cast<size_t>(255);
 }
 
 cudaError_t launch_permute(const PermuteParams& pin, cudaStream_t s) {
@@ -322,10 +327,15 @@ __global__ void __launch_bounds__(1024) small_permute_kernel(const FusedPermuteP
   extern __shared__ int4 small_smem[];
   const int n = p.T * p.top_k, E = p.E, k = p.top_k;
   const int n2 = (n + 1) & ~1;
-  int16_t* s_ids = reinterpret_cast<int16_t*>(small_smem);
+  // 8-byte words first (the dynamic shared memory base is 16-byte aligned):
+  // the adapters of each 16-row tile (p.gmask only)
+  const int ntiles16 = (n + 15) / 16 + E + 1;
+  unsigned long long* s_m16 = reinterpret_cast<unsigned long long*>(small_smem);
+  int16_t* s_ids = reinterpret_cast<int16_t*>(s_m16 + ntiles16);
   int16_t* s_local = s_ids + n2;
   int* s_cnt = reinterpret_cast<int*>(s_local + n2);
   int* s_off = s_cnt + 32 * E;
+  int* s_t16 = s_off + (E + 1);  // 16-wide tile prefix
   __shared__ int warp_sums[32];
   __shared__ int s_total;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -396,8 +406,14 @@ __global__ void __launch_bounds__(1024) small_permute_kernel(const FusedPermuteP
       const int ts = block_exclusive_scan_1024(tiles, warp_sums, &s_total);
       if (tid < E) p.tile_start[wi * (E + 1) + tid] = ts;
       if (tid == 0) p.tile_start[wi * (E + 1) + E] = s_total;
+      if (bn == 16) {
+        if (tid < E) s_t16[tid] = ts;
+        if (tid == 0) s_t16[E] = s_total;
+      }
     }
   }
+  if (p.gmask != nullptr)
+    for (int i = tid; i < ntiles16; i += blockDim.x) s_m16[i] = 0ull;
   __syncthreads();
   pdl_launch_dependents();
 
@@ -417,16 +433,39 @@ __global__ void __launch_bounds__(1024) small_permute_kernel(const FusedPermuteP
           }
         }
         p.row_adapter[pidx] = a;
+        if (p.gmask != nullptr && a >= 0)
+          atomicOr(&s_m16[s_t16[id] + (pidx - s_off[id]) / 16], 1ull << a);
       }
     }
     p.e2p[x] = pidx;
   }
   for (int x = s_off[E] + tid; x < n; x += blockDim.x) p.p2e[x] = -1;
+  if (p.gmask != nullptr) {
+    __syncthreads();  // every 16-row tile's adapters are in s_m16
+    const int ntiles = s_t16[E];
+    const int per = p.gemm_bn / 16;  // 16-row tiles per GEMM tile
+    for (int t = tid; t < ntiles; t += blockDim.x) {
+      int lo = 0, hi = E - 1;  // expert of 16-row tile t
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_t16[mid] <= t) lo = mid;
+        else hi = mid - 1;
+      }
+      // the GEMM tile starts at a multiple of gemm_bn rows within the expert
+      const int first = s_t16[lo] + ((t - s_t16[lo]) / per) * per;
+      const int last = min(first + per, s_t16[lo + 1]);
+      unsigned long long m = 0;
+      for (int u = first; u < last; ++u) m |= s_m16[u];
+      p.gmask[t] = m;
+    }
+  }
 }
 
 size_t small_permute_smem(int n, int E) {
   const size_t n2 = (static_cast<size_t>(n) + 1) & ~static_cast<size_t>(1);
-  return n2 * 2 * 2 + static_cast<size_t>(32) * E * 4 + (static_cast<size_t>(E) + 1) * 4;
+  const size_t tiles16 = (static_cast<size_t>(n) + 15) / 16 + E + 1;
+  return tiles16 * 8 + n2 * 2 * 2 + static_cast<size_t>(32) * E * 4 +
+         2 * (static_cast<size_t>(E) + 1) * 4;
 }
 
 bool small_permute_fits(int n, int E) {
