@@ -526,7 +526,11 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   sp.mapping = lora ? a->token_lora_mapping : nullptr;
   // Many rows: 128-row tiles streamed through a cp.async pipeline (the
   // per-token mode keeps the 16-token kernel).
-  const bool row_blocks = n_local > 16 * static_cast<int64_t>(sms);
+  // Many rows, or a large rank with several rows per expert (the factor is
+  // then read once per 128 rows instead of once per 16): 128-row tiles.
+  bool row_blocks = n_local > 16 * static_cast<int64_t>(sms) ||
+                    (r >= 64 && n_local >= 8 * std::min<int64_t>(E, n_local));
+  if (const char* env = std::getenv("MOE_LORA_SHRINK_ROWS")) row_blocks = std::atoi(env) != 0;  // tuning
   sp.tile_start128 = tile_start + moe::tile_width_index(128) * (E + 1);
   sp.gmask = fp.gmask;
   if ((row_blocks && !sp.per_token ? moe::launch_rows_shrink(sp, static_cast<int>(n), stream)

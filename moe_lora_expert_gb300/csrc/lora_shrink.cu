@@ -134,7 +134,11 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
 #pragma unroll
     for (int i = 0; i < 16; ++i) present |= (s_adapter[i] == ad);
   }
-  const bool do_gather = p.gathered != nullptr && ad == 0;
+  // Row gather: slot 0's CTA copies each row; in the per-token mode a token's
+  // top_k copies are shared out over the adapter-slot CTAs of the tile
+  // (slot j goes to CTA j mod gridDim.y).
+  const int gshare = p.per_token ? static_cast<int>(gridDim.y) : 1;
+  const bool do_gather = p.gathered != nullptr && (p.per_token ? ad < p.top_k : ad == 0);
   const int passes = (present || do_gather) ? 1 : 0;
   const int K = p.K;
   uint32_t parity = 0;
@@ -174,10 +178,11 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
       parity ^= 1;
       if (do_gather) {
         const int vpr = cur / 8;
-        const int copies = p.per_token ? p.top_k : 1;  // every permuted row of the token
+        // permuted rows of a token this CTA copies: slots ad, ad + gshare, ...
+        const int copies = p.per_token ? (p.top_k - ad + gshare - 1) / gshare : 1;
         for (int v = tid; v < nrows * copies * vpr; v += kShrinkThreads) {
           const int rc = v / vpr, c = (v - rc * vpr) * 8;
-          const int row = rc / copies, j = rc - row * copies;
+          const int row = rc / copies, j = ad + (rc - row * copies) * gshare;
           const int dst = p.per_token ? p.e2p[(row0 + row) * p.top_k + j] : row0 + row;
           if (dst < 0) continue;  // slot not routed here (dropped id, another shard's expert)
           *reinterpret_cast<uint4*>(p.gathered + static_cast<size_t>(dst) * K + kc0 + c) =
@@ -372,7 +377,7 @@ __global__ void __launch_bounds__(kShrinkThreads) rows_shrink_kernel(const Shrin
   const bool compute = lora && m > 0;
 
   // This thread's share of every chunk: column jc of compacted rows
-  // (tid >> 3) + 32 q, and column jc of factor row tid >> 3.
+  // (tid >> 3) + 32 q, and column jc of factor rows (tid >> 3) + 32 q.
   const int jc = tid & 7;
   const __nv_bfloat16* xsrc[4];
   __nv_bfloat16* gdst[4];
@@ -388,10 +393,17 @@ __global__ void __launch_bounds__(kShrinkThreads) rows_shrink_kernel(const Shrin
     gdst[q] = do_gather ? p.gathered + static_cast<size_t>(row0 + tr) * K + jc * 8 : nullptr;
     xoff[q] = static_cast<uint32_t>(i * 128 + swz16(i, jc));
   }
-  const int fr = tid >> 3;
-  const bool fval = compute && fr < R;
-  const __nv_bfloat16* fsrc = fval ? Af + static_cast<size_t>(fr) * K + jc * 8 : p.X;
-  const uint32_t foff = static_cast<uint32_t>(kXStage + fr * 128 + swz16(fr, jc));
+  constexpr int kFQ = (R + 31) / 32;  // factor rows per thread (rank up to 128)
+  const __nv_bfloat16* fsrc[kFQ > 0 ? kFQ : 1];
+  uint32_t foff[kFQ > 0 ? kFQ : 1];
+  bool fval[kFQ > 0 ? kFQ : 1];
+#pragma unroll
+  for (int q = 0; q < kFQ; ++q) {
+    const int fr = (tid >> 3) + 32 * q;
+    fval[q] = compute && fr < R;
+    fsrc[q] = fval[q] ? Af + static_cast<size_t>(fr) * K + jc * 8 : p.X;
+    foff[q] = static_cast<uint32_t>(kXStage + fr * 128 + swz16(fr, jc));
+  }
 
   auto load_chunk = [&](int c, int st) {
     uint8_t* sx = stages + st * kStage;
@@ -399,7 +411,9 @@ __global__ void __launch_bounds__(kShrinkThreads) rows_shrink_kernel(const Shrin
     const bool kval = k0 + jc * 8 < K;
 #pragma unroll
     for (int q = 0; q < 4; ++q) cp_async_16(sx + xoff[q], xsrc[q] + (kval ? k0 : 0), xval[q] && kval);
-    if (fval) cp_async_16(sx + foff, fsrc + (kval ? k0 : 0), kval);
+#pragma unroll
+    for (int q = 0; q < kFQ; ++q)
+      if (fval[q]) cp_async_16(sx + foff[q], fsrc[q] + (kval ? k0 : 0), kval);
   };
 
   float acc[NT > 0 ? NT : 1][4];

@@ -309,6 +309,22 @@ def test_forward_many_rows_row_block_shrink(with_lora):
     assert_output_close(res["out64"][tokens], ref, f"rows lora={with_lora}")
 
 
+@pytest.mark.parametrize("rank", [64, 128])
+def test_forward_many_rows_large_rank(rank):
+    """The 128-row-tile shrink with ranks above 32 (each thread then copies
+    several factor rows per chunk) and shared-outer factors."""
+    wl = workloads.small_workload("rows_rank", T=700, H=192, I=64, E=6, top_k=4, num_adapters=2,
+                                  rank=rank, map_lo=-1, map_hi=1, shared_outer=(rank == 64),
+                                  seed=90 + rank)
+    inp = workloads.make_inputs(wl)
+    res = run_gpu(inp)
+    assert res["status"] == 0, res["status_str"]
+    check_routing(res, inp)
+    tokens = np.arange(0, wl.T, 5)
+    ref = oracle.forward_inputs(inp, tokens=tokens)["out64"]
+    assert_output_close(res["out64"][tokens], ref, f"rank {rank}")
+
+
 def test_forward_replays_from_a_cuda_graph():
     """The forward enqueues only launches and memsets: captured into a CUDA graph
     and replayed it gives the eager result bit for bit, also after the inputs
