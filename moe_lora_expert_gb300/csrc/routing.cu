@@ -20,9 +20,11 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 
 // ------------------------------------------------------------------ router
 // One warp per token.  Expert i lives in lane i % 32, register slot i / 32.
-// A selection key orders by the float32 logit (as a sortable integer, -0
-// folded onto +0) and, among equal logits, by the lower expert id; 0 marks
-// "already taken / no expert".  Every real key is > 0.
+// The selection key is the float32 logit as a sortable unsigned integer
+// (-0 folded onto +0); 0 marks "already taken / no expert" (every finite
+// logit has a key > 0).  Each round takes the largest key with two warp
+// reductions (redux.sync): the maximum key, then the lowest expert id among
+// the lanes holding it, so equal logits go to the lower id.
 __device__ __forceinline__ uint32_t float_order_bits(float l) {
   uint32_t b = __float_as_uint(l);
   if (b == 0x80000000u) b = 0u;
@@ -39,32 +41,35 @@ __device__ __forceinline__ float float_from_order_bits(uint32_t o) {
 template <int EPL>
 __device__ __forceinline__ void route_token(const float* __restrict__ row, int E, int k, int lane,
                                             int* out_id, float* out_w) {
-  uint64_t key[EPL];
+  uint32_t key[EPL];
 #pragma unroll
   for (int s = 0; s < EPL; ++s) {
     const int i = s * 32 + lane;
-    key[s] = (i < E) ? ((static_cast<uint64_t>(float_order_bits(row[i])) << 32) |
-                        static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(i)))
-                     : 0ull;
+    key[s] = (i < E) ? float_order_bits(row[i]) : 0u;
   }
 
   float my_logit = 0.f;  // lane j keeps slot j
   int my_id = 0;
   for (int j = 0; j < k; ++j) {
-    uint64_t best = 0;
-#pragma unroll
-    for (int s = 0; s < EPL; ++s) best = key[s] > best ? key[s] : best;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const uint64_t o = __shfl_xor_sync(kFull, best, off);
-      best = o > best ? o : best;
-    }
-    const uint32_t idx = 0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFull);
+    // this lane's best: the largest key, the lowest slot (= id) among equals
+    uint32_t best = 0u;
+    int bs = 0;
 #pragma unroll
     for (int s = 0; s < EPL; ++s)
-      if (static_cast<uint32_t>(s * 32 + lane) == idx) key[s] = 0ull;
+      if (key[s] > best) {
+        best = key[s];
+        bs = s;
+      }
+    const uint32_t m = __reduce_max_sync(kFull, best);
+    const uint32_t cand = (best == m) ? static_cast<uint32_t>(bs * 32 + lane) : 0xFFFFFFFFu;
+    const uint32_t idx = __reduce_min_sync(kFull, cand);
+    if (static_cast<int>(idx & 31u) == lane) {
+#pragma unroll
+      for (int s = 0; s < EPL; ++s)
+        if (static_cast<uint32_t>(s) == (idx >> 5)) key[s] = 0u;
+    }
     if (lane == j) {
-      my_logit = float_from_order_bits(static_cast<uint32_t>(best >> 32));
+      my_logit = float_from_order_bits(m);
       my_id = static_cast<int>(idx);
     }
   }
