@@ -167,11 +167,17 @@ int num_sms() {
   return n;
 }
 
+// Token-tile width from the rows per expert.  avg assumes every expert is
+// routed to; skewed routing touches fewer experts with more rows each, and a
+// tile narrower than an expert's rows streams that expert's weights once per
+// tile.  So: the power of two >= 2 avg, raised up to 64 (still two CTAs per
+// SM) when 4 avg reaches it.
 int auto_tile_n(int n_rows, int E) {
   const int touched = std::max(1, std::min(E, n_rows));
   const int avg = (n_rows + touched - 1) / touched;
   int bn = 16;
   while (bn < 256 && bn < 2 * avg) bn *= 2;
+  while (bn < 64 && bn < 4 * avg) bn *= 2;
   return bn;
 }
 
