@@ -310,6 +310,87 @@ def moe_lora_forward(hidden_bits, logits, w13_bits, w2_bits, mapping, top_k, sca
     return res
 
 
+# ---------------------------------------------------------------------------
+# FP8 block-scaled expert weights (the FP8 block-quant checkpoints of the
+# pages' sibling path, trtllm_fp8_block_scale_routed_moe_lora, summary of
+# "[WIP][LoRA] BF16 support for the experimental_sgl_trtllm MoE-LoRA path &
+# lora expert_outer_shared").  Reading: float8 e4m3 (finite-only variant: no
+# infinities, 0x7F/0xFF are NaN, max 448) with one float32 scale per 128 x 128
+# block of (rows, K); the activations stay bf16.
+# ---------------------------------------------------------------------------
+
+def e4m3_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Decode float8 e4m3 bit patterns (uint8): sign, 4 exponent bits with
+    bias 7, 3 mantissa bits; exponent 0 is subnormal (m/8 * 2^-6); exponent 15
+    with mantissa 7 is NaN (there is no infinity)."""
+    table = np.empty(256, dtype=np.float64)
+    for c in range(256):
+        sgn = -1.0 if c & 0x80 else 1.0
+        e = (c >> 3) & 0xF
+        m = c & 0x7
+        if e == 0xF and m == 0x7:
+            table[c] = np.nan
+        elif e == 0:
+            table[c] = sgn * (m / 8.0) * 2.0 ** -6
+        else:
+            table[c] = sgn * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return table[np.asarray(bits, dtype=np.uint8)]
+
+
+def dequant_fp8_blocks(q_bits: np.ndarray, scale: np.ndarray, block: int = 128) -> np.ndarray:
+    """w[e, n, k] = e4m3(q[e, n, k]) * scale[e, n // block, k // block], float64."""
+    q = e4m3_to_f64(q_bits)
+    E, N, K = q.shape
+    s = np.repeat(np.repeat(np.asarray(scale, dtype=np.float64), block, axis=1), block, axis=2)
+    return q * s[:, :N, :K]
+
+
+def f64_weights_to_bf16_bits_exact(w: np.ndarray) -> np.ndarray:
+    """float64 weights -> the uint16 layout moe_lora_forward reads, only for
+    values that bf16 holds exactly (checked)."""
+    bits = (w.astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    assert np.array_equal(bf16_bits_to_f64(bits), w), "weights not exact in bf16"
+    return bits
+
+
+def moe_lora_forward_fp8(hidden_bits, logits, w13_q, w13_scale, w2_q, w2_scale, mapping, top_k,
+                         scaling=2.0, lora_gu=None, lora_dn=None, tokens=None,
+                         local_expert_offset=0):
+    """The layer forward with FP8 block-scaled expert weights: the weights are
+    dequantized (e4m3 value times its block's scale, in float64) and the
+    forward is then exactly ``moe_lora_forward``'s."""
+    w13 = dequant_fp8_blocks(w13_q, w13_scale)
+    w2 = dequant_fp8_blocks(w2_q, w2_scale)
+    hidden_bits = np.asarray(hidden_bits)
+    T, H = hidden_bits.shape
+    E = w13.shape[0]
+    ids, w = route_topk(logits, top_k)
+    tokens = list(range(T)) if tokens is None else list(tokens)
+    out = np.zeros((len(tokens), H), dtype=np.float64)
+    for i, t in enumerate(tokens):
+        x = bf16_bits_to_f64(hidden_bits[t])
+        a = int(mapping[t])
+        acc = np.zeros(H, dtype=np.float64)
+        for j in range(top_k):
+            e = int(ids[t, j]) - local_expert_offset
+            if not 0 <= e < E:
+                continue
+            _, _, y = expert_slot(x, w13[e], w2[e], lora_gu, lora_dn, a, e, scaling)
+            acc = acc + w[t, j] * y
+        out[i] = acc
+    return {"ids": ids, "w": w, "tokens": tokens, "out64": out, "out_bf16": f64_to_bf16_bits(out)}
+
+
+def forward_inputs_fp8(inp, fp8, tokens=None, with_lora=True):
+    """``moe_lora_forward_fp8`` on a ``workloads.LayerInputs`` and its
+    (w13_q, w13_scale, w2_q, w2_scale)."""
+    gu, dn = factors_from_inputs(inp) if with_lora else (None, None)
+    wl = inp.wl
+    q13, s13, q2, s2 = fp8
+    return moe_lora_forward_fp8(inp.hidden, inp.logits, q13, s13, q2, s2, inp.mapping, wl.top_k,
+                                wl.scaling, gu, dn, tokens=tokens)
+
+
 def factors_from_inputs(inp):
     """Wrap a ``workloads.LayerInputs`` LoRA set as oracle factors (None when absent)."""
     if inp.A_gu is None:

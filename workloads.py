@@ -155,6 +155,42 @@ def small_workload(name="custom", T=8, H=64, I=32, E=4, top_k=2, num_adapters=2,
                     shared_outer, bias_sigma, seed)
 
 
+FP8_BLOCK = 128          # weight block (rows x K) sharing one scale
+FP8_E4M3_MAX = 448.0    # largest finite float8 e4m3 value
+
+
+def quantize_fp8_blocks(w_bits: np.ndarray):
+    """Block-quantize bf16 weights [E, N, K] (uint16 bits) to float8 e4m3.
+
+    How an FP8 block-scaled checkpoint is made (upstream of the layer): per
+    expert and 128 x 128 block of (rows, K), scale = max|w| / 448 (1 for an
+    all-zero block) and q = e4m3(w / scale), rounded to nearest even by
+    torch's float8_e4m3fn conversion.  Returns (q bits uint8 [E, N, K],
+    scales float32 [E, ceil(N/128), ceil(K/128)]).
+    """
+    import torch
+    E, N, K = w_bits.shape
+    B = FP8_BLOCK
+    nb, kb = (N + B - 1) // B, (K + B - 1) // B
+    w = (w_bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    pad = np.zeros((E, nb * B, kb * B), dtype=np.float32)
+    pad[:, :N, :K] = w
+    blocks = pad.reshape(E, nb, B, kb, B)
+    amax = np.abs(blocks).max(axis=(2, 4))
+    scale = np.where(amax > 0, amax / np.float32(FP8_E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    scaled = blocks / scale[:, :, None, :, None]
+    q = torch.from_numpy(np.ascontiguousarray(scaled)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    q = q.reshape(E, nb * B, kb * B)[:, :N, :K]
+    return np.ascontiguousarray(q), scale
+
+
+def fp8_weights(inp: "LayerInputs"):
+    """(w13_q, w13_scale, w2_q, w2_scale) for a layer's bf16 weights."""
+    q13, s13 = quantize_fp8_blocks(inp.w13)
+    q2, s2 = quantize_fp8_blocks(inp.w2)
+    return q13, s13, q2, s2
+
+
 def shard_experts(inp: "LayerInputs", offset: int, count: int) -> "LayerInputs":
     """The inputs of one expert-parallel shard: experts [offset, offset + count).
 
