@@ -356,27 +356,35 @@ def f64_weights_to_bf16_bits_exact(w: np.ndarray) -> np.ndarray:
 def moe_lora_forward_fp8(hidden_bits, logits, w13_q, w13_scale, w2_q, w2_scale, mapping, top_k,
                          scaling=2.0, lora_gu=None, lora_dn=None, tokens=None,
                          local_expert_offset=0):
-    """The layer forward with FP8 block-scaled expert weights: the weights are
-    dequantized (e4m3 value times its block's scale, in float64) and the
-    forward is then exactly ``moe_lora_forward``'s."""
-    w13 = dequant_fp8_blocks(w13_q, w13_scale)
-    w2 = dequant_fp8_blocks(w2_q, w2_scale)
+    """The layer forward with FP8 block-scaled expert weights: each touched
+    expert's weights are dequantized (e4m3 value times its block's scale, in
+    float64; one expert at a time, to bound memory) and the per-slot
+    arithmetic is exactly ``expert_slot``; the slot sum runs in slot order."""
     hidden_bits = np.asarray(hidden_bits)
     T, H = hidden_bits.shape
-    E = w13.shape[0]
+    E = w13_q.shape[0]
     ids, w = route_topk(logits, top_k)
     tokens = list(range(T)) if tokens is None else list(tokens)
-    out = np.zeros((len(tokens), H), dtype=np.float64)
-    for i, t in enumerate(tokens):
-        x = bf16_bits_to_f64(hidden_bits[t])
-        a = int(mapping[t])
-        acc = np.zeros(H, dtype=np.float64)
+    by_expert = {}
+    for t in tokens:
         for j in range(top_k):
             e = int(ids[t, j]) - local_expert_offset
-            if not 0 <= e < E:
-                continue
-            _, _, y = expert_slot(x, w13[e], w2[e], lora_gu, lora_dn, a, e, scaling)
-            acc = acc + w[t, j] * y
+            if 0 <= e < E:
+                by_expert.setdefault(e, []).append((t, j))
+    y_slot = {}
+    for e in sorted(by_expert):
+        w13_e = dequant_fp8_blocks(w13_q[e:e + 1], w13_scale[e:e + 1])[0]
+        w2_e = dequant_fp8_blocks(w2_q[e:e + 1], w2_scale[e:e + 1])[0]
+        for (t, j) in by_expert[e]:
+            x = bf16_bits_to_f64(hidden_bits[t])
+            _, _, y = expert_slot(x, w13_e, w2_e, lora_gu, lora_dn, int(mapping[t]), e, scaling)
+            y_slot[(t, j)] = y
+    out = np.zeros((len(tokens), H), dtype=np.float64)
+    for i, t in enumerate(tokens):
+        acc = np.zeros(H, dtype=np.float64)
+        for j in range(top_k):
+            if (t, j) in y_slot:
+                acc = acc + w[t, j] * y_slot[(t, j)]
         out[i] = acc
     return {"ids": ids, "w": w, "tokens": tokens, "out64": out, "out_bf16": f64_to_bf16_bits(out)}
 
