@@ -42,6 +42,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--tile-n", type=int, default=0)
+    ap.add_argument("--weights", choices=["bf16", "fp8"], default="bf16",
+                    help="expert weight format (fp8: e4m3 with 128x128 block scales)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help=argparse.SUPPRESS)
@@ -52,10 +54,11 @@ def parse_args():
 # Algorithmic work of one forward (from the actual routing of the inputs)
 # ---------------------------------------------------------------------------
 
-def algorithmic_work(wl, ids, mapping):
+def algorithmic_work(wl, ids, mapping, fp8=False):
     """Bytes and FLOPs the forward must move / compute, intermediates excluded.
 
-    Bytes: every touched expert's w13 and w2 once, every touched LoRA factor
+    Bytes: every touched expert's w13 and w2 once (fp8: one byte per weight
+    plus one float32 scale per 128 x 128 block), every touched LoRA factor
     once (shared factors once per adapter), the hidden input, the output, the
     router logits and the mapping.  FLOPs: 2 per multiply-add of the two expert
     GEMMs for every (token, slot) and of the four LoRA products for adapted
@@ -69,7 +72,11 @@ def algorithmic_work(wl, ids, mapping):
     adapted = [(t, int(mapping[t])) for t in range(T) if lora and mapping[t] >= 0]
     pairs = sorted({(a, int(e)) for t, a in adapted for e in ids[t]})
     adapters = sorted({a for _, a in adapted})
-    w13_b, w2_b = 2 * I * H * 2, H * I * 2
+    if fp8:
+        nb = lambda x: (x + 127) // 128
+        w13_b, w2_b = 2 * I * H + nb(2 * I) * nb(H) * 4, H * I + nb(H) * nb(I) * 4
+    else:
+        w13_b, w2_b = 2 * I * H * 2, H * I * 2
     gu_A = (len(adapters) if wl.shared_outer else len(pairs)) * r * H * 2
     gu_B = len(pairs) * 2 * I * r * 2
     dn_A = len(pairs) * r * I * 2
@@ -282,10 +289,17 @@ def run_ours(args):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
 
     lora = inp.A_gu is not None
-    layer = m.MoeLoraLayer(bf16(inp.w13), bf16(inp.w2), wl.top_k,
+    fp8 = args.weights == "fp8"
+    if fp8:
+        q13, s13, q2, s2 = workloads.fp8_weights(inp)
+        w13_d, w2_d = torch.from_numpy(q13).to(dev), torch.from_numpy(q2).to(dev)
+        scales = dict(w13_scale=torch.from_numpy(s13).to(dev), w2_scale=torch.from_numpy(s2).to(dev))
+    else:
+        w13_d, w2_d, scales = bf16(inp.w13), bf16(inp.w2), {}
+    layer = m.MoeLoraLayer(w13_d, w2_d, wl.top_k,
                            bf16(inp.A_gu) if lora else None, bf16(inp.B_gu) if lora else None,
                            bf16(inp.A_dn) if lora else None, bf16(inp.B_dn) if lora else None,
-                           scaling=wl.scaling, max_tokens=wl.T)
+                           scaling=wl.scaling, max_tokens=wl.T, **scales)
     hidden = bf16(inp.hidden)
     logits = torch.from_numpy(inp.logits).to(dev)
     mapping = torch.from_numpy(inp.mapping).to(dev) if lora else None
@@ -419,7 +433,7 @@ def run_ours(args):
 
     # ---------------- roofline
     ids_np = ids.cpu().numpy()
-    work = algorithmic_work(wl, ids_np, inp.mapping)
+    work = algorithmic_work(wl, ids_np, inp.mapping, fp8=fp8)
     peaks, peak_src = load_peaks()
     med = [statistics.median(s[j] for s in stage_ms) for j in range(len(m.STAGE_NAMES))]
     stages_us = {nm: round(v * 1e3, 2) for nm, v in zip(m.STAGE_NAMES, med)}
@@ -436,7 +450,7 @@ def run_ours(args):
         achieved = kw["flops"] / (kt_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4)}
-    roof.update({"traffic": committed_traffic(top, args.workload), "kernel": top,
+    roof.update({"traffic": committed_traffic(top, args.workload + ("_fp8" if fp8 else "")), "kernel": top,
                  "kernel_us": round(kt_ms * 1e3, 2), "algorithmic_bytes": kw["bytes"],
                  "algorithmic_flops": kw["flops"], "peak_source": f"{peak_src} (MEASURED_PEAKS.json)"
                  if peak_src == "measured" else "fallback"})
@@ -450,12 +464,13 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 (fp8 e4m3 expert weights, dequantized to bf16)" if fp8 else "bf16",
         "data": "synthetic (seeded normal inputs and weights; no trained weights)",
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
                    "top_k": wl.top_k, "num_adapters": wl.num_adapters, "rank": wl.rank,
                    "lora_scaling": wl.scaling, "shared_outer": wl.shared_outer,
-                   "tile_n": args.tile_n or "auto",
+                   "tile_n": args.tile_n or "auto", "weights": args.weights,
                    "l2": "flushed before every step (256 MiB write, outside the step events)",
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": roof, "forward_roofline": fwd, "stages_us": stages_us,

@@ -235,6 +235,9 @@ typedef struct {
  *     0 <= offset <= num_router_experts - E, else MOE_ERR_SHAPE.  Callers
  *     built against the header without these two fields pass the smaller
  *     struct_size and get no sharding.
+ *   weight_format, w13_scale, w2_scale: FP8 block-scaled expert weights (see
+ *     MOE_WEIGHTS_FP8_E4M3_B128); callers passing a struct_size that ends
+ *     before weight_format get bf16 weights.
  * ------------------------------------------------------------------------- */
 typedef struct {
   uint32_t struct_size;           /* sizeof(moe_lora_args_t) */
@@ -260,7 +263,22 @@ typedef struct {
   const float* adapter_scaling;   /* HOST array [num_adapters] or NULL */
   int local_expert_offset;        /* expert parallelism; 0 without sharding */
   int num_router_experts;         /* 0 = E */
+  int weight_format;              /* MOE_WEIGHTS_BF16 (0) or MOE_WEIGHTS_FP8_E4M3_B128 */
+  const float* w13_scale;         /* FP8: [E, ceil(2I/128), ceil(H/128)] float32 */
+  const float* w2_scale;          /* FP8: [E, ceil(H/128), ceil(I/128)] float32 */
 } moe_lora_args_t;
+
+/* Expert weight formats (moe_lora_args_t.weight_format). */
+#define MOE_WEIGHTS_BF16 0
+/* w13 [E, 2I, H] and w2 [E, H, I] as float8 e4m3 (finite-only variant: max
+ * 448, no infinities, 0x7F/0xFF are NaN), one float32 scale per 128 x 128
+ * block of (rows, K): w[e][n][k] = e4m3(q[e][n][k]) * scale[e][n/128][k/128].
+ * The block-quant format of the pages' FP8 sibling path
+ * (trtllm_fp8_block_scale_routed_moe_lora) as read here; activations stay
+ * bf16 and the dequantized weights enter the tensor cores as bf16.
+ * Requires H % 16 == 0 and I % 16 == 0 (MOE_ERR_ALIGN) and both scale
+ * arrays (MOE_ERR_NULL). */
+#define MOE_WEIGHTS_FP8_E4M3_B128 1
 
 /* Test-only flag for debug_flags: the gate_up GEMM's MMA role first waits on
  * a barrier that nothing signals, so its wait runs out after wait_timeout_ms;

@@ -30,6 +30,8 @@ MOE_ERR_DEVICE_TIMEOUT = -7
 MOE_ERR_BAD_MAPPING = -8
 MOE_ERR_BAD_EXPERT_ID = -9
 MOE_NUM_STAGE_EVENTS = 8
+MOE_WEIGHTS_BF16 = 0
+MOE_WEIGHTS_FP8_E4M3_B128 = 1
 MOE_DEBUG_STALL_GATE_UP_MMA = 1
 STAGE_NAMES = ["route", "permute", "shrink_gate_up", "gemm_gate_up", "shrink_down", "gemm_down",
                "finalize"]
@@ -69,7 +71,9 @@ class MoeLoraArgs(ctypes.Structure):
                 ("debug_flags", ctypes.c_uint32),
                 ("stage_events", ctypes.c_void_p),
                 ("adapter_scaling", ctypes.c_void_p),
-                ("local_expert_offset", ctypes.c_int), ("num_router_experts", ctypes.c_int)]
+                ("local_expert_offset", ctypes.c_int), ("num_router_experts", ctypes.c_int),
+                ("weight_format", ctypes.c_int), ("w13_scale", ctypes.c_void_p),
+                ("w2_scale", ctypes.c_void_p)]
 
 
 class WorkspacePlan(ctypes.Structure):
@@ -228,6 +232,10 @@ class MoeLoraLayer:
     A_gu [A, E, r, H] or shared [A, r, H]; B_gu [A, E, 2I, r];
     A_dn [A, E, r, I]; B_dn [A, E, H, r] or shared [A, H, r].
 
+    FP8 weights: w13 / w2 as uint8 (or float8_e4m3fn) e4m3 codes with
+    ``w13_scale`` [E, ceil(2I/128), ceil(H/128)] and ``w2_scale``
+    [E, ceil(H/128), ceil(I/128)] float32 block scales (128 x 128 blocks).
+
     Expert parallelism: ``num_router_experts`` > E makes this layer one shard
     holding experts [local_expert_offset, local_expert_offset + E) of a router
     over num_router_experts experts (router_logits [T, num_router_experts]);
@@ -236,14 +244,27 @@ class MoeLoraLayer:
 
     def __init__(self, w13, w2, top_k: int, A_gu=None, B_gu=None, A_dn=None, B_dn=None,
                  scaling: float = 1.0, max_tokens: int = 0, adapter_scaling=None,
-                 local_expert_offset: int = 0, num_router_experts: int = 0):
+                 local_expert_offset: int = 0, num_router_experts: int = 0,
+                 w13_scale=None, w2_scale=None):
         torch = _torch()
         self.E, twoI, self.H = w13.shape
         self.local_expert_offset = int(local_expert_offset)
         self.num_router_experts = int(num_router_experts) or self.E
         self.I = twoI // 2
-        _require(w13, torch.bfloat16, (self.E, 2 * self.I, self.H), "w13")
-        _require(w2, torch.bfloat16, (self.E, self.H, self.I), "w2")
+        self.fp8 = w13.dtype != torch.bfloat16
+        if self.fp8:
+            fp8_types = (torch.uint8,) + ((torch.float8_e4m3fn,) if hasattr(torch, "float8_e4m3fn") else ())
+            if w13.dtype not in fp8_types or w2.dtype != w13.dtype:
+                raise TypeError("FP8 weights: w13 and w2 as uint8 or float8_e4m3fn")
+            _require(w13, w13.dtype, (self.E, 2 * self.I, self.H), "w13")
+            _require(w2, w2.dtype, (self.E, self.H, self.I), "w2")
+            nb = lambda n: (n + 127) // 128
+            _require(w13_scale, torch.float32, (self.E, nb(2 * self.I), nb(self.H)), "w13_scale")
+            _require(w2_scale, torch.float32, (self.E, nb(self.H), nb(self.I)), "w2_scale")
+        else:
+            _require(w13, torch.bfloat16, (self.E, 2 * self.I, self.H), "w13")
+            _require(w2, torch.bfloat16, (self.E, self.H, self.I), "w2")
+        self.w13_scale, self.w2_scale = w13_scale, w2_scale
         self.w13, self.w2, self.top_k, self.scaling = w13, w2, top_k, float(scaling)
         self.A_gu, self.B_gu, self.A_dn, self.B_dn = A_gu, B_gu, A_dn, B_dn
         if A_gu is not None:
@@ -309,6 +330,9 @@ class MoeLoraLayer:
         a.tile_n, a.wait_timeout_ms = int(tile_n), int(wait_timeout_ms)
         a.debug_flags = int(debug_flags)
         a.local_expert_offset, a.num_router_experts = self.local_expert_offset, self.num_router_experts
+        if self.fp8:
+            a.weight_format = MOE_WEIGHTS_FP8_E4M3_B128
+            a.w13_scale, a.w2_scale = self.w13_scale.data_ptr(), self.w2_scale.data_ptr()
         a.adapter_scaling = ctypes.cast(self._scales, ctypes.c_void_p) if self._scales is not None else None
         self._events_keepalive = None
         if stage_events is not None:

@@ -70,10 +70,11 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// N-D bf16 tensor (dims innermost first, strides in bytes for dims 1..rank-1),
-// 128-byte swizzle, zero fill out of bounds.
+// N-D tensor (dims innermost first, strides in bytes for dims 1..rank-1),
+// zero fill out of bounds: bf16 with 128-byte swizzle, or (fp8) bytes
+// without swizzle (the converter warps read them).
 bool encode_nd(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-               const uint64_t* strides, const uint32_t* box) {
+               const uint64_t* strides, const uint32_t* box, bool fp8 = false) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t d[5], st[4];
@@ -84,8 +85,9 @@ bool encode_nd(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
     e[i] = 1;
     if (i + 1 < rank) st[i] = strides[i];
   }
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, st, b, e,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+            const_cast<void*>(base), d, st, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -94,14 +96,15 @@ bool encode_nd(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
 // {H, 16 rows, 2 halves, I/16 groups, E} does it in one box; otherwise a 3-D
 // view {H, I, 2E} in four boxes of {64, 16, 2}.  Rows past I fall outside a
 // dimension of either view and are zero-filled.
-bool encode_w13(CUtensorMap* m, const void* w13, int H, int I, int E, bool* single_box) {
-  const uint64_t row = static_cast<uint64_t>(H) * 2;
+bool encode_w13(CUtensorMap* m, const void* w13, int H, int I, int E, bool* single_box,
+                bool fp8 = false) {
+  const uint64_t row = static_cast<uint64_t>(H) * (fp8 ? 1 : 2);
   if (I % 16 == 0) {
     const uint64_t dims[5] = {static_cast<uint64_t>(H), 16, 2, static_cast<uint64_t>(I / 16),
                               static_cast<uint64_t>(E)};
     const uint64_t strides[4] = {row, row * I, row * 16, row * 2 * I};
     const uint32_t box[5] = {64, 16, 2, 4, 1};
-    if (encode_nd(m, w13, 5, dims, strides, box)) {
+    if (encode_nd(m, w13, 5, dims, strides, box, fp8)) {
       *single_box = true;
       return true;
     }
@@ -111,7 +114,7 @@ bool encode_w13(CUtensorMap* m, const void* w13, int H, int I, int E, bool* sing
   const uint64_t strides[2] = {row, row * I};
   const uint32_t box[3] = {64, 16, 2};
   *single_box = false;
-  return encode_nd(m, w13, 3, dims, strides, box);
+  return encode_nd(m, w13, 3, dims, strides, box, fp8);
 }
 
 // ------------------------------------------------------------ workspace plan
@@ -302,10 +305,15 @@ int moe_read_device_status(const void* workspace, moe_stream_t stream) {
 
 int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   if (a == nullptr) return MOE_ERR_NULL;
-  // Structures from before the expert-parallel fields end at adapter_scaling.
+  // Structures from before the expert-parallel fields end at adapter_scaling,
+  // those from before the weight-format fields at num_router_experts.
   constexpr size_t kSizeNoShard = offsetof(moe_lora_args_t, local_expert_offset);
+  constexpr size_t kSizeNoFormat = offsetof(moe_lora_args_t, weight_format);
   if (a->struct_size < kSizeNoShard) return MOE_ERR_UNSUPPORTED;
-  const bool has_shard = a->struct_size >= sizeof(moe_lora_args_t);
+  const bool has_shard = a->struct_size >= kSizeNoFormat;
+  const bool has_format = a->struct_size >= sizeof(moe_lora_args_t);
+  const int wfmt = has_format ? a->weight_format : MOE_WEIGHTS_BF16;
+  const bool w8 = wfmt == MOE_WEIGHTS_FP8_E4M3_B128;
   const int T = a->T, H = a->H, I = a->I, E = a->E, K = a->top_k;
   const int shard_off = has_shard ? a->local_expert_offset : 0;
   const int R = (has_shard && a->num_router_experts != 0) ? a->num_router_experts : E;
@@ -313,6 +321,9 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   int st = limits_status(H, I, E, K, a->num_adapters, a->rank);
   if (st != MOE_OK) return st;
   if (R < E || R > MOE_MAX_EXPERTS || K > R || shard_off < 0 || shard_off > R - E) return MOE_ERR_SHAPE;
+  if (wfmt != MOE_WEIGHTS_BF16 && wfmt != MOE_WEIGHTS_FP8_E4M3_B128) return MOE_ERR_UNSUPPORTED;
+  // FP8 weight rows are 1 byte per element: TMA wants 16-byte row pitches.
+  if (w8 && (H % 16 != 0 || I % 16 != 0)) return MOE_ERR_ALIGN;
   const bool lora = a->num_adapters > 0 && a->rank > 0;
   const int A = lora ? a->num_adapters : 0;
   const int r = lora ? a->rank : 0;
@@ -345,6 +356,9 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
       a->router_logits == nullptr || a->out == nullptr || a->workspace == nullptr)
     return MOE_ERR_NULL;
   if (!aligned16(a->hidden) || !aligned16(a->w13) || !aligned16(a->w2) || !aligned16(a->out))
+    return MOE_ERR_ALIGN;
+  if (w8 && (a->w13_scale == nullptr || a->w2_scale == nullptr)) return MOE_ERR_NULL;
+  if (w8 && ((reinterpret_cast<uintptr_t>(a->w13_scale) | reinterpret_cast<uintptr_t>(a->w2_scale)) & 3))
     return MOE_ERR_ALIGN;
   if (lora) {
     if (a->token_lora_mapping == nullptr || a->gate_up.A == nullptr || a->gate_up.B == nullptr ||
@@ -412,6 +426,10 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   // MOE_LORA_PAIR=0/1 overrides the default for tuning (128- or 256-wide tiles).
   bool pair = cl == 1 && moe::gemm_use_pair(bn);
   if (const char* env = std::getenv("MOE_LORA_PAIR")) pair = cl == 1 && std::atoi(env) != 0 && bn >= 128;
+  if (w8) {  // FP8 weights run one CTA per tile
+    pair = false;
+    cl = 1;
+  }
   if (pair) cl = 2;  // a pair is a cluster of two; each CTA loads bn / 2 token rows
   const int sms = num_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
@@ -421,8 +439,11 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   // TMA descriptors (host-encoded, passed by value as kernel parameters).
   CUtensorMap tm_w13, tm_w2, tm_xp, tm_h, tm_bgu, tm_bdn, tm_u, tm_v;
   bool gu_single_box = false;
-  bool enc = encode_w13(&tm_w13, a->w13, H, I, E, &gu_single_box) &&
-             encode_2d(&tm_w2, a->w2, I, static_cast<uint64_t>(E) * H, I * 2ull, 64, 128) &&
+  const uint64_t w2_dims[2] = {static_cast<uint64_t>(I), static_cast<uint64_t>(E) * H};
+  const uint64_t w2_row[1] = {static_cast<uint64_t>(I) * (w8 ? 1 : 2)};
+  const uint32_t w2_box[2] = {64, 128};
+  bool enc = encode_w13(&tm_w13, a->w13, H, I, E, &gu_single_box, w8) &&
+             encode_nd(&tm_w2, a->w2, 2, w2_dims, w2_row, w2_box, w8) &&
              encode_2d(&tm_xp, xp, H, n, H * 2ull, 64, bn / cl) &&
              encode_2d(&tm_h, h, I, n, I * 2ull, 64, bn / cl);
   int64_t gu_rs_a = 0, gu_rs_e = 0, dn_rs_a = 0, dn_rs_e = 0;
@@ -564,7 +585,10 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.status = status;
   gp.timeout_ns = timeout_ns;
   gp.tables_ready = 1;  // launched right after the gate_up shrink (n > 0 here)
-  if (moe::launch_expert_gemm(moe::kGateUp, bn, cl, pair, tm_w13, tm_xp, tm_bgu, tm_u, gp,
+  gp.w_scale = w8 ? a->w13_scale : nullptr;
+  gp.scale_nb = (2 * I + 127) / 128;
+  gp.scale_kb = (H + 127) / 128;
+  if (moe::launch_expert_gemm(moe::kGateUp, bn, cl, pair, w8, tm_w13, tm_xp, tm_bgu, tm_u, gp,
                               sms * moe::gemm_ctas_per_sm(bn), stream) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
@@ -596,7 +620,10 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.lb_row_stride_expert = dn_rs_e;
   gp.out = y;
   gp.tables_ready = lora ? 1 : 0;  // else the gate_up GEMM precedes this launch
-  if (moe::launch_expert_gemm(moe::kDown, bn, cl, pair, tm_w2, tm_h, tm_bdn, tm_v, gp,
+  gp.w_scale = w8 ? a->w2_scale : nullptr;
+  gp.scale_nb = (H + 127) / 128;
+  gp.scale_kb = (I + 127) / 128;
+  if (moe::launch_expert_gemm(moe::kDown, bn, cl, pair, w8, tm_w2, tm_h, tm_bdn, tm_v, gp,
                               sms * moe::gemm_ctas_per_sm(bn), stream) !=
       cudaSuccess)
     return MOE_ERR_CUDA;

@@ -33,6 +33,8 @@
 // MMAs of the next.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "../../include/moe_lora.h"
@@ -43,22 +45,35 @@ namespace moe {
 
 constexpr unsigned kFullMask = 0xFFFFFFFFu;
 
-template <int BN, bool PAIR = false>
+template <int BN, bool PAIR = false, bool W8 = false>
 struct GemmCfg {
   // Narrow (decode) tiles run two CTAs per SM so that two producers keep TMA
   // loads in flight; wide tiles run one CTA per SM with deeper stages.
   static constexpr int kCtasPerSm = BN <= 64 ? 2 : 1;
-  static constexpr int kStageBudget = BN <= 64 ? 96 * 1024 : 200 * 1024;
+  // FP8 weights add four converter warps.
+  static constexpr int kThreads = W8 ? 320 : 192;
+  static constexpr int kStageBudget = BN <= 64 ? (W8 ? 104 : 96) * 1024 : 200 * 1024;
   static constexpr int kABytes = 128 * 64 * 2;   // 128 rows x 64 K of bf16
   // A CTA of a pair holds half of the token tile.
   static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * 64 * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStagesRaw = kStageBudget / kStageBytes;
+  // FP8: a deep ring of (raw 128 x 64 e4m3 weight tile, token tile) stages
+  // filled by TMA; the converter warps write the bf16 A tiles into a ring of
+  // two A-only stages.
+  static constexpr int kW8Bytes = 128 * 64;
+  static constexpr int kW8Stage = (kW8Bytes + kBBytes + 1023) / 1024 * 1024;
+  static constexpr int kStagesRaw = W8 ? (BN <= 64 ? 3 : 4) : kStageBudget / kStageBytes;
   static constexpr int kStages = kStagesRaw > 16 ? 16 : kStagesRaw;
+  static constexpr int kARingBytes = W8 ? kStages * kABytes : kStages * kStageBytes;
+  static constexpr int kStages8Raw = W8 ? (kStageBudget - kARingBytes) / kW8Stage : 0;
+  static constexpr int kStages8 = kStages8Raw > 16 ? 16 : kStages8Raw;
   static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr int kMetaBytes = 512;                         // barriers, flags
   static constexpr int kTableBytes = 2 * (MOE_MAX_EXPERTS + 1) * 4;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kMetaBytes + kTableBytes;
+  static constexpr int kSmemBytes =
+      1024 + kARingBytes + kStages8 * kW8Stage + kMetaBytes + kTableBytes;
+  static_assert((2 * kStages + 2 * kStages8 + 6) * 8 + 16 <= kMetaBytes, "barriers fit");
+  static_assert(kCtasPerSm * (kSmemBytes + 1024) <= 233472, "the CTAs of an SM fit its shared memory");
 };
 
 struct Work {
@@ -120,6 +135,34 @@ __device__ __forceinline__ void raise_timeout(int* status, volatile int* abort_f
   *abort_flag = 1;
 }
 
+// As raise_timeout; the first error also records where in the status detail
+// words: [1] = the wait (kWait*), [2] = (CTA << 8) | warp, [3] = (unit << 16)
+// | (K block << 4) | ring stage.
+enum WaitSite {
+  kWaitProducerW8 = 1, kWaitProducer = 2, kWaitMmaAccEmpty = 4, kWaitMmaFull = 5,
+  kWaitMmaFull8 = 6, kWaitEpilogue = 7, kWaitConvEmpty = 8, kWaitConvFull8 = 9,
+  kWaitDrainProducer = 10, kWaitDrainProducerW8 = 11, kWaitDrainConv = 12, kWaitDrainMma = 13
+};
+
+// A teardown wait that ran out: the status and its place, no abort (the
+// roles have left their loops already).
+__device__ __forceinline__ void note_drain_timeout(int* status, int site, int stage) {
+  if (status != nullptr && atomicCAS(status, 0, MOE_ERR_DEVICE_TIMEOUT) == 0) {
+    status[1] = site;
+    status[2] = static_cast<int>((blockIdx.x << 8) | (threadIdx.x >> 5));
+    status[3] = stage & 15;
+  }
+}
+__device__ __forceinline__ void raise_timeout_at(int* status, volatile int* abort_flag, int site, int unit,
+                                                 int blk, int stage) {
+  if (status != nullptr && atomicCAS(status, 0, MOE_ERR_DEVICE_TIMEOUT) == 0) {
+    status[1] = site;
+    status[2] = static_cast<int>((blockIdx.x << 8) | (threadIdx.x >> 5));
+    status[3] = (unit << 16) | ((blk & 0xFFF) << 4) | (stage & 15);
+  }
+  *abort_flag = 1;
+}
+
 // Weight-side (A operand) loads of one K block: 128 rows of the feature block.
 // gate_up: the map views w13 so that one box (or four, see the host code)
 // brings gate rows 64 fb + 16q + (0..15) to smem rows 32q + (0..15) and the
@@ -133,7 +176,9 @@ __device__ __forceinline__ void load_2d(void* dst, const CUtensorMap* map, uint6
   else tma_load_2d(dst, map, bar, c0, c1, pol);
 }
 
-template <int MODE, bool PAIR>
+// ESZ: bytes per weight element (2 bf16, 1 fp8): the smem offset between
+// the four 16-row boxes of the 3-D gate_up view.
+template <int MODE, bool PAIR, int ESZ = 2>
 __device__ __forceinline__ void load_weight_block(uint8_t* sA, const CUtensorMap* map,
                                                   uint64_t* bar, uint32_t cbar, int kc, int e, int fb,
                                                   int rows_per_expert, int gu_single_box,
@@ -147,8 +192,8 @@ __device__ __forceinline__ void load_weight_block(uint8_t* sA, const CUtensorMap
       // map dims {H, I, 2E}, box {64, 16, 2}
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        if constexpr (PAIR) tma_load_3d_pair(sA + q * 4096, map, cbar, kc, fb * 64 + q * 16, 2 * e, pol);
-        else tma_load_3d(sA + q * 4096, map, bar, kc, fb * 64 + q * 16, 2 * e, pol);
+        if constexpr (PAIR) tma_load_3d_pair(sA + q * 2048 * ESZ, map, cbar, kc, fb * 64 + q * 16, 2 * e, pol);
+        else tma_load_3d(sA + q * 2048 * ESZ, map, bar, kc, fb * 64 + q * 16, 2 * e, pol);
       }
     }
   } else {
@@ -181,25 +226,37 @@ __device__ __forceinline__ void load_lora_b_block(uint8_t* sA, const CUtensorMap
 // and commits to both CTAs' barriers.  Each CTA's TMEM receives its own
 // feature block for the whole token tile, so the epilogue is unchanged; the
 // epilogue warps of both CTAs release the even CTA's accumulator barrier.
-template <int BN, int MODE, int CL, bool PAIR>
-__global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
+//
+// W8 (FP8 block-scaled weights, CL == 1): warp 0 streams raw e4m3 weight
+// tiles through the deep ring (full8/empty8); warps 6..9 convert: for each K
+// block they wait for a free bf16 stage, issue the token-tile (or LoRA) loads
+// into it, write the dequantized weight tile (e4m3 value times its 128 x 128
+// block scale, rounded to bf16) in the 128-byte-swizzled layout the MMA
+// reads, and release it with a second arrival on full.  MMA and epilogue
+// are unchanged.
+template <int BN, int MODE, int CL, bool PAIR, bool W8>
+__global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, PAIR, W8>::kCtasPerSm)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                        const __grid_constant__ CUtensorMap tm_lb, const __grid_constant__ CUtensorMap tm_lu,
                        const GemmParams p) {
   static_assert(!PAIR || CL == 2, "a pair is a cluster of two");
-  using C = GemmCfg<BN, PAIR>;
+  static_assert(!W8 || (CL == 1 && !PAIR), "FP8 weights: one CTA per tile");
+  using C = GemmCfg<BN, PAIR, W8>;
   constexpr bool kMulticast = CL > 1 && !PAIR;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* meta = smem + C::kStages * C::kStageBytes;
+  uint8_t* w8ring = smem + C::kARingBytes;  // FP8 only
+  uint8_t* meta = w8ring + C::kStages8 * C::kW8Stage;
   uint64_t* full = reinterpret_cast<uint64_t*>(meta);
   uint64_t* empty = full + C::kStages;
   uint64_t* accf = empty + C::kStages;
   uint64_t* acce = accf + 2;
   uint64_t* drain = acce + 2;
   uint64_t* never = drain + 1;  // test hook: a barrier nothing arrives on
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
+  uint64_t* full8 = never + 1;
+  uint64_t* empty8 = full8 + C::kStages8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty8 + C::kStages8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_off = reinterpret_cast<int*>(meta + C::kMetaBytes);
   int* s_ts = s_off + (MOE_MAX_EXPERTS + 1);
@@ -210,8 +267,12 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
   const int lkb = (p.rank + 63) / 64;  // K blocks per adapter of the LoRA expand
 
   if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages8; ++s) {
+      mbar_init(&full8[s], 1);
+      mbar_init(&empty8[s], 1);
+    }
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], W8 ? 4 : 1);  // FP8: one arrival per converter warp
       // multicast: every CTA of the cluster releases the stage; pair: the
       // leader's commit arrives once in each CTA
       mbar_init(&empty[s], kMulticast ? CL : 1);
@@ -270,7 +331,92 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
   constexpr int kPieceRows = BN / CL;              // token rows each CTA loads and multicasts
   const bool leader = !PAIR || crank == 0;
 
-  if (warp == 0) {
+  if (W8 && warp == 0) {
+    // ---------------------------------------------------- FP8 producer
+    // Per K block one ring stage: the raw e4m3 weight tile (main blocks) and
+    // the token tile (x, or the one-hot u of a LoRA block), 128-byte
+    // swizzled, that the MMA reads in place.  Weights are static and go out
+    // at once; the token tiles of the first ring pass wait for the previous
+    // kernel (griddepcontrol.wait).
+    const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_x = l2_policy_evict_last();
+    uint32_t s8 = 0, ph8 = 0, armed = 0, armed_parity = 0;
+    bool ok = true;
+    bool waited = !p.tables_ready;
+    int n_pend = 0;
+    const CUtensorMap* pend_map[C::kStages8 > 0 ? C::kStages8 : 1];
+    int pend_c0[C::kStages8 > 0 ? C::kStages8 : 1], pend_c1[C::kStages8 > 0 ? C::kStages8 : 1],
+        pend_stage[C::kStages8 > 0 ? C::kStages8 : 1];
+    auto release_pending = [&]() {
+      pdl_wait();
+      waited = true;
+      for (int i = 0; i < n_pend; ++i)
+        tma_load_2d(w8ring + pend_stage[i] * C::kW8Stage + C::kW8Bytes, pend_map[i], &full8[pend_stage[i]],
+                    pend_c0[i], pend_c1[i], pol_x);
+      n_pend = 0;
+    };
+    for (int w = unit0; w < total_work && ok; w += unit_step) {
+      if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
+      const Work wk = decode_work<BN>(w, crank, CL, s_off, s_ts, p.E, FBg);
+      uint64_t amask = use_lora ? tile_adapter_mask(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
+      const int nblocks = nk + __popcll(amask) * lkb;
+      int adapter = -1, j = 0;
+      for (int b = 0; b < nblocks; ++b) {
+        if (b >= nk && j == 0) {
+          adapter = __ffsll(static_cast<long long>(amask)) - 1;
+          amask &= amask - 1;
+        }
+        if (lane == 0) {
+          ok = wait_or_abort(&empty8[s8], ph8 ^ 1, p.timeout_ns, abort_flag);
+          if (ok) {
+            uint8_t* st = w8ring + s8 * C::kW8Stage;
+            mbar_arrive_expect_tx(&full8[s8], (b < nk ? C::kW8Bytes : 0) + C::kBBytes);
+            const CUtensorMap* tmap;
+            int tc0;
+            if (b < nk) {
+              load_weight_block<MODE, false, 1>(st, &tm_w, &full8[s8], 0u, b * 64, wk.e, wk.fb,
+                                                p.rows_per_expert, p.gu_single_box, pol_w);
+              tmap = &tm_x;
+              tc0 = b * 64;
+            } else {
+              tmap = &tm_lu;
+              tc0 = adapter * p.rank + j * 64;
+            }
+            if (waited) {
+              tma_load_2d(st + C::kW8Bytes, tmap, &full8[s8], tc0, wk.row0, pol_x);
+            } else {
+              pend_map[n_pend] = tmap;
+              pend_c0[n_pend] = tc0;
+              pend_c1[n_pend] = wk.row0;
+              pend_stage[n_pend] = s8;
+              ++n_pend;
+              if (static_cast<int>(s8) == C::kStages8 - 1) release_pending();  // before the ring wraps
+            }
+            armed |= 1u << s8;
+            armed_parity = (armed_parity & ~(1u << s8)) | (ph8 << s8);
+          } else {
+            raise_timeout_at(p.status, abort_flag, kWaitProducerW8, w, b, s8);
+          }
+        }
+        ok = __shfl_sync(kFullMask, ok, 0);
+        if (!ok) break;
+        if (b >= nk) j = (j + 1 == lkb) ? 0 : j + 1;
+        if (++s8 == C::kStages8) {
+          s8 = 0;
+          ph8 ^= 1;
+        }
+      }
+    }
+    if (lane == 0 && !waited) release_pending();
+    if (lane == 0) {  // every load issued must have landed before the CTA leaves
+      const uint64_t lim = *abort_flag ? 1000000ull : p.timeout_ns;
+      for (int s = 0; s < C::kStages8; ++s)
+        if (armed & (1u << s))
+          if (!mbar_wait(&full8[s], (armed_parity >> s) & 1u, lim))
+            note_drain_timeout(p.status, kWaitDrainProducerW8, s);
+    }
+    __syncwarp();
+  } else if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     const uint64_t pol_w = l2_policy_evict_first();
     const uint64_t pol_x = l2_policy_evict_last();
@@ -349,7 +495,7 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
             armed |= 1u << stage;
             armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           } else {
-            raise_timeout(p.status, abort_flag);
+            raise_timeout_at(p.status, abort_flag, kWaitProducer, w, b, stage);
           }
         }
         ok = __shfl_sync(kFullMask, ok, 0);
@@ -372,14 +518,14 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
       for (int s = 0; s < C::kStages; ++s)
         if (armed & (1u << s)) {
           uint64_t* bar = leader ? &full[s] : &empty[s];
-          if (!mbar_wait(bar, (armed_parity >> s) & 1u, lim))
-            set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
+          if (!mbar_wait(bar, (armed_parity >> s) & 1u, lim)) note_drain_timeout(p.status, kWaitDrainProducer, s);
         }
     }
     __syncwarp();
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+    uint32_t s8 = 0, ph8 = 0;  // FP8: the ring stage holding this block's token tile
     bool ok = leader;  // a pair's odd CTA issues no MMA
     if (p.debug_stall_mma && leader) {  // failure-path test: this wait can only run out
       if (lane == 0 && !wait_or_abort(never, 0, p.timeout_ns, abort_flag))
@@ -397,7 +543,7 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
       const uint32_t idesc = make_idesc_bf16(PAIR ? 256 : 128, ncols);
       if (lane == 0) {
         ok = wait_or_abort<PAIR>(&acce[acc], acc_phase ^ 1, p.timeout_ns, abort_flag);
-        if (!ok) raise_timeout(p.status, abort_flag);
+        if (!ok) raise_timeout_at(p.status, abort_flag, kWaitMmaAccEmpty, w, 0, acc);
       }
       ok = __shfl_sync(kFullMask, ok, 0);
       if (!ok) break;
@@ -407,11 +553,19 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
       for (int b = 0; b < nblocks; ++b) {
         if (lane == 0) {
           ok = wait_or_abort<PAIR>(&full[stage], phase, p.timeout_ns, abort_flag);
+          int site = kWaitMmaFull;
+          if (W8 && ok) {
+            ok = wait_or_abort(&full8[s8], ph8, p.timeout_ns, abort_flag);
+            site = kWaitMmaFull8;
+          }
           if (ok) {
             tc_fence_after_sync();
-            const uint32_t a_addr = smem_u32(smem + stage * C::kStageBytes);
+            const uint32_t a_addr =
+                smem_u32(smem + stage * (W8 ? C::kABytes : C::kStageBytes));
+            const uint32_t b_addr =
+                W8 ? smem_u32(w8ring + s8 * C::kW8Stage + C::kW8Bytes) : a_addr + C::kABytes;
             const uint64_t adesc = make_sdesc_sw128(a_addr);
-            const uint64_t bdesc = make_sdesc_sw128(a_addr + C::kABytes);
+            const uint64_t bdesc = make_sdesc_sw128(b_addr);
             int ksteps = 4;
             if (b >= nk) {
               const int rem = p.rank - j * 64;
@@ -428,8 +582,9 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
             if constexpr (PAIR) tc_commit_pair(&empty[stage], 0x3);
             else if constexpr (kMulticast) tc_commit_multicast(&empty[stage], kClusterMask);
             else tc_commit(&empty[stage]);
+            if constexpr (W8) tc_commit(&empty8[s8]);
           } else {
-            raise_timeout(p.status, abort_flag);
+            raise_timeout_at(p.status, abort_flag, site, w, b, site == kWaitMmaFull8 ? s8 : stage);
           }
         }
         ok = __shfl_sync(kFullMask, ok, 0);
@@ -438,6 +593,10 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
         if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1;
+        }
+        if (W8 && ++s8 == C::kStages8) {
+          s8 = 0;
+          ph8 ^= 1;
         }
       }
       if (!ok) break;
@@ -452,10 +611,10 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
     if (lane == 0 && leader) {
       if constexpr (PAIR) tc_commit_pair(drain, 0x1);
       else tc_commit(drain);
-      if (!mbar_wait(drain, 0, p.timeout_ns)) set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
+      if (!mbar_wait(drain, 0, p.timeout_ns)) note_drain_timeout(p.status, kWaitDrainMma, 0);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     uint32_t acc = 0, acc_phase = 0;
@@ -466,7 +625,7 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
       bool ok = true;
       if (lane == 0) {
         ok = wait_or_abort<PAIR>(&accf[acc], acc_phase, p.timeout_ns, abort_flag);
-        if (!ok) raise_timeout(p.status, abort_flag);
+        if (!ok) raise_timeout_at(p.status, abort_flag, kWaitEpilogue, w, 0, acc);
       }
       ok = __shfl_sync(kFullMask, ok, 0);
       if (!ok) break;
@@ -512,6 +671,113 @@ __global__ void __launch_bounds__(192, GemmCfg<BN>::kCtasPerSm)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+  } else if constexpr (W8) {
+    // ------------------------------------------------- FP8 converters
+    // Warps 6..9, each on its own: converter warp cw writes tile rows
+    // [32 cw, 32 cw + 32).  Lane l takes 16-byte chunks 128 cw + l + 32 i of
+    // the 8 KB e4m3 tile (row = chunk / 4, columns 16 (chunk % 4) + 0..15)
+    // and writes them as two 16-byte bf16 chunks of the row at the 128-byte
+    // swizzle positions (chunk j of row r at j ^ (r % 8)), then arrives on
+    // the stage's full barrier (4 arrivals complete it; for a LoRA block
+    // warp 6's arrival also carries the byte count of the B-factor tile).
+    const int cw = warp - 6;
+    const uint64_t pol_b = l2_policy_evict_last();
+    uint32_t sa = 0, pha = 0, s8 = 0, ph8 = 0, armed = 0, armed_parity = 0;
+    bool ok = true;
+    for (int w = unit0; w < total_work && ok; w += unit_step) {
+      if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
+      const Work wk = decode_work<BN>(w, crank, CL, s_off, s_ts, p.E, FBg);
+      uint64_t amask = use_lora ? tile_adapter_mask(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
+      const int nblocks = nk + __popcll(amask) * lkb;
+      int adapter = -1, j = 0;
+      for (int b = 0; b < nblocks; ++b) {
+        if (b >= nk && j == 0) {  // next LoRA block: adapters in ascending order
+          adapter = __ffsll(static_cast<long long>(amask)) - 1;
+          amask &= amask - 1;
+        }
+        uint8_t* sA = smem + sa * C::kABytes;
+        if (lane == 0) {
+          int site = kWaitConvEmpty;
+          ok = wait_or_abort(&empty[sa], pha ^ 1, p.timeout_ns, abort_flag);
+          if (ok && b < nk) {
+            ok = wait_or_abort(&full8[s8], ph8, p.timeout_ns, abort_flag);
+            site = kWaitConvFull8;
+            // a main block reuses the stage: its earlier B-factor load (if
+            // any) was consumed, so nothing of it is left to drain
+            armed &= ~(1u << sa);
+          }
+          if (ok && b >= nk && cw == 0) {  // LoRA block: the B factor tile (bf16) to the A stage
+            const int64_t frow = static_cast<int64_t>(adapter) * p.lb_row_stride_adapter +
+                                 static_cast<int64_t>(wk.e) * p.lb_row_stride_expert;
+            mbar_arrive_expect_tx(&full[sa], C::kABytes);
+            load_lora_b_block<MODE, false>(sA, &tm_lb, &full[sa], 0u, j * 64, frow, wk.fb, p.n_feat,
+                                           pol_b);
+            armed |= 1u << sa;
+            armed_parity = (armed_parity & ~(1u << sa)) | (pha << sa);
+          }
+          if (!ok && !*abort_flag)
+            raise_timeout_at(p.status, abort_flag, site, w, b, site == kWaitConvFull8 ? s8 : sa);
+        }
+        ok = __shfl_sync(kFullMask, ok, 0);
+        if (!ok) break;
+        if (b < nk) {
+          const uint8_t* src8 = w8ring + s8 * C::kW8Stage;
+          const int kblk = (b * 64) >> 7;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c = 128 * cw + lane + 32 * i;
+            const int r = c >> 2, part = c & 3;
+            int wrow;  // the weight row behind tile row r
+            if (MODE == kGateUp) wrow = ((r >> 4) & 1) * p.n_feat + wk.fb * 64 + (r >> 5) * 16 + (r & 15);
+            else wrow = wk.fb * 128 + r;
+            const float sc = wrow < p.rows_per_expert
+                                 ? __ldg(p.w_scale + (static_cast<size_t>(wk.e) * p.scale_nb + (wrow >> 7)) *
+                                                         p.scale_kb + kblk)
+                                 : 0.f;
+            const uint4 raw = *reinterpret_cast<const uint4*>(src8 + c * 16);
+            const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+            uint32_t ov[8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
+                  static_cast<__nv_fp8x2_storage_t>(wv[u] & 0xFFFFu), __NV_E4M3);
+              const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
+                  static_cast<__nv_fp8x2_storage_t>(wv[u] >> 16), __NV_E4M3);
+              const float2 flo = __half22float2(__half2(lo));
+              const float2 fhi = __half22float2(__half2(hi));
+              const __nv_bfloat162 blo = __floats2bfloat162_rn(flo.x * sc, flo.y * sc);
+              const __nv_bfloat162 bhi = __floats2bfloat162_rn(fhi.x * sc, fhi.y * sc);
+              ov[2 * u] = *reinterpret_cast<const uint32_t*>(&blo);
+              ov[2 * u + 1] = *reinterpret_cast<const uint32_t*>(&bhi);
+            }
+            uint8_t* rowp = sA + r * 128;
+            const int j0 = 2 * part;
+            *reinterpret_cast<uint4*>(rowp + ((j0 ^ (r & 7)) << 4)) = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+            *reinterpret_cast<uint4*>(rowp + (((j0 + 1) ^ (r & 7)) << 4)) =
+                make_uint4(ov[4], ov[5], ov[6], ov[7]);
+          }
+          fence_proxy_async_shared();  // the tensor cores read what this thread wrote
+        }
+        __syncwarp();
+        if (lane == 0 && !(b >= nk && cw == 0)) mbar_arrive(&full[sa]);
+        if (b >= nk) j = (j + 1 == lkb) ? 0 : j + 1;
+        if (++s8 == C::kStages8) {  // one ring stage per block, main and LoRA
+          s8 = 0;
+          ph8 ^= 1;
+        }
+        if (++sa == C::kStages) {
+          sa = 0;
+          pha ^= 1;
+        }
+      }
+    }
+    if (lane == 0 && cw == 0) {  // every load issued must have landed before the CTA leaves
+      const uint64_t lim = *abort_flag ? 1000000ull : p.timeout_ns;
+      for (int s = 0; s < C::kStages; ++s)
+        if (armed & (1u << s))
+          if (!mbar_wait(&full[s], (armed_parity >> s) & 1u, lim)) note_drain_timeout(p.status, kWaitDrainConv, s);
+    }
+    __syncwarp();
   }
 
   tc_fence_before_sync();
@@ -556,18 +822,20 @@ size_t gemm_smem_bytes(int bn, bool pair) {
   }
 }
 
-template <int BN, int MODE, int CL, bool PAIR>
+template <int BN, int MODE, int CL, bool PAIR, bool W8 = false>
 static cudaError_t launch_one(const CUtensorMap& tm_w, const CUtensorMap& tm_x,
                               const CUtensorMap& tm_lb, const CUtensorMap& tm_lu,
                               const GemmParams& p, int grid, cudaStream_t s) {
-  auto kern = expert_gemm_kernel<BN, MODE, CL, PAIR>;
-  const int smem = GemmCfg<BN, PAIR>::kSmemBytes;
+  using C = GemmCfg<BN, PAIR, W8>;
+  auto kern = expert_gemm_kernel<BN, MODE, CL, PAIR, W8>;
+  const int smem = C::kSmemBytes;
   cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
-  if (CL == 1) return launch_pdl(kern, dim3(grid), dim3(192), smem, s, tm_w, tm_x, tm_lb, tm_lu, p);
+  if (CL == 1)
+    return launch_pdl(kern, dim3(grid), dim3(C::kThreads), smem, s, tm_w, tm_x, tm_lb, tm_lu, p);
 
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(192);
+  cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -601,10 +869,25 @@ int gemm_cluster_size(int) { return 1; }
 // of the token tile per stage, which leaves room for deeper stages.
 bool gemm_use_pair(int bn) { return bn == 256; }
 
-cudaError_t launch_expert_gemm(int mode, int bn, int cl, bool pair, const CUtensorMap& tm_w,
+cudaError_t launch_expert_gemm(int mode, int bn, int cl, bool pair, bool w8, const CUtensorMap& tm_w,
                                const CUtensorMap& tm_x, const CUtensorMap& tm_lb,
                                const CUtensorMap& tm_lu, const GemmParams& p, int grid,
                                cudaStream_t s) {
+  if (w8) {
+    if (cl != 1 || pair) return cudaErrorInvalidValue;
+#define MOE_GEMM_W8_CASE(BNV)                                                                     \
+    if (bn == BNV)                                                                                \
+      return mode == kGateUp                                                                      \
+                 ? launch_one<BNV, kGateUp, 1, false, true>(tm_w, tm_x, tm_lb, tm_lu, p, grid, s) \
+                 : launch_one<BNV, kDown, 1, false, true>(tm_w, tm_x, tm_lb, tm_lu, p, grid, s);
+    MOE_GEMM_W8_CASE(16)
+    MOE_GEMM_W8_CASE(32)
+    MOE_GEMM_W8_CASE(64)
+    MOE_GEMM_W8_CASE(128)
+    MOE_GEMM_W8_CASE(256)
+#undef MOE_GEMM_W8_CASE
+    return cudaErrorInvalidValue;
+  }
 #define MOE_GEMM_CASE(BNV, CLV, PV)                                                               \
   if (bn == BNV && cl == CLV && pair == PV)                                                       \
     return mode == kGateUp                                                                        \

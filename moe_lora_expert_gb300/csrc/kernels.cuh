@@ -168,6 +168,11 @@ struct GemmParams {
   __nv_bfloat16* out;             // [n, n_feat]
   int* status;
   uint64_t timeout_ns;
+  // FP8 weights (e4m3, 128 x 128 blocks): w_scale [E, scale_nb, scale_kb]
+  // float32, scale_nb = ceil(rows_per_expert / 128), scale_kb = ceil(K / 128).
+  const float* w_scale;
+  int scale_nb;
+  int scale_kb;
   // 1 when the kernel launched just before this one is the shrink, which
   // calls griddepcontrol.wait before it lets dependents launch: the routing
   // tables are then complete when this grid starts, and the weight stream
@@ -183,7 +188,9 @@ size_t gemm_smem_bytes(int bn, bool pair);
 int gemm_cluster_size(int bn);
 // pair: clusters of two CTAs sharing one M = 256 MMA (cta_group::2); cl = 2.
 bool gemm_use_pair(int bn);
-cudaError_t launch_expert_gemm(int mode, int bn, int cl, bool pair, const CUtensorMap& tm_w,
+// w8: FP8 block-scaled weights (tm_w is then a 1-byte view, p.w_scale set);
+// one CTA per tile (cl = 1, no pair).
+cudaError_t launch_expert_gemm(int mode, int bn, int cl, bool pair, bool w8, const CUtensorMap& tm_w,
                                const CUtensorMap& tm_x, const CUtensorMap& tm_lb,
                                const CUtensorMap& tm_lu, const GemmParams& p, int grid,
                                cudaStream_t s);

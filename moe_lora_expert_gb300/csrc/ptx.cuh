@@ -124,6 +124,18 @@ __device__ __forceinline__ void tma_load_2d_multicast(void* smem_dst, const CUte
       : "memory");
 }
 
+// Orders this thread's earlier generic-proxy writes to shared memory before
+// later async-proxy reads of it (TMA, tcgen05.mma operands).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Barrier among ``nthreads`` threads (whole warps) of the CTA on named
+// barrier ``id`` (0 is the one __syncthreads uses).
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // Cluster coordinates and a full cluster barrier (every thread of every CTA).
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

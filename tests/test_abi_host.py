@@ -161,9 +161,17 @@ def _valid_args(**over):
     # a valid shard passes the shard checks (then fails on the fake workspace size)
     ({"num_router_experts": 256, "local_expert_offset": 128, "workspace_bytes": 1024},
      m.MOE_ERR_WORKSPACE),
-    # a structure from before the shard fields: no sharding, checks go on
-    ({"struct_size": ctypes.sizeof(m.MoeLoraArgs) - 8, "hidden": None}, m.MOE_ERR_NULL),
-    ({"struct_size": ctypes.sizeof(m.MoeLoraArgs) - 12}, m.MOE_ERR_UNSUPPORTED),
+    # structures from before the shard fields, or before the weight-format
+    # fields: accepted with the defaults, checks go on
+    ({"struct_size": m.MoeLoraArgs.local_expert_offset.offset, "hidden": None}, m.MOE_ERR_NULL),
+    ({"struct_size": m.MoeLoraArgs.weight_format.offset, "hidden": None}, m.MOE_ERR_NULL),
+    ({"struct_size": m.MoeLoraArgs.local_expert_offset.offset - 4}, m.MOE_ERR_UNSUPPORTED),
+    # FP8 block-scaled weights
+    ({"weight_format": 2}, m.MOE_ERR_UNSUPPORTED),
+    ({"weight_format": m.MOE_WEIGHTS_FP8_E4M3_B128}, m.MOE_ERR_NULL),          # no scales
+    ({"weight_format": m.MOE_WEIGHTS_FP8_E4M3_B128, "w13_scale": 1 << 20, "w2_scale": (1 << 20) + 2},
+     m.MOE_ERR_ALIGN),
+    ({"weight_format": m.MOE_WEIGHTS_FP8_E4M3_B128, "H": 2056}, m.MOE_ERR_ALIGN),  # 1-byte rows
 ])
 def test_forward_rejects_on_host(lib, over, status):
     a = _valid_args(**over)
