@@ -483,7 +483,9 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   fp.e2p = e2p;
   fp.p2e = p2e;
   fp.tile_start = tile_start;
-  fp.tile_width_mask = (1u << moe::tile_width_index(16)) | (1u << moe::tile_width_index(128)) |
+  // widths read later: the 16-row shrink, the row-block shrink, the GEMM
+  fp.tile_width_mask = (1u << moe::tile_width_index(16)) |
+                       (1u << moe::tile_width_index(moe::rows_shrink_tile())) |
                        (1u << moe::tile_width_index(bn));
   fp.status = status;
   // Per 16-row tile, the adapters of its GEMM tile: lets the 16-row shrink
@@ -551,14 +553,14 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   sp.T = T;
   sp.e2p = e2p;
   sp.mapping = lora ? a->token_lora_mapping : nullptr;
-  // Many rows: 128-row tiles streamed through a cp.async pipeline (the
-  // per-token mode keeps the 16-token kernel).
   // Many rows, or a large rank with several rows per expert (the factor is
-  // then read once per 128 rows instead of once per 16): 128-row tiles.
+  // then read once per row tile instead of once per 16 rows): row tiles
+  // streamed through a cp.async pipeline.  The per-token mode keeps the
+  // 16-row kernel.
   bool row_blocks = n_local > 16 * static_cast<int64_t>(sms) ||
                     (r >= 64 && n_local >= 8 * std::min<int64_t>(E, n_local));
   if (const char* env = std::getenv("MOE_LORA_SHRINK_ROWS")) row_blocks = std::atoi(env) != 0;  // tuning
-  sp.tile_start128 = tile_start + moe::tile_width_index(128) * (E + 1);
+  sp.tile_start_rows = tile_start + moe::tile_width_index(moe::rows_shrink_tile()) * (E + 1);
   sp.gmask = fp.gmask;
   if ((row_blocks && !sp.per_token ? moe::launch_rows_shrink(sp, static_cast<int>(n), stream)
                                    : moe::launch_gather_shrink(sp, static_cast<int>(n), stream)) !=

@@ -50,16 +50,17 @@ struct GemmCfg {
   // Narrow (decode) tiles run two CTAs per SM so that two producers keep TMA
   // loads in flight; wide tiles run one CTA per SM with deeper stages.
   static constexpr int kCtasPerSm = BN <= 64 ? 2 : 1;
-  // FP8 weights add four converter warps.
-  static constexpr int kThreads = W8 ? 320 : 192;
+  // FP8 weights add kConvWarps converter warps (warps 6, 7, ...).
+  static constexpr int kConvWarps = 4;
+  static constexpr int kThreads = W8 ? 192 + 32 * kConvWarps : 192;
   static constexpr int kStageBudget = BN <= 64 ? (W8 ? 104 : 96) * 1024 : 200 * 1024;
   static constexpr int kABytes = 128 * 64 * 2;   // 128 rows x 64 K of bf16
   // A CTA of a pair holds half of the token tile.
   static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * 64 * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   // FP8: a deep ring of (raw 128 x 64 e4m3 weight tile, token tile) stages
-  // filled by TMA; the converter warps write the bf16 A tiles into a ring of
-  // two A-only stages.
+  // filled by TMA; the converter warps write the bf16 A tiles into a short
+  // ring of A-only stages.
   static constexpr int kW8Bytes = 128 * 64;
   static constexpr int kW8Stage = (kW8Bytes + kBBytes + 1023) / 1024 * 1024;
   static constexpr int kStagesRaw = W8 ? (BN <= 64 ? 3 : 4) : kStageBudget / kStageBytes;
@@ -227,13 +228,14 @@ __device__ __forceinline__ void load_lora_b_block(uint8_t* sA, const CUtensorMap
 // feature block for the whole token tile, so the epilogue is unchanged; the
 // epilogue warps of both CTAs release the even CTA's accumulator barrier.
 //
-// W8 (FP8 block-scaled weights, CL == 1): warp 0 streams raw e4m3 weight
-// tiles through the deep ring (full8/empty8); warps 6..9 convert: for each K
-// block they wait for a free bf16 stage, issue the token-tile (or LoRA) loads
-// into it, write the dequantized weight tile (e4m3 value times its 128 x 128
-// block scale, rounded to bf16) in the 128-byte-swizzled layout the MMA
-// reads, and release it with a second arrival on full.  MMA and epilogue
-// are unchanged.
+// W8 (FP8 block-scaled weights, CL == 1): warp 0 streams each K block's raw
+// e4m3 weight tile and its token tile through the deep ring (full8/empty8);
+// the converter warps wait for a free bf16 A stage, write the dequantized
+// weight tile (e4m3 value times its 128 x 128 block scale, rounded to bf16)
+// in the 128-byte-swizzled layout the MMA reads, and arrive on full, one
+// arrival per warp.  A LoRA block's bf16 B-factor tile goes straight to the
+// A stage by TMA.  The MMA reads A from the A ring and the token tile from
+// the deep ring; the epilogue is unchanged.
 template <int BN, int MODE, int CL, bool PAIR, bool W8>
 __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, PAIR, W8>::kCtasPerSm)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
@@ -272,7 +274,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
       mbar_init(&empty8[s], 1);
     }
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&full[s], W8 ? 4 : 1);  // FP8: one arrival per converter warp
+      mbar_init(&full[s], W8 ? C::kConvWarps : 1);  // FP8: one arrival per converter warp
       // multicast: every CTA of the cluster releases the stage; pair: the
       // leader's commit arrives once in each CTA
       mbar_init(&empty[s], kMulticast ? CL : 1);
@@ -673,13 +675,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
     }
   } else if constexpr (W8) {
     // ------------------------------------------------- FP8 converters
-    // Warps 6..9, each on its own: converter warp cw writes tile rows
-    // [32 cw, 32 cw + 32).  Lane l takes 16-byte chunks 128 cw + l + 32 i of
-    // the 8 KB e4m3 tile (row = chunk / 4, columns 16 (chunk % 4) + 0..15)
-    // and writes them as two 16-byte bf16 chunks of the row at the 128-byte
-    // swizzle positions (chunk j of row r at j ^ (r % 8)), then arrives on
-    // the stage's full barrier (4 arrivals complete it; for a LoRA block
-    // warp 6's arrival also carries the byte count of the B-factor tile).
+    // Warps 6.., each on its own: converter warp cw writes tile rows
+    // [kRows cw, kRows (cw + 1)).  Lane l takes 16-byte chunks
+    // 4 kRows cw + l + 32 i of the 8 KB e4m3 tile (row = chunk / 4, columns
+    // 16 (chunk % 4) + 0..15) and writes them as two 16-byte bf16 chunks of
+    // the row at the 128-byte swizzle positions (chunk j of row r at
+    // j ^ (r % 8)), then arrives on the stage's full barrier (kConvWarps
+    // arrivals complete it; for a LoRA block warp 6's arrival also carries
+    // the byte count of the B-factor tile).
+    constexpr int kRows = 128 / C::kConvWarps;
     const int cw = warp - 6;
     const uint64_t pol_b = l2_policy_evict_last();
     uint32_t sa = 0, pha = 0, s8 = 0, ph8 = 0, armed = 0, armed_parity = 0;
@@ -724,8 +728,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
           const uint8_t* src8 = w8ring + s8 * C::kW8Stage;
           const int kblk = (b * 64) >> 7;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int c = 128 * cw + lane + 32 * i;
+          for (int i = 0; i < kRows / 8; ++i) {
+            const int c = 4 * kRows * cw + lane + 32 * i;
             const int r = c >> 2, part = c & 3;
             int wrow;  // the weight row behind tile row r
             if (MODE == kGateUp) wrow = ((r >> 4) & 1) * p.n_feat + wk.fb * 64 + (r >> 5) * 16 + (r & 15);

@@ -108,7 +108,7 @@ struct ShrinkParams {
   int T;
   const int32_t* e2p;           // [T * top_k]
   const int32_t* mapping;       // [T]
-  const int32_t* tile_start128; // [E + 1] prefix of ceil(n_e / 128) (row-block kernel)
+  const int32_t* tile_start_rows;  // [E + 1] prefix of ceil(n_e / rows_shrink_tile()) (row-block kernel)
   // Or null.  gmask[t]: adapters present in the expert-GEMM token tile that
   // contains 16-row tile t.  The CTA of (t, adapter a) exits at once when a is
   // absent there (no GEMM tile reads a's columns of these rows), unless it
@@ -117,9 +117,10 @@ struct ShrinkParams {
 };
 int shrink_chunk(int K, int rank, size_t smem_budget);
 cudaError_t launch_gather_shrink(const ShrinkParams& p, int n_rows, cudaStream_t s);
-// Many rows: 128-row tiles of one expert, K streamed through a cp.async
-// pipeline.  Not for the per-token mode.  Uses p.tile_start128.
+// Many rows: rows_shrink_tile()-row tiles of one expert, K streamed through a cp.async
+// pipeline.  Not for the per-token mode.  Uses p.tile_start_rows.
 cudaError_t launch_rows_shrink(const ShrinkParams& p, int n_rows, cudaStream_t s);
+int rows_shrink_tile();  // rows per CTA of the row-block shrink (a tile width of the tables)
 
 // ------------------------------------------------- one-CTA permute (fused)
 struct FusedPermuteParams {

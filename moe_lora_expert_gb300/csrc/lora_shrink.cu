@@ -285,8 +285,8 @@ cudaError_t launch_gather_shrink(const ShrinkParams& p, int n_rows, cudaStream_t
 }
 
 // ------------------------------------------------------ row-block variant
-// For many rows (prefill).  One CTA per (128-row tile of one expert, adapter
-// slot a).  The CTA takes the tile's rows of adapter a (slot 0 with a gather
+// For many rows (prefill).  One CTA per (kRowTile-row tile of one expert,
+// adapter slot a), two threads per tile row.  The CTA takes the tile's rows of adapter a (slot 0 with a gather
 // to do: all rows, for the copy) and streams K in 64-element chunks through
 // a kRowStages-deep cp.async pipeline; warp w owns compacted rows
 // [16w, 16w + 16) and keeps their u in registers for the whole K, so no
@@ -296,36 +296,43 @@ cudaError_t launch_gather_shrink(const ShrinkParams& p, int n_rows, cudaStream_t
 // eight 16-byte chunks, chunk j at position j ^ 4 (row & 1): the 8 lanes of
 // a quarter-warp read rows g, g' of both parities and four chunks each, and
 // land in 8 distinct bank groups.
-constexpr int kRowStages = 3;
-constexpr int kRowTile = 128;
+// 64-row tiles and four stages: at prefill sizes (tens of thousands of rows)
+// this gives every SM four to five resident CTAs with three chunks in flight
+// each; 128-row tiles with three stages left the SMs latency-bound.
+constexpr int kRowStages = 4;
+constexpr int kRowTile = 64;
+constexpr int kRowThreads = 2 * kRowTile;  // warp w owns compacted rows [16w, 16w + 16)
+constexpr int kRowStride = kRowThreads / 8;  // rows between one thread's copy rows
 
-__host__ __device__ inline size_t rows_shrink_smem_bytes(int rank) {
+int rows_shrink_tile() { return kRowTile; }
+
+__host__ __device__ inline size_t rows_shrink_smem_bytes(int rank, int E) {
   return static_cast<size_t>(kRowStages) * (kRowTile + rank) * 128 +
-         static_cast<size_t>(kRowTile) * rank * 2;
+         static_cast<size_t>(kRowTile) * rank * 2 + static_cast<size_t>(E + 1) * 4;
 }
 
 __device__ __forceinline__ int swz16(int row, int j) { return (j ^ ((row & 1) << 2)) * 16; }
 
 template <int NT>
-__global__ void __launch_bounds__(kShrinkThreads) rows_shrink_kernel(const ShrinkParams p) {
+__global__ void __launch_bounds__(kRowThreads) rows_shrink_kernel(const ShrinkParams p) {
   constexpr int R = 8 * NT;
   constexpr int kXStage = kRowTile * 128;
   constexpr int kStage = kXStage + R * 128;
   extern __shared__ int4 rows_smem[];
   uint8_t* stages = reinterpret_cast<uint8_t*>(rows_smem);
-  __nv_bfloat16* s_u = reinterpret_cast<__nv_bfloat16*>(stages + kRowStages * kStage);  // [128][R]
+  __nv_bfloat16* s_u = reinterpret_cast<__nv_bfloat16*>(stages + kRowStages * kStage);  // [kRowTile][R]
+  int* s_ts = reinterpret_cast<int*>(s_u + kRowTile * R);                                // [E + 1]
   __shared__ int s_rows[kRowTile];  // tile row of compacted row i
   __shared__ int s_adp[kRowTile];   // adapter of tile row i
-  __shared__ int s_warp_cnt[kShrinkThreads / 32];
+  __shared__ int s_warp_cnt[kRowThreads / 32];
   __shared__ int s_info[4];
-  __shared__ int s_ts[MOE_MAX_EXPERTS + 1];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int a = static_cast<int>(blockIdx.y);
 
   pdl_wait();
-  for (int i = tid; i <= p.E; i += kShrinkThreads) s_ts[i] = p.tile_start128[i];
+  for (int i = tid; i <= p.E; i += kRowThreads) s_ts[i] = p.tile_start_rows[i];
   __syncthreads();
   if (tid == 0) {
     const int tile = blockIdx.x;
@@ -362,7 +369,7 @@ __global__ void __launch_bounds__(kShrinkThreads) rows_shrink_kernel(const Shrin
   if (lane == 0) s_warp_cnt[warp] = __popc(bal);
   __syncthreads();
   int before = 0, m = 0;
-  for (int w = 0; w < kShrinkThreads / 32; ++w) {
+  for (int w = 0; w < kRowThreads / 32; ++w) {
     const int c = s_warp_cnt[w];
     if (w < warp) before += c;
     m += c;
@@ -377,7 +384,7 @@ __global__ void __launch_bounds__(kShrinkThreads) rows_shrink_kernel(const Shrin
   const bool compute = lora && m > 0;
 
   // This thread's share of every chunk: column jc of compacted rows
-  // (tid >> 3) + 32 q, and column jc of factor rows (tid >> 3) + 32 q.
+  // (tid >> 3) + kRowStride q, and column jc of factor rows (tid >> 3) + kRowStride q.
   const int jc = tid & 7;
   const __nv_bfloat16* xsrc[4];
   __nv_bfloat16* gdst[4];
@@ -385,7 +392,7 @@ __global__ void __launch_bounds__(kShrinkThreads) rows_shrink_kernel(const Shrin
   bool xval[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const int i = (tid >> 3) + 32 * q;
+    const int i = (tid >> 3) + kRowStride * q;
     xval[q] = i < m;
     const int tr = xval[q] ? s_rows[i] : 0;
     const int src = p.p2e != nullptr ? p.p2e[row0 + tr] / p.top_k : row0 + tr;
@@ -393,13 +400,13 @@ __global__ void __launch_bounds__(kShrinkThreads) rows_shrink_kernel(const Shrin
     gdst[q] = do_gather ? p.gathered + static_cast<size_t>(row0 + tr) * K + jc * 8 : nullptr;
     xoff[q] = static_cast<uint32_t>(i * 128 + swz16(i, jc));
   }
-  constexpr int kFQ = (R + 31) / 32;  // factor rows per thread (rank up to 128)
+  constexpr int kFQ = (R + kRowStride - 1) / kRowStride;  // factor rows per thread
   const __nv_bfloat16* fsrc[kFQ > 0 ? kFQ : 1];
   uint32_t foff[kFQ > 0 ? kFQ : 1];
   bool fval[kFQ > 0 ? kFQ : 1];
 #pragma unroll
   for (int q = 0; q < kFQ; ++q) {
-    const int fr = (tid >> 3) + 32 * q;
+    const int fr = (tid >> 3) + kRowStride * q;
     fval[q] = compute && fr < R;
     fsrc[q] = fval[q] ? Af + static_cast<size_t>(fr) * K + jc * 8 : p.X;
     foff[q] = static_cast<uint32_t>(kXStage + fr * 128 + swz16(fr, jc));
@@ -469,7 +476,7 @@ __global__ void __launch_bounds__(kShrinkThreads) rows_shrink_kernel(const Shrin
     if (p.U != nullptr) {
       // u of the compacted rows into s_u[tile row] (rows of adapter a only);
       // then columns [a r, a r + r) of every row of the tile: u or 0.
-      for (int i = tid; i < kRowTile * R; i += kShrinkThreads) s_u[i] = __float2bfloat16_rn(0.f);
+      for (int i = tid; i < kRowTile * R; i += kRowThreads) s_u[i] = __float2bfloat16_rn(0.f);
       __syncthreads();
       if (compute && warp * 16 < m) {
         const float sc = p.scaling[a];
@@ -492,7 +499,7 @@ __global__ void __launch_bounds__(kShrinkThreads) rows_shrink_kernel(const Shrin
       __syncthreads();
       const int ld = p.num_adapters * R;
       constexpr int vpr = R / 8;
-      for (int v = tid; v < nrows * vpr; v += kShrinkThreads) {
+      for (int v = tid; v < nrows * vpr; v += kRowThreads) {
         const int row = v / vpr, c = (v - row * vpr) * 8;
         *reinterpret_cast<uint4*>(p.U + static_cast<size_t>(row0 + row) * ld + a * R + c) =
             *reinterpret_cast<const uint4*>(s_u + row * R + c);
@@ -506,12 +513,12 @@ cudaError_t launch_rows_shrink(const ShrinkParams& p, int n_rows, cudaStream_t s
   const int NT = p.rank / 8;
   const int tiles = (n_rows + kRowTile - 1) / kRowTile + (p.E < n_rows ? p.E : n_rows);
   const dim3 grid(tiles, (NT > 0 && p.U != nullptr) ? p.num_adapters : 1);
-  const size_t smem = rows_shrink_smem_bytes(p.U != nullptr ? p.rank : 0);
+  const size_t smem = rows_shrink_smem_bytes(p.U != nullptr ? p.rank : 0, p.E);
 #define MOE_ROWS_CASE(N)                                                                          \
   case N: {                                                                                       \
     cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(rows_shrink_kernel<N>), (int)smem); \
     if (err != cudaSuccess) return err;                                                           \
-    return launch_pdl(rows_shrink_kernel<N>, grid, dim3(kShrinkThreads), smem, s, p);             \
+    return launch_pdl(rows_shrink_kernel<N>, grid, dim3(kRowThreads), smem, s, p);             \
   }
   switch (p.U != nullptr ? NT : 0) {
     MOE_ROWS_CASE(0) MOE_ROWS_CASE(1) MOE_ROWS_CASE(2) MOE_ROWS_CASE(3)
