@@ -71,8 +71,12 @@ struct GemmCfg {
   static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr int kMetaBytes = 512;                         // barriers, flags
   static constexpr int kTableBytes = 2 * (MOE_MAX_EXPERTS + 1) * 4;
+  // Epilogue: a 1 KB staging tile per epilogue warp (16 token columns of its
+  // features), so the output leaves in 16-byte row segments.
+  static constexpr int kEpiOffset = (kMetaBytes + kTableBytes + 15) / 16 * 16;
+  static constexpr int kEpiBytes = 4 * 1024;
   static constexpr int kSmemBytes =
-      1024 + kARingBytes + kStages8 * kW8Stage + kMetaBytes + kTableBytes;
+      1024 + kARingBytes + kStages8 * kW8Stage + kEpiOffset + kEpiBytes;
   static_assert((2 * kStages + 2 * kStages8 + 6) * 8 + 16 <= kMetaBytes, "barriers fit");
   static_assert(kCtasPerSm * (kSmemBytes + 1024) <= 233472, "the CTAs of an SM fit its shared memory");
 };
@@ -262,6 +266,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_off = reinterpret_cast<int*>(meta + C::kMetaBytes);
   int* s_ts = s_off + (MOE_MAX_EXPERTS + 1);
+  uint8_t* s_epi = meta + C::kEpiOffset;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool use_lora = p.num_adapters > 0 && p.rank > 0;
@@ -633,36 +638,51 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
       if (!ok) break;
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      // Per 16 columns: TMEM -> registers -> (SwiGLU) -> bf16 staging tile
+      // [column][feature] -> 16-byte row segments to global memory.  The
+      // output feature count is a multiple of 8, so an 8-feature segment is
+      // either wholly inside or wholly outside the output.
+      uint8_t* stg = s_epi + q * 1024;
+      __nv_bfloat16* stg16 = reinterpret_cast<__nv_bfloat16*>(stg);
       for (int c0 = 0; c0 < ncols; c0 += 16) {
         float v[16];
         tmem_ld16(t_row + c0, v);
+        const int col = c0 + (lane >> 1);  // the column this lane writes out
         if (MODE == kGateUp) {
           // lanes < 16 hold gate rows, lanes >= 16 the up rows of the same
           // 16 features.  Column pairs (2i, 2i+1): the low half finishes
           // column 2i, the high half column 2i+1, after one exchange.
           const bool hi = lane >= 16;
-          const int feat = wk.fb * 64 + q * 16 + (lane & 15);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float send = hi ? v[2 * i] : v[2 * i + 1];
             const float recv = __shfl_xor_sync(kFullMask, send, 16);
             const float gate = hi ? recv : v[2 * i];
             const float up = hi ? v[2 * i + 1] : recv;
-            const int col = c0 + 2 * i + (hi ? 1 : 0);
-            if (col < wk.nrows && feat < p.n_feat) {
-              const float h = gate / (1.0f + expf(-gate)) * up;
-              p.out[static_cast<size_t>(wk.row0 + col) * p.n_feat + feat] = __float2bfloat16_rn(h);
-            }
+            const float h = __fdividef(gate, 1.0f + __expf(-gate)) * up;
+            stg16[(2 * i + (hi ? 1 : 0)) * 16 + (lane & 15)] = __float2bfloat16_rn(h);
           }
+          __syncwarp();
+          // lane L: column L / 2, features 8 (L % 2) .. + 7 of the warp's 16
+          const int feat = wk.fb * 64 + q * 16 + 8 * (lane & 1);
+          const uint4 o = *reinterpret_cast<const uint4*>(stg + lane * 16);
+          if (col < wk.nrows && feat < p.n_feat)
+            *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(wk.row0 + col) * p.n_feat + feat) = o;
         } else {
-          const int feat = wk.fb * 128 + q * 32 + lane;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int col = c0 + i;
-            if (col < wk.nrows && feat < p.n_feat)
-              p.out[static_cast<size_t>(wk.row0 + col) * p.n_feat + feat] = __float2bfloat16_rn(v[i]);
+          for (int i = 0; i < 16; ++i) stg16[i * 32 + lane] = __float2bfloat16_rn(v[i]);
+          __syncwarp();
+          // lane L: column L / 2, features 16 (L % 2) .. + 15 of the warp's 32
+          const int feat = wk.fb * 128 + q * 32 + 16 * (lane & 1);
+          const uint4 o0 = *reinterpret_cast<const uint4*>(stg + lane * 32);
+          const uint4 o1 = *reinterpret_cast<const uint4*>(stg + lane * 32 + 16);
+          if (col < wk.nrows) {
+            __nv_bfloat16* dst = p.out + static_cast<size_t>(wk.row0 + col) * p.n_feat + feat;
+            if (feat < p.n_feat) *reinterpret_cast<uint4*>(dst) = o0;
+            if (feat + 8 < p.n_feat) *reinterpret_cast<uint4*>(dst + 8) = o1;
           }
         }
+        __syncwarp();  // the staging tile is free again
       }
       tc_fence_before_sync();
       __syncwarp();
