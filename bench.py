@@ -103,13 +103,34 @@ def algorithmic_work(wl, ids, mapping, fp8=False):
     return work
 
 
-def kernels_per_forward(wl):
-    """Kernels one moe_lora_forward launches (mirrors the library's choices)."""
+def auto_tile_n(n_rows, E):
+    """The library's default token-tile width (api.cu, auto_tile_n)."""
+    touched = max(1, min(E, n_rows))
+    avg = -(-n_rows // touched)
+    bn = 16
+    while bn < 256 and bn < 2 * avg:
+        bn *= 2
+    while bn < 64 and bn < 4 * avg:
+        bn *= 2
+    return bn
+
+
+def kernels_per_forward(wl, fp8=False):
+    """Kernels one moe_lora_forward launches (mirrors the library's choices):
+    routing (unless fused into the one-CTA permute), the permute (one CTA, or
+    count + scan + scatter), the gather/gate_up shrink, the gate_up GEMM, the
+    down shrink (LoRA, unless it runs inside the down GEMM), the down GEMM
+    and the finalize."""
     n, E = wl.T * wl.top_k, wl.E
     small = n <= 8192 and (((n + 1) & ~1) * 4 + 32 * E * 4 + (E + 1) * 4) <= 200 * 1024
     fuse_route = small and wl.T <= 128
     lora = wl.num_adapters > 0 and wl.rank > 0
-    return ((0 if fuse_route else 1) + (1 if small else 4) + 1 + 1 + (1 if lora else 0) + 1 + 1)
+    # in-GEMM shrinks: 16-wide tiles (at most four rows per expert on average,
+    # so never the row-block shrink), rank <= 32, per-expert gate_up A factors
+    fuse_shrink = (lora and not fp8 and small and auto_tile_n(n, E) == 16 and wl.rank <= 32
+                   and not wl.shared_outer)
+    return ((0 if fuse_route else 1) + (1 if small else 3) + 1 + 1 +
+            (1 if lora and not fuse_shrink else 0) + 1 + 1)
 
 
 def max_over_ranks(value_ms, dist=None, device=None):
@@ -460,7 +481,7 @@ def run_ours(args):
            "frac": round(t_roof / (ms_per_step / 1e3), 4), "bytes": work["bytes"], "flops": work["flops"],
            "distinct_experts": work["distinct_experts"], "lora_pairs": work["lora_pairs"]}
 
-    n_kernels = kernels_per_forward(wl)
+    n_kernels = kernels_per_forward(wl, fp8)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),

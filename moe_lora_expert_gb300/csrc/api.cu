@@ -405,6 +405,8 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
       ws + pl.permute_scratch + align_up(nchunks * E * sizeof(int32_t)));
   uint64_t* gmask = reinterpret_cast<uint64_t*>(
       reinterpret_cast<uint8_t*>(tile_start) + align_up(moe::kNumTileWidths * (E + 1) * sizeof(int32_t)));
+  int* flags_gu = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(gmask) + moe::gmask_bytes(static_cast<int>(n), E));
+  int* flags_dn = flags_gu + moe::shrink_flag_words(static_cast<int>(n), E);
   __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(ws + pl.permuted_hidden);
   __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(ws + pl.expert_out);
   __nv_bfloat16* U = reinterpret_cast<__nv_bfloat16*>(ws + pl.lora_u);
@@ -433,6 +435,22 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   if (pair) cl = 2;  // a pair is a cluster of two; each CTA loads bn / 2 token rows
   const int sms = num_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
+  // Many rows, or a large rank with several rows per expert (the factor is
+  // then read once per row tile instead of once per 16 rows): row tiles
+  // streamed through a cp.async pipeline.  The per-token mode keeps the
+  // 16-row kernel.
+  bool row_blocks = n_local > 16 * static_cast<int64_t>(sms) ||
+                    (r >= 64 && n_local >= 8 * std::min<int64_t>(E, n_local));
+  if (const char* env = std::getenv("MOE_LORA_SHRINK_ROWS")) row_blocks = std::atoi(env) != 0;  // tuning
+  // Decode-sized tiles: the LoRA shrinks run inside the expert GEMMs (their
+  // epilogue warps are idle until the first accumulator is ready), so no
+  // shrink kernel sits between the GEMMs; the gate_up shrink kernel only
+  // gathers the rows.  Needs the one-CTA permute (it clears the tile flags),
+  // one CTA per 16-wide tile, rank <= 32 and per-expert gate_up A factors.
+  // MOE_LORA_FUSE_SHRINK=0 turns it off (tuning).
+  bool fuse_shrink = lora && !w8 && small_permute && bn == 16 && cl == 1 && !pair && r <= 32 &&
+                     !row_blocks && a->gate_up.a_stride_expert != 0;
+  if (const char* env = std::getenv("MOE_LORA_FUSE_SHRINK")) fuse_shrink = fuse_shrink && std::atoi(env) != 0;
   const uint64_t timeout_ns =
       static_cast<uint64_t>(a->wait_timeout_ms ? a->wait_timeout_ms : 2000) * 1000000ull;
 
@@ -492,6 +510,8 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   // skip (tile, adapter) pairs without work.
   fp.gmask = (lora && small_permute) ? gmask : nullptr;
   fp.gemm_bn = bn;
+  fp.clear_flags = fuse_shrink ? flags_gu : nullptr;
+  fp.clear_count = fuse_shrink ? static_cast<int>(2 * moe::shrink_flag_words(static_cast<int>(n), E)) : 0;
   fp.id_offset = shard_off;
   fp.id_limit = R;
   if (!fuse_route &&
@@ -544,7 +564,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   sp.rank = r;
   for (int i = 0; i < MOE_MAX_ADAPTERS; ++i)
     sp.scaling[i] = (a->adapter_scaling != nullptr && i < A) ? a->adapter_scaling[i] : a->scaling;
-  sp.U = lora ? U : nullptr;
+  sp.U = (lora && !fuse_shrink) ? U : nullptr;  // fused: the gather alone
   sp.status = status;
   sp.timeout_ns = timeout_ns;
   sp.kc = moe::shrink_chunk(H, r, shrink_budget);
@@ -553,13 +573,6 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   sp.T = T;
   sp.e2p = e2p;
   sp.mapping = lora ? a->token_lora_mapping : nullptr;
-  // Many rows, or a large rank with several rows per expert (the factor is
-  // then read once per row tile instead of once per 16 rows): row tiles
-  // streamed through a cp.async pipeline.  The per-token mode keeps the
-  // 16-row kernel.
-  bool row_blocks = n_local > 16 * static_cast<int64_t>(sms) ||
-                    (r >= 64 && n_local >= 8 * std::min<int64_t>(E, n_local));
-  if (const char* env = std::getenv("MOE_LORA_SHRINK_ROWS")) row_blocks = std::atoi(env) != 0;  // tuning
   sp.tile_start_rows = tile_start + moe::tile_width_index(moe::rows_shrink_tile()) * (E + 1);
   sp.gmask = fp.gmask;
   if ((row_blocks && !sp.per_token ? moe::launch_rows_shrink(sp, static_cast<int>(n), stream)
@@ -590,13 +603,23 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.w_scale = w8 ? a->w13_scale : nullptr;
   gp.scale_nb = (2 * I + 127) / 128;
   gp.scale_kb = (H + 127) / 128;
+  gp.fuse_shrink = fuse_shrink ? 1 : 0;
+  if (fuse_shrink) {
+    gp.sx = xp;
+    gp.sa = static_cast<const __nv_bfloat16*>(a->gate_up.A);
+    gp.sa_stride_adapter = a->gate_up.a_stride_adapter;
+    gp.sa_stride_expert = a->gate_up.a_stride_expert;
+    gp.su = U;
+    gp.tile_flags = flags_gu;
+    for (int i = 0; i < MOE_MAX_ADAPTERS; ++i) gp.sscale[i] = sp.scaling[i];
+  }
   if (moe::launch_expert_gemm(moe::kGateUp, bn, cl, pair, w8, tm_w13, tm_xp, tm_bgu, tm_u, gp,
                               sms * moe::gemm_ctas_per_sm(bn), stream) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
   if (!mark()) return MOE_ERR_CUDA;
-  // 5. down LoRA shrink: V = s * A_dn h
-  if (lora) {
+  // 5. down LoRA shrink: V = s * A_dn h (fused: inside the down GEMM)
+  if (lora && !fuse_shrink) {
     sp.X = h;
     sp.p2e = nullptr;
     sp.K = I;
@@ -621,7 +644,17 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.lb_row_stride_adapter = dn_rs_a;
   gp.lb_row_stride_expert = dn_rs_e;
   gp.out = y;
-  gp.tables_ready = lora ? 1 : 0;  // else the gate_up GEMM precedes this launch
+  // After the shrink, or (fused) after the gate_up GEMM, which runs no
+  // earlier than the gate_up shrink's own wait: the tables are complete.
+  gp.tables_ready = lora ? 1 : 0;
+  if (fuse_shrink) {
+    gp.sx = h;
+    gp.sa = static_cast<const __nv_bfloat16*>(a->down.A);
+    gp.sa_stride_adapter = a->down.a_stride_adapter;
+    gp.sa_stride_expert = a->down.a_stride_expert;
+    gp.su = V;
+    gp.tile_flags = flags_dn;
+  }
   gp.w_scale = w8 ? a->w2_scale : nullptr;
   gp.scale_nb = (H + 127) / 128;
   gp.scale_kb = (I + 127) / 128;

@@ -146,7 +146,8 @@ __device__ __forceinline__ void raise_timeout(int* status, volatile int* abort_f
 enum WaitSite {
   kWaitProducerW8 = 1, kWaitProducer = 2, kWaitMmaAccEmpty = 4, kWaitMmaFull = 5,
   kWaitMmaFull8 = 6, kWaitEpilogue = 7, kWaitConvEmpty = 8, kWaitConvFull8 = 9,
-  kWaitDrainProducer = 10, kWaitDrainProducerW8 = 11, kWaitDrainConv = 12, kWaitDrainMma = 13
+  kWaitDrainProducer = 10, kWaitDrainProducerW8 = 11, kWaitDrainConv = 12, kWaitDrainMma = 13,
+  kWaitShrinkFlag = 14
 };
 
 // A teardown wait that ran out: the status and its place, no abort (the
@@ -166,6 +167,90 @@ __device__ __forceinline__ void raise_timeout_at(int* status, volatile int* abor
     status[3] = (unit << 16) | ((blk & 0xFFF) << 4) | (stage & 15);
   }
   *abort_flag = 1;
+}
+
+// The LoRA shrink of rows blockIdx.x, blockIdx.x + gridDim.x, ... of the
+// permuted rows, by the four epilogue warps (ew = 0..3) before their first
+// accumulator (GemmParams::fuse_shrink).  For row p with adapter
+// a = row_adapter[p] >= 0, su[p, a r + i] = bf16(s_a sum_k A[a, e][i][k]
+// sx[p][k]) for i < r; every other column of the row is zero.  The 128
+// threads split K in 8-element pieces (thread j takes k = 8 j + 1024 m), sum
+// their pieces for 8 outputs at a time, reduce across each warp by shuffles
+// and across the four warps in shared memory (s_red, 4 x 32 floats).  Each
+// finished row adds one to the flag of its token tile (release, after a
+// proxy fence that makes the row visible to other CTAs' TMA reads); a tile
+// is complete when its flag equals its row count.
+template <int BN>
+__device__ void shrink_rows_in_gemm(const GemmParams& p, const int* s_off, const int* s_ts, int ew,
+                                    int lane, float* s_red) {
+  const int R = p.rank, ld = p.num_adapters * p.rank, K = p.K;
+  const int tid = ew * 32 + lane;
+  const int nrows_all = s_off[p.E];
+  for (int prow = blockIdx.x; prow < nrows_all; prow += gridDim.x) {
+    int lo = 0, hi = p.E - 1;  // expert of the row: largest e with s_off[e] <= prow
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_off[mid] <= prow) lo = mid;
+      else hi = mid - 1;
+    }
+    const int e = lo;
+    const int tile = s_ts[e] + (prow - s_off[e]) / BN;
+    const int a = __ldcg(p.row_adapter + prow);
+    __nv_bfloat16* urow = p.su + static_cast<size_t>(prow) * ld;
+    // the other adapters' columns: zero (8 columns per store)
+    for (int c = tid * 8; c < ld; c += 128 * 8)
+      if (a < 0 || c / R != a) *reinterpret_cast<uint4*>(urow + c) = make_uint4(0, 0, 0, 0);
+    if (a >= 0) {  // uniform over the CTA
+      const __nv_bfloat16* x = p.sx + static_cast<size_t>(prow) * K;
+      const __nv_bfloat16* A = p.sa + a * p.sa_stride_adapter + static_cast<int64_t>(e) * p.sa_stride_expert;
+      for (int i0 = 0; i0 < R; i0 += 8) {
+        float acc[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+        for (int k = tid * 8; k < K; k += 128 * 8) {
+          const uint4 xv = __ldcg(reinterpret_cast<const uint4*>(x + k));
+          const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xv);
+          float xf[8];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const float2 f = __bfloat1622float2(x2[h]);
+            xf[2 * h] = f.x;
+            xf[2 * h + 1] = f.y;
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint4 av = __ldg(reinterpret_cast<const uint4*>(A + static_cast<size_t>(i0 + q) * K + k));
+            const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&av);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const float2 f = __bfloat1622float2(a2[h]);
+              acc[q] = fmaf(f.x, xf[2 * h], acc[q]);
+              acc[q] = fmaf(f.y, xf[2 * h + 1], acc[q]);
+            }
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) acc[q] += __shfl_xor_sync(kFullMask, acc[q], off);
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) s_red[ew * 32 + i0 + q] = acc[q];
+        }
+      }
+      named_barrier_sync(1, 128);  // every warp's partial sums of this row
+      if (ew == 0 && lane < R)
+        urow[a * R + lane] = __float2bfloat16_rn(
+            p.sscale[a] * (s_red[lane] + s_red[32 + lane] + s_red[64 + lane] + s_red[96 + lane]));
+    }
+    fence_proxy_async_global();
+    named_barrier_sync(1, 128);  // the row is written; s_red is free again
+    if (tid == 0) {
+      __threadfence();
+      red_release_gpu_add(p.tile_flags + tile, 1);
+    }
+  }
 }
 
 // Weight-side (A operand) loads of one K block: 128 rows of the feature block.
@@ -468,7 +553,21 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
             amask &= amask - 1;
           }
         }
-        if (lane == 0) {
+        if (lane == 0 && p.fuse_shrink && b == nk) {
+          // the tile's LoRA rows come from the in-kernel shrink of other
+          // CTAs (or this one): wait until all of them are published
+          const int* flag = p.tile_flags + w / FBg;
+          const uint64_t t0 = global_timer_ns();
+          while (ld_acquire_gpu(flag) < wk.nrows) {
+            if (*abort_flag || global_timer_ns() - t0 > p.timeout_ns) {
+              ok = false;
+              break;
+            }
+          }
+          if (ok) fence_proxy_async_global();
+          else if (!*abort_flag) raise_timeout_at(p.status, abort_flag, kWaitShrinkFlag, w, b, stage);
+        }
+        if (lane == 0 && ok) {
           ok = wait_or_abort<PAIR>(&empty[stage], phase ^ 1, p.timeout_ns, abort_flag);
           if (ok) {
             uint8_t* sA = smem + stage * C::kStageBytes;
@@ -625,6 +724,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     uint32_t acc = 0, acc_phase = 0;
+    if constexpr (CL == 1) {
+      if (p.fuse_shrink) {  // the LoRA rows of this CTA's tiles, before any accumulator is ready
+        pdl_wait();
+        shrink_rows_in_gemm<BN>(p, s_off, s_ts, warp - 2, lane, reinterpret_cast<float*>(s_epi));
+      }
+    }
     for (int w = unit0; w < total_work; w += unit_step) {
       if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
       const Work wk = decode_work<BN>(w, crank, CL, s_off, s_ts, p.E, FBg);

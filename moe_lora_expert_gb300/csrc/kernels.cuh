@@ -75,6 +75,9 @@ constexpr int kPermuteChunk = 1024;
 // [kNumTileWidths, E + 1], then the 16-row-tile adapter masks (gmask_bytes).
 size_t permute_scratch_bytes(int n, int E);
 size_t gmask_bytes(int n, int E);
+// Tile flags of the in-kernel shrink: two arrays (gate_up, down) of
+// ceil(n / 16) + E + 1 words each, after the adapter masks.
+size_t shrink_flag_words(int n, int E);
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s);
 
 // ------------------------------------------------- gather + LoRA shrink
@@ -144,6 +147,8 @@ struct FusedPermuteParams {
   // tile prefix (tile_width_mask bit 0).
   uint64_t* gmask;
   int gemm_bn;
+  int* clear_flags;             // or null: clear_count words zeroed first
+  int clear_count;
 };
 bool small_permute_fits(int n, int E);
 cudaError_t launch_small_permute(const FusedPermuteParams& p, cudaStream_t s);
@@ -179,6 +184,21 @@ struct GemmParams {
   // tables are then complete when this grid starts, and the weight stream
   // may begin before this grid's own wait.  0: everything waits first.
   int tables_ready;
+  // LoRA shrink inside the kernel (narrow tiles, one CTA per tile, rank <=
+  // 32): before their first accumulator, the epilogue warps of CTA b write
+  // permuted rows b, b + gridDim.x, ... of su = bf16(s_a A[a, e] x) (the
+  // row's own adapter's columns; zeros in the others) and count each row on
+  // its token tile's flag; the producer waits until a tile's flag equals its
+  // row count before the tile's first LoRA block.  The flags are cleared by
+  // the permute of the same forward.
+  int fuse_shrink;
+  const __nv_bfloat16* sx;             // [n, K]: the token rows (xp or h)
+  const __nv_bfloat16* sa;             // A factors, rows of K elements
+  int64_t sa_stride_adapter;           // elements between adapters
+  int64_t sa_stride_expert;            // elements between experts
+  __nv_bfloat16* su;                   // [n, num_adapters * rank]
+  int* tile_flags;                     // [tiles of this width]
+  float sscale[MOE_MAX_ADAPTERS];      // per adapter
 };
 enum GemmMode { kGateUp = 0, kDown = 1 };
 int gemm_stage_count(int bn, bool pair);

@@ -266,14 +266,14 @@ cudaError_t launch_gather_shrink(const ShrinkParams& p, int n_rows, cudaStream_t
   const int NT = p.rank / 8;
   const int tiles = p.per_token ? (p.T + 15) / 16 : (n_rows + 15) / 16 + (p.E < n_rows ? p.E : n_rows);
   const dim3 grid(tiles, (NT > 0 && p.U != nullptr) ? p.num_adapters : 1);
-  const size_t smem = shrink_smem_bytes(p.kc, p.rank);
+  const size_t smem = shrink_smem_bytes(p.kc, p.U != nullptr ? p.rank : 0);
 #define MOE_SHRINK_CASE(N)                                                                        \
   case N: {                                                                                       \
     cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(gather_shrink_kernel<N>), (int)smem); \
     if (err != cudaSuccess) return err;                                                           \
     return launch_pdl(gather_shrink_kernel<N>, grid, dim3(kShrinkThreads), smem, s, p);           \
   }
-  switch (NT) {
+  switch (p.U != nullptr ? NT : 0) {  // no U: the gather alone
     MOE_SHRINK_CASE(0) MOE_SHRINK_CASE(1) MOE_SHRINK_CASE(2) MOE_SHRINK_CASE(3)
     MOE_SHRINK_CASE(4) MOE_SHRINK_CASE(5) MOE_SHRINK_CASE(6) MOE_SHRINK_CASE(7)
     MOE_SHRINK_CASE(8) MOE_SHRINK_CASE(9) MOE_SHRINK_CASE(10) MOE_SHRINK_CASE(11)

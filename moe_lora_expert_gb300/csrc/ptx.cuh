@@ -130,6 +130,28 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders this thread's earlier generic-proxy writes to global memory before
+// later async-proxy (TMA) reads of it, and, on the reading side, an acquire
+// before the TMA reads that depend on it.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Flag word in global memory: release store or add (after this thread's and,
+// through a preceding barrier, its CTA's writes) and acquire load, all at GPU
+// scope.
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // Barrier among ``nthreads`` threads (whole warps) of the CTA on named
 // barrier ``id`` (0 is the one __syncthreads uses).
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {

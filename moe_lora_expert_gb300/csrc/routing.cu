@@ -294,8 +294,10 @@ size_t permute_scratch_bytes(int n, int E) {
   const size_t a = (nchunks * E * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
   const size_t b = (static_cast<size_t>(kNumTileWidths) * (E + 1) * sizeof(int32_t) + 255) &
                    ~static_cast<size_t>(255);
-  return a + b + gmask_bytes(n, E);
+  return a + b + gmask_bytes(n, E) + ((2 * shrink_flag_words(n, E) * sizeof(int) + 255) & ~static_cast<size_t>(255));
 }
+
+size_t shrink_flag_words(int n, int E) { return (static_cast<size_t>(n) + 15) / 16 + E + 1; }
 
 size_t gmask_bytes(int n, int E) {
   const size_t tiles16 = (static_cast<size_t>(n) + 15) / 16 + E + 1;
@@ -347,6 +349,7 @@ __global__ void __launch_bounds__(1024) small_permute_kernel(const FusedPermuteP
 
   pdl_wait();
   if (tid == 0) p.status[0] = 0;
+  for (int i = tid; i < p.clear_count; i += blockDim.x) p.clear_flags[i] = 0;
   for (int i = tid; i < 32 * E; i += blockDim.x) s_cnt[i] = 0;
   __syncthreads();
   if (p.logits != nullptr) {

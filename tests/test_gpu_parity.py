@@ -309,6 +309,33 @@ def test_forward_many_rows_row_block_shrink(with_lora):
     assert_output_close(res["out64"][tokens], ref, f"rows lora={with_lora}")
 
 
+@pytest.mark.parametrize("fused", ["1", "0"])
+@pytest.mark.parametrize("name", ["decode_T16", "decode_T64_mixed8", "tiny_T8"])
+def test_forward_shrink_in_gemm_and_separate(name, fused, monkeypatch):
+    """Decode-sized tiles compute the LoRA shrinks inside the expert GEMMs
+    (tile flags between CTAs); MOE_LORA_FUSE_SHRINK=0 keeps the separate
+    shrink kernels.  Both against the oracle."""
+    monkeypatch.setenv("MOE_LORA_FUSE_SHRINK", fused)
+    inp = cached_inputs(name)
+    res = run_gpu(inp)
+    assert res["status"] == 0, res["status_str"]
+    check_routing(res, inp)
+    assert_output_close(res["out64"], oracle.forward_inputs(inp)["out64"], f"{name} fused={fused}")
+
+
+def test_forward_shrink_in_gemm_full_tiles():
+    """Sixteen rows per expert in 16-wide tiles (every tile full, so each
+    CTA's in-kernel shrink walks 16 rows), four adapters and unadapted rows
+    mixed in the tiles, rank 32 (the largest the in-kernel shrink takes)."""
+    wl = workloads.small_workload("fulltiles", T=256, H=320, I=96, E=16, top_k=1, num_adapters=4,
+                                  rank=32, map_lo=-1, map_hi=3, seed=91)
+    inp = workloads.make_inputs(wl)
+    res = run_gpu(inp, tile_n=16)
+    assert res["status"] == 0, res["status_str"]
+    check_routing(res, inp)
+    assert_output_close(res["out64"], oracle.forward_inputs(inp)["out64"], "fulltiles")
+
+
 @pytest.mark.parametrize("rank", [64, 128])
 def test_forward_many_rows_large_rank(rank):
     """The 128-row-tile shrink with ranks above 32 (each thread then copies
