@@ -118,9 +118,9 @@ def auto_tile_n(n_rows, E):
 def kernels_per_forward(wl, fp8=False):
     """Kernels one moe_lora_forward launches (mirrors the library's choices):
     routing (unless fused into the one-CTA permute), the permute (one CTA, or
-    count + scan + scatter), the gather/gate_up shrink, the gate_up GEMM, the
-    down shrink (LoRA, unless it runs inside the down GEMM), the down GEMM
-    and the finalize."""
+    count + scan + scatter), the gather/gate_up shrink and the down shrink
+    (unless both run inside the GEMMs), the gate_up GEMM, the down GEMM and
+    the finalize."""
     n, E = wl.T * wl.top_k, wl.E
     small = n <= 8192 and (((n + 1) & ~1) * 4 + 32 * E * 4 + (E + 1) * 4) <= 200 * 1024
     fuse_route = small and wl.T <= 128
@@ -129,7 +129,7 @@ def kernels_per_forward(wl, fp8=False):
     # so never the row-block shrink), rank <= 32, per-expert gate_up A factors
     fuse_shrink = (lora and not fp8 and small and auto_tile_n(n, E) == 16 and wl.rank <= 32
                    and not wl.shared_outer)
-    return ((0 if fuse_route else 1) + (1 if small else 3) + 1 + 1 +
+    return ((0 if fuse_route else 1) + (1 if small else 3) + (0 if fuse_shrink else 1) + 1 +
             (1 if lora and not fuse_shrink else 0) + 1 + 1)
 
 

@@ -442,10 +442,10 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   bool row_blocks = n_local > 16 * static_cast<int64_t>(sms) ||
                     (r >= 64 && n_local >= 8 * std::min<int64_t>(E, n_local));
   if (const char* env = std::getenv("MOE_LORA_SHRINK_ROWS")) row_blocks = std::atoi(env) != 0;  // tuning
-  // Decode-sized tiles: the LoRA shrinks run inside the expert GEMMs (their
-  // epilogue warps are idle until the first accumulator is ready), so no
-  // shrink kernel sits between the GEMMs; the gate_up shrink kernel only
-  // gathers the rows.  Needs the one-CTA permute (it clears the tile flags),
+  // Decode-sized tiles: the row gather and the LoRA shrinks run inside the
+  // expert GEMMs (their epilogue warps are idle until the first accumulator
+  // is ready), so no kernel sits between the permute and the gate_up GEMM or
+  // between the GEMMs.  Needs the one-CTA permute (it clears the tile flags),
   // one CTA per 16-wide tile, rank <= 32 and per-expert gate_up A factors.
   // MOE_LORA_FUSE_SHRINK=0 turns it off (tuning).
   bool fuse_shrink = lora && !w8 && small_permute && bn == 16 && cl == 1 && !pair && r <= 32 &&
@@ -508,7 +508,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   fp.status = status;
   // Per 16-row tile, the adapters of its GEMM tile: lets the 16-row shrink
   // skip (tile, adapter) pairs without work.
-  fp.gmask = (lora && small_permute) ? gmask : nullptr;
+  fp.gmask = (lora && small_permute && !fuse_shrink) ? gmask : nullptr;
   fp.gemm_bn = bn;
   fp.clear_flags = fuse_shrink ? flags_gu : nullptr;
   fp.clear_count = fuse_shrink ? static_cast<int>(2 * moe::shrink_flag_words(static_cast<int>(n), E)) : 0;
@@ -575,9 +575,10 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   sp.mapping = lora ? a->token_lora_mapping : nullptr;
   sp.tile_start_rows = tile_start + moe::tile_width_index(moe::rows_shrink_tile()) * (E + 1);
   sp.gmask = fp.gmask;
-  if ((row_blocks && !sp.per_token ? moe::launch_rows_shrink(sp, static_cast<int>(n), stream)
+  if (!fuse_shrink &&  // fused: the gate_up GEMM gathers the rows itself
+      (row_blocks && !sp.per_token ? moe::launch_rows_shrink(sp, static_cast<int>(n), stream)
                                    : moe::launch_gather_shrink(sp, static_cast<int>(n), stream)) !=
-      cudaSuccess)
+          cudaSuccess)
     return MOE_ERR_CUDA;
   if (!mark()) return MOE_ERR_CUDA;
   // 4. gate_up GEMM + LoRA expand + SwiGLU -> h
@@ -599,13 +600,18 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.out = h;
   gp.status = status;
   gp.timeout_ns = timeout_ns;
-  gp.tables_ready = 1;  // launched right after the gate_up shrink (n > 0 here)
+  // Launched right after the gate_up shrink (n > 0 here), or (fused) right
+  // after the permute, whose tables may still be in flight.
+  gp.tables_ready = fuse_shrink ? 0 : 1;
   gp.w_scale = w8 ? a->w13_scale : nullptr;
   gp.scale_nb = (2 * I + 127) / 128;
   gp.scale_kb = (H + 127) / 128;
   gp.fuse_shrink = fuse_shrink ? 1 : 0;
   if (fuse_shrink) {
     gp.sx = xp;
+    gp.gather_src = static_cast<const __nv_bfloat16*>(a->hidden);
+    gp.gather_map = p2e;
+    gp.gather_div = K;
     gp.sa = static_cast<const __nv_bfloat16*>(a->gate_up.A);
     gp.sa_stride_adapter = a->gate_up.a_stride_adapter;
     gp.sa_stride_expert = a->gate_up.a_stride_expert;
@@ -649,6 +655,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.tables_ready = lora ? 1 : 0;
   if (fuse_shrink) {
     gp.sx = h;
+    gp.gather_src = nullptr;
     gp.sa = static_cast<const __nv_bfloat16*>(a->down.A);
     gp.sa_stride_adapter = a->down.a_stride_adapter;
     gp.sa_stride_expert = a->down.a_stride_expert;

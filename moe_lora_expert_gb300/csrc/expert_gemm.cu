@@ -179,7 +179,9 @@ __device__ __forceinline__ void raise_timeout_at(int* status, volatile int* abor
 // and across the four warps in shared memory (s_red, 4 x 32 floats).  Each
 // finished row adds one to the flag of its token tile (release, after a
 // proxy fence that makes the row visible to other CTAs' TMA reads); a tile
-// is complete when its flag equals its row count.
+// is complete when its flag equals its row count.  With p.gather_src the
+// pass first copies the row's token vector from gather_src (the hidden row
+// of its slot) into sx, so the gather needs no kernel of its own.
 template <int BN>
 __device__ void shrink_rows_in_gemm(const GemmParams& p, const int* s_off, const int* s_ts, int ew,
                                     int lane, float* s_red) {
@@ -197,18 +199,24 @@ __device__ void shrink_rows_in_gemm(const GemmParams& p, const int* s_off, const
     const int tile = s_ts[e] + (prow - s_off[e]) / BN;
     const int a = __ldcg(p.row_adapter + prow);
     __nv_bfloat16* urow = p.su + static_cast<size_t>(prow) * ld;
+    const __nv_bfloat16* x = p.sx + static_cast<size_t>(prow) * K;
+    if (p.gather_src != nullptr) {
+      x = p.gather_src + static_cast<size_t>(__ldcg(p.gather_map + prow) / p.gather_div) * K;
+      __nv_bfloat16* dst = const_cast<__nv_bfloat16*>(p.sx) + static_cast<size_t>(prow) * K;
+      for (int k = tid * 8; k < K; k += 128 * 8)
+        *reinterpret_cast<uint4*>(dst + k) = __ldg(reinterpret_cast<const uint4*>(x + k));
+    }
     // the other adapters' columns: zero (8 columns per store)
     for (int c = tid * 8; c < ld; c += 128 * 8)
       if (a < 0 || c / R != a) *reinterpret_cast<uint4*>(urow + c) = make_uint4(0, 0, 0, 0);
     if (a >= 0) {  // uniform over the CTA
-      const __nv_bfloat16* x = p.sx + static_cast<size_t>(prow) * K;
       const __nv_bfloat16* A = p.sa + a * p.sa_stride_adapter + static_cast<int64_t>(e) * p.sa_stride_expert;
       for (int i0 = 0; i0 < R; i0 += 8) {
         float acc[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) acc[q] = 0.f;
         for (int k = tid * 8; k < K; k += 128 * 8) {
-          const uint4 xv = __ldcg(reinterpret_cast<const uint4*>(x + k));
+          const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + k));
           const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xv);
           float xf[8];
 #pragma unroll
@@ -553,9 +561,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
             amask &= amask - 1;
           }
         }
-        if (lane == 0 && p.fuse_shrink && b == nk) {
-          // the tile's LoRA rows come from the in-kernel shrink of other
-          // CTAs (or this one): wait until all of them are published
+        if (lane == 0 && p.fuse_shrink && b == (p.gather_src != nullptr ? 0 : nk)) {
+          // the tile's LoRA rows (and, gathering, its token rows) come from
+          // the in-kernel pass of other CTAs (or this one): wait until all
+          // of them are published
           const int* flag = p.tile_flags + w / FBg;
           const uint64_t t0 = global_timer_ns();
           while (ld_acquire_gpu(flag) < wk.nrows) {

@@ -193,6 +193,12 @@ struct GemmParams {
   // the permute of the same forward.
   int fuse_shrink;
   const __nv_bfloat16* sx;             // [n, K]: the token rows (xp or h)
+  // Or also gather them: sx row p = gather_src row gather_map[p] / gather_div
+  // (hidden rows by slot), written by the same in-kernel pass; the producer
+  // then waits for a tile's flag before the tile's first K block.
+  const __nv_bfloat16* gather_src;
+  const int32_t* gather_map;
+  int gather_div;
   const __nv_bfloat16* sa;             // A factors, rows of K elements
   int64_t sa_stride_adapter;           // elements between adapters
   int64_t sa_stride_expert;            // elements between experts
