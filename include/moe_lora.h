@@ -285,6 +285,12 @@ typedef struct {
  * the kernel then reports MOE_ERR_DEVICE_TIMEOUT, drains its own copies and
  * MMAs, frees its tensor memory and exits (the output is then garbage). */
 #define MOE_DEBUG_STALL_GATE_UP_MMA 1u
+/* Test-only flag: when the LoRA shrink runs inside the gate_up GEMM
+ * (decode-sized tiles), the row flag of permuted row 0 is never raised, so
+ * the wait for that row's token tile runs out after wait_timeout_ms with
+ * MOE_ERR_DEVICE_TIMEOUT (the output is then garbage).  Without that mode
+ * the flag has no effect. */
+#define MOE_DEBUG_HOLD_SHRINK_ROW 2u
 
 /* Byte offsets of the intermediates inside the workspace (for inspection). */
 typedef struct {

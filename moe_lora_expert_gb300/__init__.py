@@ -33,6 +33,7 @@ MOE_NUM_STAGE_EVENTS = 8
 MOE_WEIGHTS_BF16 = 0
 MOE_WEIGHTS_FP8_E4M3_B128 = 1
 MOE_DEBUG_STALL_GATE_UP_MMA = 1
+MOE_DEBUG_HOLD_SHRINK_ROW = 2
 STAGE_NAMES = ["route", "permute", "shrink_gate_up", "gemm_gate_up", "shrink_down", "gemm_down",
                "finalize"]
 

@@ -591,6 +591,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.rows_per_expert = 2 * I;
   gp.gu_single_box = gu_single_box ? 1 : 0;
   gp.debug_stall_mma = (a->debug_flags & MOE_DEBUG_STALL_GATE_UP_MMA) ? 1 : 0;
+  gp.debug_hold_row = (a->debug_flags & MOE_DEBUG_HOLD_SHRINK_ROW) ? 1 : 0;
   gp.n_feat = I;
   gp.feat_blocks = (I + 63) / 64;
   gp.num_adapters = A;
@@ -647,6 +648,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.n_feat = H;
   gp.feat_blocks = (H + 127) / 128;
   gp.debug_stall_mma = 0;
+  gp.debug_hold_row = 0;
   gp.lb_row_stride_adapter = dn_rs_a;
   gp.lb_row_stride_expert = dn_rs_e;
   gp.out = y;

@@ -254,7 +254,7 @@ __device__ void shrink_rows_in_gemm(const GemmParams& p, const int* s_off, const
     }
     fence_proxy_async_global();
     named_barrier_sync(1, 128);  // the row is written; s_red is free again
-    if (tid == 0) {
+    if (tid == 0 && !(p.debug_hold_row && prow == 0)) {
       __threadfence();
       red_release_gpu_add(p.tile_flags + tile, 1);
     }

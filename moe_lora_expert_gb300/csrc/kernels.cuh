@@ -165,6 +165,7 @@ struct GemmParams {
   int rows_per_expert;            // rows of the weight per expert (2I or H)
   int gu_single_box;              // gate_up weight map is the 5-D one-box view
   int debug_stall_mma;            // test only: MMA role first waits on a barrier nobody signals
+  int debug_hold_row;             // test only: the in-kernel shrink never counts permuted row 0
   int n_feat;                     // output features (I for gate_up, H for down)
   int feat_blocks;                // feature blocks per expert
   int num_adapters;               // 0 = no LoRA

@@ -399,6 +399,25 @@ def test_device_wait_timeout_is_reported_and_recoverable():
     assert_output_close(to_f64(out), oracle.forward_inputs(inp)["out64"], "after timeout")
 
 
+def test_shrink_flag_wait_timeout_is_reported_and_recoverable():
+    """The in-GEMM shrink's tile flags: with permuted row 0 never counted
+    (test flag), the wait for its tile runs out and reports
+    MOE_ERR_DEVICE_TIMEOUT; the kernels drain and exit, and the next call on
+    the same workspace (the permute clears the flags) is correct."""
+    import moe_lora_expert_gb300 as m
+    torch = torch_mod()
+    inp = cached_inputs("decode_T16")
+    layer = make_layer(inp)
+    hid = bf16_tensor(inp.hidden)
+    lg = torch.from_numpy(inp.logits).to(dev())
+    mp = torch.from_numpy(inp.mapping).to(dev())
+    layer.forward(hid, lg, mp, wait_timeout_ms=20, debug_flags=m.MOE_DEBUG_HOLD_SHRINK_ROW)
+    assert layer.device_status() == m.MOE_ERR_DEVICE_TIMEOUT
+    out = layer.forward(hid, lg, mp)
+    assert layer.device_status() == m.MOE_OK
+    assert_output_close(to_f64(out), oracle.forward_inputs(inp)["out64"], "after flag timeout")
+
+
 @pytest.mark.parametrize("shape", ["small", "decode_T16"])
 def test_peft_adapters_separate_gate_up_mixed_ranks_and_scales(shape):
     """Separate gate/up pairs, per-adapter ranks and scales, packed into the
