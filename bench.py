@@ -100,6 +100,13 @@ def algorithmic_work(wl, ids, mapping, fp8=False):
         "bytes": len(experts) * w2_b + dn_B + n * I * 2 + n_ad * r * 2 + n * H * 2,
         "flops": n * 2 * H * I + n_ad * 2 * H * r,
     }
+    if shrink_in_gemm(wl, fp8):
+        # the GEMMs also gather the rows (gate_up: hidden in, permuted rows
+        # out) and run the LoRA shrinks (A factors in)
+        work["gemm_gate_up"]["bytes"] += gu_A + T * H * 2 + n * H * 2
+        work["gemm_gate_up"]["flops"] += n_ad * 2 * r * H
+        work["gemm_down"]["bytes"] += dn_A
+        work["gemm_down"]["flops"] += n_ad * 2 * r * I
     return work
 
 
@@ -115,6 +122,18 @@ def auto_tile_n(n_rows, E):
     return bn
 
 
+def shrink_in_gemm(wl, fp8=False):
+    """Whether the library runs the row gather and the LoRA shrinks inside
+    the expert GEMMs (api.cu: 16-wide tiles, so at most four rows per expert
+    on average and never the row-block shrink; rank <= 32; per-expert gate_up
+    A factors; the one-CTA permute; bf16 weights)."""
+    n, E = wl.T * wl.top_k, wl.E
+    small = n <= 8192 and (((n + 1) & ~1) * 4 + 32 * E * 4 + (E + 1) * 4) <= 200 * 1024
+    lora = wl.num_adapters > 0 and wl.rank > 0
+    return (lora and not fp8 and small and auto_tile_n(n, E) == 16 and wl.rank <= 32
+            and not wl.shared_outer)
+
+
 def kernels_per_forward(wl, fp8=False):
     """Kernels one moe_lora_forward launches (mirrors the library's choices):
     routing (unless fused into the one-CTA permute), the permute (one CTA, or
@@ -125,10 +144,7 @@ def kernels_per_forward(wl, fp8=False):
     small = n <= 8192 and (((n + 1) & ~1) * 4 + 32 * E * 4 + (E + 1) * 4) <= 200 * 1024
     fuse_route = small and wl.T <= 128
     lora = wl.num_adapters > 0 and wl.rank > 0
-    # in-GEMM shrinks: 16-wide tiles (at most four rows per expert on average,
-    # so never the row-block shrink), rank <= 32, per-expert gate_up A factors
-    fuse_shrink = (lora and not fp8 and small and auto_tile_n(n, E) == 16 and wl.rank <= 32
-                   and not wl.shared_outer)
+    fuse_shrink = shrink_in_gemm(wl, fp8)
     return ((0 if fuse_route else 1) + (1 if small else 3) + (0 if fuse_shrink else 1) + 1 +
             (1 if lora and not fuse_shrink else 0) + 1 + 1)
 
