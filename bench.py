@@ -126,12 +126,11 @@ def shrink_in_gemm(wl, fp8=False):
     """Whether the library runs the row gather and the LoRA shrinks inside
     the expert GEMMs (api.cu: 16-wide tiles, so at most four rows per expert
     on average and never the row-block shrink; rank <= 32; per-expert gate_up
-    A factors; the one-CTA permute; bf16 weights)."""
+    A factors; the one-CTA permute; bf16 or FP8 weights alike)."""
     n, E = wl.T * wl.top_k, wl.E
     small = n <= 8192 and (((n + 1) & ~1) * 4 + 32 * E * 4 + (E + 1) * 4) <= 200 * 1024
     lora = wl.num_adapters > 0 and wl.rank > 0
-    return (lora and not fp8 and small and auto_tile_n(n, E) == 16 and wl.rank <= 32
-            and not wl.shared_outer)
+    return lora and small and auto_tile_n(n, E) == 16 and wl.rank <= 32 and not wl.shared_outer
 
 
 def kernels_per_forward(wl, fp8=False):

@@ -448,7 +448,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   // between the GEMMs.  Needs the one-CTA permute (it clears the tile flags),
   // one CTA per 16-wide tile, rank <= 32 and per-expert gate_up A factors.
   // MOE_LORA_FUSE_SHRINK=0 turns it off (tuning).
-  bool fuse_shrink = lora && !w8 && small_permute && bn == 16 && cl == 1 && !pair && r <= 32 &&
+  bool fuse_shrink = lora && small_permute && bn == 16 && cl == 1 && !pair && r <= 32 &&
                      !row_blocks && a->gate_up.a_stride_expert != 0;
   if (const char* env = std::getenv("MOE_LORA_FUSE_SHRINK")) fuse_shrink = fuse_shrink && std::atoi(env) != 0;
   const uint64_t timeout_ns =

@@ -261,6 +261,17 @@ __device__ void shrink_rows_in_gemm(const GemmParams& p, const int* s_off, const
   }
 }
 
+// Bounded wait until ``count`` rows of a token tile are published by the
+// in-kernel pass; then a proxy fence orders the TMA reads of them after it.
+__device__ __forceinline__ bool wait_tile_rows(const int* flag, int count, uint64_t limit_ns,
+                                               volatile int* abort_flag) {
+  const uint64_t t0 = global_timer_ns();
+  while (ld_acquire_gpu(flag) < count)
+    if (*abort_flag || global_timer_ns() - t0 > limit_ns) return false;
+  fence_proxy_async_global();
+  return true;
+}
+
 // Weight-side (A operand) loads of one K block: 128 rows of the feature block.
 // gate_up: the map views w13 so that one box (or four, see the host code)
 // brings gate rows 64 fb + 16q + (0..15) to smem rows 32q + (0..15) and the
@@ -466,7 +477,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
           adapter = __ffsll(static_cast<long long>(amask)) - 1;
           amask &= amask - 1;
         }
-        if (lane == 0) {
+        if (lane == 0 && p.fuse_shrink && b == (p.gather_src != nullptr ? 0 : nk)) {
+          // the tile's token / LoRA rows come from the in-kernel pass
+          ok = wait_tile_rows(p.tile_flags + w / FBg, wk.nrows, p.timeout_ns, abort_flag);
+          if (!ok && !*abort_flag) raise_timeout_at(p.status, abort_flag, kWaitShrinkFlag, w, b, s8);
+        }
+        if (lane == 0 && ok) {
           ok = wait_or_abort(&empty8[s8], ph8 ^ 1, p.timeout_ns, abort_flag);
           if (ok) {
             uint8_t* st = w8ring + s8 * C::kW8Stage;
@@ -565,16 +581,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
           // the tile's LoRA rows (and, gathering, its token rows) come from
           // the in-kernel pass of other CTAs (or this one): wait until all
           // of them are published
-          const int* flag = p.tile_flags + w / FBg;
-          const uint64_t t0 = global_timer_ns();
-          while (ld_acquire_gpu(flag) < wk.nrows) {
-            if (*abort_flag || global_timer_ns() - t0 > p.timeout_ns) {
-              ok = false;
-              break;
-            }
-          }
-          if (ok) fence_proxy_async_global();
-          else if (!*abort_flag) raise_timeout_at(p.status, abort_flag, kWaitShrinkFlag, w, b, stage);
+          ok = wait_tile_rows(p.tile_flags + w / FBg, wk.nrows, p.timeout_ns, abort_flag);
+          if (!ok && !*abort_flag) raise_timeout_at(p.status, abort_flag, kWaitShrinkFlag, w, b, stage);
         }
         if (lane == 0 && ok) {
           ok = wait_or_abort<PAIR>(&empty[stage], phase ^ 1, p.timeout_ns, abort_flag);
