@@ -302,7 +302,8 @@ typedef struct {
   size_t expanded_to_permuted;/* int32 [T*top_k]                               */
   size_t permuted_to_expanded;/* int32 [T*top_k]                               */
   size_t row_adapter;         /* int32 [T*top_k] adapter of each permuted row  */
-  size_t permute_scratch;     /* counting-sort scratch                         */
+  size_t permute_scratch;     /* counting-sort scratch, tile tables, adapter
+                                 masks, tile flags of the in-GEMM shrink      */
   size_t permuted_hidden;     /* bf16  [T*top_k, H]                            */
   size_t lora_u;              /* bf16  [T*top_k, A*r] s*A_gu x, one-hot slot   */
   size_t act;                 /* bf16  [T*top_k, I]   h = silu(gate)*up        */
