@@ -977,22 +977,8 @@ static cudaError_t launch_one(const CUtensorMap& tm_w, const CUtensorMap& tm_x,
   const int smem = C::kSmemBytes;
   cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
-  if (CL == 1) {
-    if (p.fuse_shrink) {
-      // CTAs wait for rows that other CTAs of the grid publish: the grid
-      // must not exceed what can be resident at once (the work is spread
-      // over gridDim.x, so any grid size is correct).
-      static int occ = -1;
-      if (occ < 0) {
-        int v = 0;
-        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, C::kThreads, smem);
-        if (err != cudaSuccess) return err;
-        occ = v;
-      }
-      grid = std::max(1, std::min(grid, occ * (grid / C::kCtasPerSm)));
-    }
+  if (CL == 1)
     return launch_pdl(kern, dim3(grid), dim3(C::kThreads), smem, s, tm_w, tm_x, tm_lb, tm_lu, p);
-  }
 
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(C::kThreads);
