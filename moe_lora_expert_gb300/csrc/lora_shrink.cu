@@ -297,8 +297,8 @@ cudaError_t launch_gather_shrink(const ShrinkParams& p, int n_rows, cudaStream_t
 // a quarter-warp read rows g, g' of both parities and four chunks each, and
 // land in 8 distinct bank groups.
 // 64-row tiles and four stages: at prefill sizes (tens of thousands of rows)
-// this gives every SM four to five resident CTAs with three chunks in flight
-// each; 128-row tiles with three stages left the SMs latency-bound.
+// this gives every SM four resident CTAs with three chunks in flight each;
+// 128-row tiles with three stages left the SMs latency-bound.
 constexpr int kRowStages = 4;
 constexpr int kRowTile = 64;
 constexpr int kRowThreads = 2 * kRowTile;  // warp w owns compacted rows [16w, 16w + 16)
@@ -306,9 +306,16 @@ constexpr int kRowStride = kRowThreads / 8;  // rows between one thread's copy r
 
 int rows_shrink_tile() { return kRowTile; }
 
+// At least 48 KB of shared memory per CTA, so that no more than four CTAs
+// share an SM: at prefill sizes four per SM measured faster than five
+// (gate_up shrink 40 against 47 us), the fifth adding L2 pressure rather
+// than latency hiding.  The part above the tiles is unused.
+constexpr size_t kRowMinSmem = 48 * 1024;
+
 __host__ __device__ inline size_t rows_shrink_smem_bytes(int rank, int E) {
-  return static_cast<size_t>(kRowStages) * (kRowTile + rank) * 128 +
-         static_cast<size_t>(kRowTile) * rank * 2 + static_cast<size_t>(E + 1) * 4;
+  const size_t need = static_cast<size_t>(kRowStages) * (kRowTile + rank) * 128 +
+                      static_cast<size_t>(kRowTile) * rank * 2 + static_cast<size_t>(E + 1) * 4;
+  return need > kRowMinSmem ? need : kRowMinSmem;
 }
 
 __device__ __forceinline__ int swz16(int row, int j) { return (j ^ ((row & 1) << 2)) * 16; }
