@@ -40,9 +40,13 @@ __host__ __device__ inline size_t shrink_smem_bytes(int kc, int rank) {
          static_cast<size_t>(16) * rank * 2;
 }
 
-template <int NT>  // rank = 8 * NT (NT = 0: gather only)
+// NT = 0: gather only.  Otherwise the CTA computes R = 8 NT columns of the
+// adapter's rank: slice blockIdx.z, columns [R z, R z + R) of p.rank (the
+// per-token mode splits a large rank over several CTAs).
+template <int NT>
 __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const ShrinkParams p) {
   constexpr int R = 8 * NT;
+  const int rs = static_cast<int>(blockIdx.z);  // rank slice
   extern __shared__ int4 shrink_smem[];
   const int KC = p.kc;
   const int pitch = KC + 8;  // elements; 16-byte pad keeps the mma loads conflict-free
@@ -138,7 +142,7 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
   // top_k copies are shared out over the adapter-slot CTAs of the tile
   // (slot j goes to CTA j mod gridDim.y).
   const int gshare = p.per_token ? static_cast<int>(gridDim.y) : 1;
-  const bool do_gather = p.gathered != nullptr && (p.per_token ? ad < p.top_k : ad == 0);
+  const bool do_gather = p.gathered != nullptr && rs == 0 && (p.per_token ? ad < p.top_k : ad == 0);
   const int passes = (present || do_gather) ? 1 : 0;
   const int K = p.K;
   uint32_t parity = 0;
@@ -147,7 +151,9 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
   for (int pass = 0; pass < passes; ++pass) {
     const int a = present ? ad : -1;
     const __nv_bfloat16* Af =
-        a >= 0 ? p.A + a * p.a_stride_adapter + static_cast<int64_t>(e) * p.a_stride_expert : nullptr;
+        a >= 0 ? p.A + a * p.a_stride_adapter + static_cast<int64_t>(e) * p.a_stride_expert +
+                     static_cast<int64_t>(rs) * R * K
+               : nullptr;
     float acc[NT > 0 ? NT : 1][4];
 #pragma unroll
     for (int nt = 0; nt < (NT > 0 ? NT : 1); ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
@@ -234,8 +240,8 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
   pdl_launch_dependents();
 
   if constexpr (NT > 0) {
-   if (p.U != nullptr) {  // this adapter's r columns of every row of the tile
-    const int ld = p.num_adapters * R;
+   if (p.U != nullptr) {  // this adapter's columns (this slice) of every row of the tile
+    const int ld = p.num_adapters * p.rank;
     constexpr int vec_per_row = R / 8;
     const int copies = p.per_token ? p.top_k : 1;  // every permuted row of the token
     for (int v = tid; v < nrows * copies * vec_per_row; v += kShrinkThreads) {
@@ -246,7 +252,7 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
       if (dst < 0) continue;  // slot not routed here
       uint4 val = zero;
       if (s_adapter[row] == ad) val = *reinterpret_cast<const uint4*>(s_u + row * R + c);
-      *reinterpret_cast<uint4*>(p.U + static_cast<size_t>(dst) * ld + ad * R + c) = val;
+      *reinterpret_cast<uint4*>(p.U + static_cast<size_t>(dst) * ld + ad * p.rank + rs * R + c) = val;
     }
    }
   }
@@ -263,10 +269,14 @@ size_t shrink_launch_smem(const ShrinkParams& p) { return shrink_smem_bytes(p.kc
 
 cudaError_t launch_gather_shrink(const ShrinkParams& p, int n_rows, cudaStream_t s) {
   if (n_rows == 0) return cudaSuccess;
-  const int NT = p.rank / 8;
+  // The per-token mode has few tiles (16 tokens each): a rank of 32 or more
+  // is split into 16-column slices, one CTA each, so that more CTAs share
+  // the factor reads.
+  const int slices = (p.per_token && p.U != nullptr && p.rank >= 32 && p.rank % 16 == 0) ? p.rank / 16 : 1;
+  const int NT = p.rank / 8 / slices;
   const int tiles = p.per_token ? (p.T + 15) / 16 : (n_rows + 15) / 16 + (p.E < n_rows ? p.E : n_rows);
-  const dim3 grid(tiles, (NT > 0 && p.U != nullptr) ? p.num_adapters : 1);
-  const size_t smem = shrink_smem_bytes(p.kc, p.U != nullptr ? p.rank : 0);
+  const dim3 grid(tiles, (NT > 0 && p.U != nullptr) ? p.num_adapters : 1, slices);
+  const size_t smem = shrink_smem_bytes(p.kc, p.U != nullptr ? p.rank / slices : 0);
 #define MOE_SHRINK_CASE(N)                                                                        \
   case N: {                                                                                       \
     cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(gather_shrink_kernel<N>), (int)smem); \

@@ -399,6 +399,20 @@ def test_device_wait_timeout_is_reported_and_recoverable():
     assert_output_close(to_f64(out), oracle.forward_inputs(inp)["out64"], "after timeout")
 
 
+@pytest.mark.parametrize("rank", [16, 48, 128])
+def test_forward_shared_outer_rank_slices(rank):
+    """Shared gate_up A factor (per-token shrink): ranks of 32 or more are
+    split into 16-column slices over separate CTAs (3 and 8 slices here);
+    rank 16 stays whole.  Partial K chunks (H=200) and unadapted tokens."""
+    wl = workloads.small_workload("slices", T=40, H=200, I=72, E=6, top_k=3, num_adapters=3,
+                                  rank=rank, map_lo=-1, map_hi=2, shared_outer=True, seed=95)
+    inp = workloads.make_inputs(wl)
+    res = run_gpu(inp)
+    assert res["status"] == 0, res["status_str"]
+    check_routing(res, inp)
+    assert_output_close(res["out64"], oracle.forward_inputs(inp)["out64"], f"slices r={rank}")
+
+
 def test_shrink_flag_wait_timeout_is_reported_and_recoverable():
     """The in-GEMM shrink's tile flags: with permuted row 0 never counted
     (test flag), the wait for its tile runs out and reports
