@@ -6,6 +6,7 @@
 // "[WIP][LoRA] BF16 support for the experimental_sgl_trtllm MoE-LoRA path &
 // lora expert_outer_shared" (yushengsu-thu/sglang#4).
 #include <algorithm>
+#include <atomic>
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -567,19 +568,23 @@ template <int KMAX>
 static cudaError_t launch_finalize_k(const __nv_bfloat16* y, const int32_t* e2p, const float* w,
                                      int T, int top_k, int H, __nv_bfloat16* out, cudaStream_t s) {
   constexpr int kMaxDevices = 64;
-  static int ctas[kMaxDevices] = {};  // resident CTAs of the persistent grid, per device
+  // resident CTAs of the persistent grid, per device (computed once; host
+  // threads may race to fill it with the same value)
+  static std::atomic<int> ctas[kMaxDevices] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (ctas[dev] == 0) {
+  int resident = ctas[dev].load(std::memory_order_relaxed);
+  if (resident == 0) {
     int sms = 0, per_sm = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, finalize_kernel<KMAX>, 256, 0) !=
             cudaSuccess)
       return cudaErrorUnknown;
-    ctas[dev] = std::max(1, sms * per_sm);
+    resident = std::max(1, sms * per_sm);
+    ctas[dev].store(resident, std::memory_order_relaxed);
   }
   const int ycols = (H / 8 + 255) / 256;
-  const int tok_ctas = std::max(1, std::min(T, ctas[dev] / ycols));
+  const int tok_ctas = std::max(1, std::min(T, resident / ycols));
   return launch_pdl(finalize_kernel<KMAX>, dim3(tok_ctas, ycols), dim3(256), 0, s, y, e2p, w, T,
                     top_k, H, out);
 }
