@@ -1,0 +1,71 @@
+"""Host-side accounting in bench.py (no GPU): the default token-tile width,
+the kernels one forward launches, and the algorithmic bytes charged to the
+expert GEMMs.  These mirror choices the library makes in api.cu; the values
+below are worked out by hand from the rules stated there."""
+import pytest
+
+import bench
+import oracle
+import workloads
+
+
+@pytest.mark.parametrize("n_rows,E,bn", [
+    (128, 128, 16),     # decode_T16: one row per expert
+    (512, 128, 16),     # decode_T64: four rows per expert (4 * 4 = 16 stays)
+    (1024, 128, 32),    # eight rows: 2 * 8 = 16, 4 * 8 = 32
+    (2048, 128, 64),    # sixteen rows: 2 * 16 = 32, raised to 64 by 4 * 16
+    (32768, 128, 256),  # prefill: 256 rows per expert
+    (5, 8, 16),         # fewer rows than experts: avg over touched experts = 1
+])
+def test_auto_tile_n(n_rows, E, bn):
+    assert bench.auto_tile_n(n_rows, E) == bn
+
+
+def test_kernel_counts_per_forward():
+    W = workloads.WORKLOADS
+    # decode: permute (routing fused) + two GEMMs (gather and shrinks inside) + finalize
+    assert bench.kernels_per_forward(W["decode_T16"]) == 4
+    assert bench.kernels_per_forward(W["decode_T64_mixed8"]) == 4
+    assert bench.kernels_per_forward(W["decode_T16"], fp8=True) == 4
+    # shared-outer rank 64: routing, permute, gather+shrink, GEMM, shrink, GEMM, finalize
+    assert bench.kernels_per_forward(W["skewed_T256_shared_outer_r64"]) == 7
+    # prefill: routing, count + scan + scatter, row shrink, GEMM, row shrink, GEMM, finalize
+    assert bench.kernels_per_forward(W["prefill_T4096"]) == 9
+
+
+def test_shrink_in_gemm_conditions():
+    W = workloads.WORKLOADS
+    assert bench.shrink_in_gemm(W["decode_T16"])
+    assert not bench.shrink_in_gemm(W["skewed_T256_shared_outer_r64"])   # shared gate_up A, rank 64
+    assert not bench.shrink_in_gemm(W["prefill_T4096"])                  # 256-wide tiles
+    big_rank = workloads.small_workload("r64", T=16, H=256, I=128, E=128, top_k=8, num_adapters=2,
+                                        rank=64)
+    assert not bench.shrink_in_gemm(big_rank)
+    no_lora = workloads.small_workload("plain", T=16, H=256, I=128, E=128, top_k=8, num_adapters=0,
+                                       rank=0)
+    assert not bench.shrink_in_gemm(no_lora)
+
+
+def test_gemm_bytes_charge_the_in_gemm_shrink():
+    """With the gather and shrinks inside the GEMMs, the gate_up kernel is
+    charged the A factors, the hidden rows read and the permuted rows
+    written; the down kernel the down A factors.  The sums are rebuilt here
+    term by term from the routing of the seeded inputs."""
+    wl = workloads.WORKLOADS["decode_T16"]
+    inp = workloads.make_inputs(wl)
+    ids, _ = oracle.route_topk(inp.logits, wl.top_k)
+    work = bench.algorithmic_work(wl, ids, inp.mapping)
+    T, H, I, E, k, r = wl.T, wl.H, wl.I, wl.E, wl.top_k, wl.rank
+    n = T * k
+    experts = len(set(int(e) for e in ids.ravel()))
+    adapted = [(t, int(inp.mapping[t])) for t in range(T) if inp.mapping[t] >= 0]
+    pairs = len({(a, int(e)) for t, a in adapted for e in ids[t]})
+    n_ad = len(adapted) * k
+    gu = experts * 2 * I * H * 2 + pairs * 2 * I * r * 2 + n * H * 2 + n_ad * r * 2 + n * I * 2
+    gu += pairs * r * H * 2 + T * H * 2 + n * H * 2
+    dn = experts * H * I * 2 + pairs * H * r * 2 + n * I * 2 + n_ad * r * 2 + n * H * 2
+    dn += pairs * r * I * 2
+    assert work["gemm_gate_up"]["bytes"] == gu
+    assert work["gemm_down"]["bytes"] == dn
+    assert work["gemm_gate_up"]["flops"] == n * 2 * 2 * I * H + n_ad * 2 * 2 * I * r + n_ad * 2 * r * H
+    assert work["gemm_down"]["flops"] == n * 2 * H * I + n_ad * 2 * H * r + n_ad * 2 * r * I
