@@ -44,6 +44,12 @@ def parse_args():
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--weights", choices=["bf16", "fp8"], default="bf16",
                     help="expert weight format (fp8: e4m3 with 128x128 block scales)")
+    ap.add_argument("--only-workload", action="store_true",
+                    help="measure --workload alone (default: also the metric's other batch shapes)")
+    ap.add_argument("--shrink-in-gemm", choices=["auto", "off"], default="auto",
+                    help="off: separate gather/shrink kernels (A/B of the in-GEMM shrink)")
+    ap.add_argument("--side-stream", action="store_true",
+                    help="two-stream schedule: gate_up LoRA shrink on a side stream")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help=argparse.SUPPRESS)
@@ -54,7 +60,7 @@ def parse_args():
 # Algorithmic work of one forward (from the actual routing of the inputs)
 # ---------------------------------------------------------------------------
 
-def algorithmic_work(wl, ids, mapping, fp8=False):
+def algorithmic_work(wl, ids, mapping, fp8=False, in_gemm_allowed=True):
     """Bytes and FLOPs the forward must move / compute, intermediates excluded.
 
     Bytes: every touched expert's w13 and w2 once (fp8: one byte per weight
@@ -63,8 +69,12 @@ def algorithmic_work(wl, ids, mapping, fp8=False):
     router logits and the mapping.  FLOPs: 2 per multiply-add of the two expert
     GEMMs for every (token, slot) and of the four LoRA products for adapted
     slots (the shared gate_up shrink once per token).
+
+    Per expert GEMM the same rule: the weights and LoRA factors it reads, plus
+    the layer input where it reads that itself (the row gather inside the
+    gate_up GEMM); the permuted rows, the LoRA operands, the activation and
+    the expert outputs are intermediates and are not charged.
     """
-    import numpy as np
     T, H, I, E, k, A, r = wl.T, wl.H, wl.I, wl.E, wl.top_k, wl.num_adapters, wl.rank
     n = T * k
     experts = sorted(set(int(e) for e in ids.ravel()))
@@ -91,19 +101,18 @@ def algorithmic_work(wl, ids, mapping, fp8=False):
         "bytes": len(experts) * (w13_b + w2_b) + gu_A + gu_B + dn_A + dn_B + io,
         "flops": flops_gemm + flops_lora,
     }
-    # per-kernel figures for the two expert GEMMs
     work["gemm_gate_up"] = {
-        "bytes": len(experts) * w13_b + gu_B + n * H * 2 + n_ad * r * 2 + n * I * 2,
+        "bytes": len(experts) * w13_b + gu_B,
         "flops": n * 2 * 2 * I * H + n_ad * 2 * 2 * I * r,
     }
     work["gemm_down"] = {
-        "bytes": len(experts) * w2_b + dn_B + n * I * 2 + n_ad * r * 2 + n * H * 2,
+        "bytes": len(experts) * w2_b + dn_B,
         "flops": n * 2 * H * I + n_ad * 2 * H * r,
     }
-    if shrink_in_gemm(wl, fp8):
-        # the GEMMs also gather the rows (gate_up: hidden in, permuted rows
-        # out) and run the LoRA shrinks (A factors in)
-        work["gemm_gate_up"]["bytes"] += gu_A + T * H * 2 + n * H * 2
+    if shrink_in_gemm(wl, fp8, in_gemm_allowed):
+        # the GEMMs also gather the rows (gate_up: the hidden input) and run
+        # the LoRA shrinks (A factors)
+        work["gemm_gate_up"]["bytes"] += gu_A + T * H * 2
         work["gemm_gate_up"]["flops"] += n_ad * 2 * r * H
         work["gemm_down"]["bytes"] += dn_A
         work["gemm_down"]["flops"] += n_ad * 2 * r * I
@@ -122,7 +131,7 @@ def auto_tile_n(n_rows, E):
     return bn
 
 
-def shrink_in_gemm(wl, fp8=False):
+def shrink_in_gemm(wl, fp8=False, allowed=True):
     """Whether the library runs the row gather and the LoRA shrinks inside
     the expert GEMMs (api.cu: 16-wide tiles, so at most four rows per expert
     on average and never the row-block shrink; rank <= 32; per-expert gate_up
@@ -130,22 +139,25 @@ def shrink_in_gemm(wl, fp8=False):
     n, E = wl.T * wl.top_k, wl.E
     small = n <= 8192 and (((n + 1) & ~1) * 4 + 32 * E * 4 + (E + 1) * 4) <= 200 * 1024
     lora = wl.num_adapters > 0 and wl.rank > 0
-    return lora and small and auto_tile_n(n, E) == 16 and wl.rank <= 32 and not wl.shared_outer
+    return (allowed and lora and small and auto_tile_n(n, E) == 16 and wl.rank <= 32 and
+            not wl.shared_outer)
 
 
-def kernels_per_forward(wl, fp8=False):
+def kernels_per_forward(wl, fp8=False, in_gemm_allowed=True, two_streams=False):
     """Kernels one moe_lora_forward launches (mirrors the library's choices):
     routing (unless fused into the one-CTA permute), the permute (one CTA, or
     count + scan + scatter), the gather/gate_up shrink and the down shrink
-    (unless both run inside the GEMMs), the gate_up GEMM, the down GEMM and
+    (unless both run inside the GEMMs; the two-stream schedule splits the
+    first into a gather and a shrink), the gate_up GEMM, the down GEMM and
     the finalize."""
     n, E = wl.T * wl.top_k, wl.E
     small = n <= 8192 and (((n + 1) & ~1) * 4 + 32 * E * 4 + (E + 1) * 4) <= 200 * 1024
     fuse_route = small and wl.T <= 128
     lora = wl.num_adapters > 0 and wl.rank > 0
-    fuse_shrink = shrink_in_gemm(wl, fp8)
-    return ((0 if fuse_route else 1) + (1 if small else 3) + (0 if fuse_shrink else 1) + 1 +
-            (1 if lora and not fuse_shrink else 0) + 1 + 1)
+    two = two_streams and lora
+    fuse_shrink = shrink_in_gemm(wl, fp8, in_gemm_allowed and not two)
+    return ((0 if fuse_route else 1) + (1 if small else 3) + (0 if fuse_shrink else 1) +
+            (1 if two else 0) + 1 + (1 if lora and not fuse_shrink else 0) + 1 + 1)
 
 
 def max_over_ranks(value_ms, dist=None, device=None):
@@ -235,7 +247,8 @@ def run_cpu_baseline(workload, seconds):
     if res.returncode != 0:
         return {"error": res.stderr.strip().splitlines()[-1:] or ["failed"]}
     d = json.loads(res.stdout.strip().splitlines()[-1])
-    return {"value": d["value"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+    return {"value": d["value"], "unit": "tokens/s", "cores": 1, "host_cores": os.cpu_count(),
+            "kind": "oracle",
             "sample": (f"{d['tokens']} tokens of {workload} in {d['calls']} oracle calls of 4 tokens "
                        f"({d['seconds']:.1f} s, float64 numpy, 1 BLAS thread)")}
 
@@ -245,67 +258,243 @@ def run_cpu_baseline(workload, seconds):
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
+    """nvidia-smi clocks polled every ``period_ms`` from before the first warm-up
+    to after the last pass, each sample stamped with the host clock so that
+    the samples inside a given window (the timed region) can be picked out."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, index):
+    def __init__(self, index, period_ms=50):
         self.index = index
+        self.period_ms = period_ms
         self.proc = None
+        self.samples = []   # (host time, sm MHz, max MHz, power W, reasons)
+        self._thread = None
 
     def start(self):
+        import threading
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
         except Exception:
             self.proc = None
+            return
+        self._thread = threading.Thread(target=self._read, daemon=True)
+        self._thread.start()
 
-    def stop(self):
-        if self.proc is None:
-            return {"samples": 0}
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except Exception:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
-            parts = [p.strip() for p in line.split(",")]
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
             if len(parts) < 8:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                sm, mx = float(parts[0]), float(parts[1])
             except ValueError:
                 continue
-            for nm, val in zip(names, parts[4:8]):
-                if val.lower().startswith("active"):
-                    reasons.add(nm)
-        if not sm:
+            try:
+                pw = float(parts[2])
+            except ValueError:
+                pw = None
+            reasons = {nm for nm, v in zip(self.NAMES, parts[4:8]) if v.lower().startswith("active")}
+            self.samples.append((time.perf_counter(), sm, mx, pw, reasons))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
+
+    @staticmethod
+    def summary(samples):
+        if not samples:
             return {"samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        sm = [x[1] for x in samples]
+        pw = [x[3] for x in samples if x[3] is not None]
+        reasons = set().union(*[x[4] for x in samples])
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(x[2] for x in samples),
+                "sm_mhz_min": min(sm), "power_w_max": max(pw) if pw else None,
+                "reasons": sorted(reasons), "samples": len(samples)}
+
+    def window(self, t0, t1):
+        return [x for x in self.samples if t0 <= x[0] <= t1]
 
 
 # ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
 
+# The metric's three batch shapes: T=16 (the headline), T=64 and T=4096.
+METRIC_WORKLOADS = ["decode_T16", "decode_T64_mixed8", "prefill_T4096"]
+
+
+def workload_config(wl, args, world):
+    """The ``config`` object of both arms' JSON lines for workload ``wl``."""
+    return {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
+            "top_k": wl.top_k, "num_adapters": wl.num_adapters, "rank": wl.rank,
+            "lora_scaling": wl.scaling, "shared_outer": wl.shared_outer,
+            "tile_n": args.tile_n or "auto", "weights": args.weights,
+            "l2": "GPU arm: flushed before every step (256 MiB write, outside the step events)",
+            "parallelism": "replicas" if world > 1 else "single"}
+
+
+def tuning_from_args(args):
+    t = {}
+    if args.shrink_in_gemm == "off":
+        t["shrink_in_gemm"] = 1
+    return t or None
+
+
+class Layer:
+    """One workload's layer on the GPU: weights, inputs, output buffers."""
+
+    def __init__(self, name, args, dev):
+        import numpy as np
+        import torch
+
+        import moe_lora_expert_gb300 as m
+        import workloads
+        self.wl = wl = workloads.WORKLOADS[name]
+        self.inp = inp = workloads.make_inputs(wl)
+
+        def bf16(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+        self.lora = inp.A_gu is not None
+        self.fp8 = args.weights == "fp8"
+        if self.fp8:
+            q13, s13, q2, s2 = workloads.fp8_weights(inp)
+            w13_d, w2_d = torch.from_numpy(q13).to(dev), torch.from_numpy(q2).to(dev)
+            scales = dict(w13_scale=torch.from_numpy(s13).to(dev), w2_scale=torch.from_numpy(s2).to(dev))
+        else:
+            w13_d, w2_d, scales = bf16(inp.w13), bf16(inp.w2), {}
+        lora = self.lora
+        self.layer = m.MoeLoraLayer(w13_d, w2_d, wl.top_k,
+                                    bf16(inp.A_gu) if lora else None, bf16(inp.B_gu) if lora else None,
+                                    bf16(inp.A_dn) if lora else None, bf16(inp.B_dn) if lora else None,
+                                    scaling=wl.scaling, max_tokens=wl.T, **scales)
+        self.hidden = bf16(inp.hidden)
+        self.logits = torch.from_numpy(inp.logits).to(dev)
+        self.mapping = torch.from_numpy(inp.mapping).to(dev) if lora else None
+        self.out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
+        self.ids = torch.empty((wl.T, wl.top_k), dtype=torch.int32, device=dev)
+        self.tile_n = args.tile_n
+        self.tuning = tuning_from_args(args)
+        self.side = None
+        self.in_gemm_allowed = args.shrink_in_gemm != "off" and not args.side_stream
+        if args.side_stream:
+            self.side = (torch.cuda.Stream(device=dev), [torch.cuda.Event(), torch.cuda.Event()])
+
+    def step(self, evs=None, hidden=None, logits=None, mapping=None):
+        side = {} if self.side is None else {"side_stream": self.side[0], "side_events": self.side[1]}
+        self.layer.forward(self.hidden if hidden is None else hidden,
+                           self.logits if logits is None else logits,
+                           self.mapping if mapping is None else mapping,
+                           out=self.out, topk_ids=self.ids, tile_n=self.tile_n, stage_events=evs,
+                           tuning=self.tuning, **side)
+
+
+def time_steps(L, flush, steps, warmup, pg):
+    """W untimed warm-ups, then ``steps`` forwards, each bracketed by one
+    CUDA event pair on the launching stream (L2 flushed before each, outside
+    the events), a barrier and a synchronize on both sides.  Returns
+    (per-step ms, host start, host end)."""
+    import torch
+    import moe_lora_expert_gb300 as m
+    for _ in range(warmup):
+        flush.zero_()
+        L.step()
+    torch.cuda.synchronize()
+    st = L.layer.device_status()
+    if st != m.MOE_OK:
+        raise SystemExit(f"{L.wl.name}: device status after warm-up: {m.status_string(st)}")
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    h0 = time.perf_counter()
+    for i in range(steps):
+        flush.zero_()
+        ev0[i].record()
+        L.step()
+        ev1[i].record()
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    h1 = time.perf_counter()
+    return [a.elapsed_time(b) for a, b in zip(ev0, ev1)], h0, h1
+
+
+def stage_breakdown(L, flush, n):
+    """A separate pass with events between the stages (they break the
+    programmatic overlap of consecutive kernels, so it is not the timed
+    pass): per-stage CUDA-event times, one list per forward."""
+    import torch
+    import moe_lora_expert_gb300 as m
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(m.MOE_NUM_STAGE_EVENTS)]
+              for _ in range(n)]
+    for i in range(n):
+        flush.zero_()
+        L.step(events[i])
+    torch.cuda.synchronize()
+    return [[ev[j].elapsed_time(ev[j + 1]) for j in range(m.MOE_NUM_STAGE_EVENTS - 1)] for ev in events]
+
+
+def rooflines(L, ms_per_step, stage_ms, peaks, peak_src, workload_tag):
+    """The dominant expert GEMM's roofline (its CUDA-event time in the stage
+    pass) and the whole forward's (max of bytes / HBM and FLOPs / bf16 peak)."""
+    import moe_lora_expert_gb300 as m
+    wl = L.wl
+    ids_np = L.ids.cpu().numpy()
+    work = algorithmic_work(wl, ids_np, L.inp.mapping, fp8=L.fp8, in_gemm_allowed=L.in_gemm_allowed)
+    med = [statistics.median(s[j] for s in stage_ms) for j in range(len(m.STAGE_NAMES))]
+    stages_us = {nm: round(v * 1e3, 2) for nm, v in zip(m.STAGE_NAMES, med)}
+    top = "gemm_gate_up" if med[3] >= med[5] else "gemm_down"
+    kt_ms = statistics.mean(s[3 if top == "gemm_gate_up" else 5] for s in stage_ms)
+    kw = work[top]
+    t_bytes = kw["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_flops = kw["flops"] / (peaks["bf16_tflops"] * 1e12)
+    if t_bytes >= t_flops:
+        achieved = kw["bytes"] / (kt_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    else:
+        achieved = kw["flops"] / (kt_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4)}
+    roof.update({"traffic": committed_traffic(top, workload_tag), "kernel": top,
+                 "kernel_us": round(kt_ms * 1e3, 2), "algorithmic_bytes": kw["bytes"],
+                 "algorithmic_flops": kw["flops"],
+                 "frac_of_max_roof": round(max(t_bytes, t_flops) / (kt_ms / 1e3), 4),
+                 "peak_source": "of measured (MEASURED_PEAKS.json)" if peak_src == "measured"
+                 else "of fallback"})
+    tb = work["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    tf = work["flops"] / (peaks["bf16_tflops"] * 1e12)
+    t_roof = max(tb, tf)
+    fwd = {"bound": "hbm" if tb >= tf else "tensor", "t_roof_us": round(t_roof * 1e6, 2),
+           "t_us": round(ms_per_step * 1e3, 2), "frac": round(t_roof / (ms_per_step / 1e3), 4),
+           "bytes": work["bytes"], "flops": work["flops"],
+           "distinct_experts": work["distinct_experts"], "lora_pairs": work["lora_pairs"]}
+    return roof, fwd, stages_us
+
+
 def run_ours(args):
-    import numpy as np
     import torch
 
     import moe_lora_expert_gb300 as m
-    import workloads
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    wl = workloads.WORKLOADS[args.workload]
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -319,100 +508,48 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
 
-    inp = workloads.make_inputs(wl)
-
-    def bf16(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
-
-    lora = inp.A_gu is not None
-    fp8 = args.weights == "fp8"
-    if fp8:
-        q13, s13, q2, s2 = workloads.fp8_weights(inp)
-        w13_d, w2_d = torch.from_numpy(q13).to(dev), torch.from_numpy(q2).to(dev)
-        scales = dict(w13_scale=torch.from_numpy(s13).to(dev), w2_scale=torch.from_numpy(s2).to(dev))
-    else:
-        w13_d, w2_d, scales = bf16(inp.w13), bf16(inp.w2), {}
-    layer = m.MoeLoraLayer(w13_d, w2_d, wl.top_k,
-                           bf16(inp.A_gu) if lora else None, bf16(inp.B_gu) if lora else None,
-                           bf16(inp.A_dn) if lora else None, bf16(inp.B_dn) if lora else None,
-                           scaling=wl.scaling, max_tokens=wl.T, **scales)
-    hidden = bf16(inp.hidden)
-    logits = torch.from_numpy(inp.logits).to(dev)
-    mapping = torch.from_numpy(inp.mapping).to(dev) if lora else None
-    out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
-    ids = torch.empty((wl.T, wl.top_k), dtype=torch.int32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
-
-    def step(evs=None):
-        layer.forward(hidden, logits, mapping, out=out, topk_ids=ids, tile_n=args.tile_n,
-                      stage_events=evs)
-
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize()
-    st = layer.device_status()
-    if st != m.MOE_OK:
-        raise SystemExit(f"device status after warm-up: {m.status_string(st)}")
-
-    # Timed steps: one event pair around each forward call (events between
-    # the stages would break the programmatic overlap of consecutive kernels).
-    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     visible = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     ids_vis = [v.strip() for v in visible.split(",") if v.strip()]
     clocks = ClockSampler(ids_vis[local] if local < len(ids_vis) else local)
     clocks.start()
-    if pg:
-        pg.barrier()
-    torch.cuda.synchronize()
-    wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.zero_()
-        ev0[i].record()
-        step()
-        ev1[i].record()
-    torch.cuda.synchronize()
-    if pg:
-        pg.barrier()
-    wall = time.perf_counter() - wall0
-    clk = clocks.stop()
-    step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
 
-    # Per-stage breakdown (separate pass, events between the stages): the
-    # dominant kernel's duration for the roofline comes from here.
-    n_br = max(3, min(args.steps, 30))
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(m.MOE_NUM_STAGE_EVENTS)]
-              for _ in range(n_br)]
-    for i in range(n_br):
-        flush.zero_()
-        step(events[i])
-    torch.cuda.synchronize()
-    stage_ms = [[ev[j].elapsed_time(ev[j + 1]) for j in range(m.MOE_NUM_STAGE_EVENTS - 1)]
-                for ev in events]
+    L = Layer(args.workload, args, dev)
+    wl = L.wl
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    peaks, peak_src = load_peaks()
+    fp8 = L.fp8
+    tag = lambda name: name + ("_fp8" if fp8 else "")
+    run0 = time.perf_counter()
+
+    step_ms, h0, h1 = time_steps(L, flush, args.steps, args.warmup, pg)
+    stage_ms = stage_breakdown(L, flush, max(3, min(args.steps, 30)))
     value, total_ms = job_throughput(wl.T, args.steps, world, sum(step_ms), pg, dev)
     ms_per_step = total_ms / args.steps
 
     # ---------------- e2e: host buffers, copies inside the timed region
-    h_hidden = hidden.cpu().pin_memory()
-    h_logits = logits.cpu().pin_memory()
-    h_mapping = mapping.cpu().pin_memory() if lora else None
+    lora = L.lora
+    h_hidden = L.hidden.cpu().pin_memory()
+    h_logits = L.logits.cpu().pin_memory()
+    h_mapping = L.mapping.cpu().pin_memory() if lora else None
     h_out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
-    d_hidden, d_logits = torch.empty_like(hidden), torch.empty_like(logits)
-    d_mapping = torch.empty_like(mapping) if lora else None
+    d_hidden, d_logits = torch.empty_like(L.hidden), torch.empty_like(L.logits)
+    d_mapping = torch.empty_like(L.mapping) if lora else None
+
+    def e2e_step():
+        d_hidden.copy_(h_hidden, non_blocking=True)
+        d_logits.copy_(h_logits, non_blocking=True)
+        if lora:
+            d_mapping.copy_(h_mapping, non_blocking=True)
+        L.step(hidden=d_hidden, logits=d_logits, mapping=d_mapping)
+        h_out.copy_(L.out, non_blocking=True)
+
     e2e_steps = max(1, min(args.steps, 200))
     e_ms = 0.0
     for i in range(args.warmup + e2e_steps):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        d_hidden.copy_(h_hidden, non_blocking=True)
-        d_logits.copy_(h_logits, non_blocking=True)
-        if lora:
-            d_mapping.copy_(h_mapping, non_blocking=True)
-        layer.forward(d_hidden, d_logits, d_mapping, out=out, tile_n=args.tile_n)
-        h_out.copy_(out, non_blocking=True)
+        e2e_step()
         e1.record()
         e1.synchronize()
         if i >= args.warmup:
@@ -424,14 +561,6 @@ def run_ours(args):
 
     # ---------------- the same steps replayed from CUDA graphs: the forward
     # alone, and the whole host-to-host step (copies + forward + copy back)
-    def e2e_step():
-        d_hidden.copy_(h_hidden, non_blocking=True)
-        d_logits.copy_(h_logits, non_blocking=True)
-        if lora:
-            d_mapping.copy_(h_mapping, non_blocking=True)
-        layer.forward(d_hidden, d_logits, d_mapping, out=out, tile_n=args.tile_n)
-        h_out.copy_(out, non_blocking=True)
-
     def replay_ms(g, n):
         total = 0.0
         for i in range(args.warmup + n):
@@ -448,71 +577,72 @@ def run_ours(args):
     g_fwd, g_e2e = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     torch.cuda.synchronize()
     with torch.cuda.graph(g_fwd):
-        step()
+        L.step()
     with torch.cuda.graph(g_e2e):
         e2e_step()
     torch.cuda.synchronize()
     gf_ms = max_over_ranks(replay_ms(g_fwd, e2e_steps), pg, dev)
     ge_ms = max_over_ranks(replay_ms(g_e2e, e2e_steps), pg, dev)
-    st = layer.device_status()
+    st = L.layer.device_status()
     if st != m.MOE_OK:
         raise SystemExit(f"device status after graph replays: {m.status_string(st)}")
     graph = {"forward_us_per_step": round(gf_ms / e2e_steps * 1e3, 2),
              "forward_value": round(world * wl.T * e2e_steps / (gf_ms / 1e3), 1),
              "e2e_value": round(world * wl.T * e2e_steps / (ge_ms / 1e3), 1), "unit": "tokens/s",
              "note": "one CUDA graph per step, replayed; e2e_value includes the host copies"}
+    roof, fwd, stages_us = rooflines(L, ms_per_step, stage_ms, peaks, peak_src, tag(wl.name))
+    n_kernels = kernels_per_forward(wl, fp8, args.shrink_in_gemm != "off", args.side_stream)
+    del L, h_hidden, h_logits, h_mapping, d_hidden, d_logits, d_mapping, g_fwd, g_e2e
+
+    # ---------------- the metric's other batch shapes (T=64, T=4096): the
+    # same timing (steps, warm-ups, L2 flush), rooflines from their own routing
+    others = {}
+    if not args.only_workload:
+        for name in METRIC_WORKLOADS:
+            if name == wl.name:
+                continue
+            Lo = Layer(name, args, dev)
+            o_ms, _, _ = time_steps(Lo, flush, args.steps, args.warmup, pg)
+            o_stage = stage_breakdown(Lo, flush, max(3, min(args.steps, 30)))
+            o_value, o_total = job_throughput(Lo.wl.T, args.steps, world, sum(o_ms), pg, dev)
+            o_roof, o_fwd, o_stages = rooflines(Lo, o_total / args.steps, o_stage, peaks, peak_src,
+                                                tag(name))
+            others[name] = {"value": round(o_value, 1), "unit": "tokens/s",
+                            "ms_per_step": round(o_total / args.steps, 5),
+                            "config": workload_config(Lo.wl, args, world),
+                            "roofline": o_roof, "forward_roofline": o_fwd, "stages_us": o_stages}
+            del Lo
+            torch.cuda.empty_cache()
+    run1 = time.perf_counter()
+    clocks.stop()
 
     if rank != 0:
         if pg:
             pg.destroy_process_group()
         return
 
-    # ---------------- roofline
-    ids_np = ids.cpu().numpy()
-    work = algorithmic_work(wl, ids_np, inp.mapping, fp8=fp8)
-    peaks, peak_src = load_peaks()
-    med = [statistics.median(s[j] for s in stage_ms) for j in range(len(m.STAGE_NAMES))]
-    stages_us = {nm: round(v * 1e3, 2) for nm, v in zip(m.STAGE_NAMES, med)}
-    top = "gemm_gate_up" if med[3] >= med[5] else "gemm_down"
-    kt_ms = statistics.mean(s[3 if top == "gemm_gate_up" else 5] for s in stage_ms)
-    kw = work[top]
-    t_bytes = kw["bytes"] / (peaks["hbm_gbs"] * 1e9)
-    t_flops = kw["flops"] / (peaks["bf16_tflops"] * 1e12)
-    if t_bytes >= t_flops:
-        achieved = kw["bytes"] / (kt_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
-    else:
-        achieved = kw["flops"] / (kt_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4)}
-    roof.update({"traffic": committed_traffic(top, args.workload + ("_fp8" if fp8 else "")), "kernel": top,
-                 "kernel_us": round(kt_ms * 1e3, 2), "algorithmic_bytes": kw["bytes"],
-                 "algorithmic_flops": kw["flops"], "peak_source": f"{peak_src} (MEASURED_PEAKS.json)"
-                 if peak_src == "measured" else "fallback"})
-    t_roof = max(work["bytes"] / (peaks["hbm_gbs"] * 1e9), work["flops"] / (peaks["bf16_tflops"] * 1e12))
-    fwd = {"bound": "hbm" if work["bytes"] / (peaks["hbm_gbs"] * 1e9) >= work["flops"] / (peaks["bf16_tflops"] * 1e12) else "tensor",
-           "t_roof_us": round(t_roof * 1e6, 2), "t_us": round(ms_per_step * 1e3, 2),
-           "frac": round(t_roof / (ms_per_step / 1e3), 4), "bytes": work["bytes"], "flops": work["flops"],
-           "distinct_experts": work["distinct_experts"], "lora_pairs": work["lora_pairs"]}
+    timed = ClockSampler.summary(clocks.window(h0, h1))
+    clk = ClockSampler.summary(clocks.window(run0, run1))
+    clk["timed_region_samples"] = timed.get("samples", 0)
+    clk["window"] = ("nvidia-smi every 50 ms from the first warm-up of the headline workload to the "
+                     "end of the last workload's passes (timed regions, stage passes, e2e, graphs)")
+    if "sm_mhz" in clk:
+        clk["us_x_mhz"] = round(ms_per_step * 1e3 * clk["sm_mhz"], 1)
 
-    n_kernels = kernels_per_forward(wl, fp8)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16 (fp8 e4m3 expert weights, dequantized to bf16)" if fp8 else "bf16",
         "data": "synthetic (seeded normal inputs and weights; no trained weights)",
-        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
-                   "top_k": wl.top_k, "num_adapters": wl.num_adapters, "rank": wl.rank,
-                   "lora_scaling": wl.scaling, "shared_outer": wl.shared_outer,
-                   "tile_n": args.tile_n or "auto", "weights": args.weights,
-                   "l2": "flushed before every step (256 MiB write, outside the step events)",
-                   "parallelism": "replicas" if world > 1 else "single"},
+        "config": workload_config(wl, args, world),
         "roofline": roof, "forward_roofline": fwd, "stages_us": stages_us,
         "cpu_baseline": cpu, "e2e": e2e, "graph": graph, "gpu_launches": n_kernels * args.steps,
-        "clocks": clk, "wall_s_timed_region": round(wall, 4),
+        "clocks": clk, "wall_s_timed_region": round(h1 - h0, 4),
+        "workloads": others,
     }
+    if args.side_stream:
+        line["schedule"] = "two streams: gate_up LoRA shrink on a side stream, joined before the gate_up GEMM"
     print(json.dumps(line))
     if pg:
         pg.destroy_process_group()
@@ -531,13 +661,13 @@ def run_reference(args):
     import workloads
     wl = workloads.WORKLOADS[args.workload]
     inp = workloads.make_inputs(wl)
-    cores = 1
+    threads = 1
     try:
         import threadpoolctl
         info = threadpoolctl.threadpool_info()
-        cores = max([d.get("num_threads", 1) for d in info] + [1])
+        threads = max([d.get("num_threads", 1) for d in info] + [1])
     except Exception:
-        cores = os.cpu_count() or 1
+        threads = os.cpu_count() or 1
     t = 0.0
     tokens = 0
     for i in range(args.warmup + args.steps):
@@ -549,17 +679,16 @@ def run_reference(args):
             t += dt
             tokens += len(tok)
     value = tokens / t
-    sample = f"1 token of {wl.name} per step (float64 numpy oracle)"
+    sample = (f"1 token of {wl.name} per step (float64 numpy oracle, BLAS pool of {threads} "
+              f"threads on a host with {os.cpu_count()} cores)")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(t / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded normal inputs and weights; no trained weights)",
-            "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
-                       "top_k": wl.top_k, "num_adapters": wl.num_adapters, "rank": wl.rank,
-                       "parallelism": "host CPU"},
-            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores,
-                             "kind": "oracle", "sample": sample},
+            "config": workload_config(wl, args, world),
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": threads,
+                             "host_cores": os.cpu_count(), "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))

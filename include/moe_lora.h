@@ -185,6 +185,33 @@ typedef struct {
 #define MOE_NUM_STAGE_EVENTS 8
 
 /* ---------------------------------------------------------------------------
+ * Kernel-choice overrides (moe_lora_args_t.tuning), for measurement and
+ * tests.  A zeroed struct keeps every choice of the library; the library
+ * reads no environment variables, so a captured CUDA graph runs exactly the
+ * kernels its arguments name.
+ *   cta_pairs:      0 = auto (pairs for 256-wide token tiles), 1 = never,
+ *                   2 = pairs for 128- and 256-wide tiles.
+ *   shrink_kernel:  0 = auto, 1 = the 16-row-tile LoRA shrink kernel,
+ *                   2 = the row-block shrink kernel (not for a shared gate_up
+ *                   A factor, which always uses the 16-row kernel).
+ *   shrink_in_gemm: 0 = auto (the row gather and both LoRA shrinks run
+ *                   inside the expert GEMMs for decode-sized tiles),
+ *                   1 = never (separate gather/shrink kernels).
+ *   gemm_max_ctas:  0 = auto (SM count x resident CTAs per SM); otherwise
+ *                   at most this many CTAs in each expert GEMM's persistent
+ *                   grid (rounded up to a pair for CTA pairs).  Any value is
+ *                   correct: no CTA waits on work that a CTA which has not
+ *                   started owns.
+ * Values outside these sets return MOE_ERR_UNSUPPORTED.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  int cta_pairs;
+  int shrink_kernel;
+  int shrink_in_gemm;
+  int gemm_max_ctas;
+} moe_lora_tuning_t;
+
+/* ---------------------------------------------------------------------------
  * moe_lora_forward arguments.
  *
  *   hidden [T, H] bf16; router_logits [T, E] float32;
@@ -238,6 +265,23 @@ typedef struct {
  *   weight_format, w13_scale, w2_scale: FP8 block-scaled expert weights (see
  *     MOE_WEIGHTS_FP8_E4M3_B128); callers passing a struct_size that ends
  *     before weight_format get bf16 weights.
+ *   tuning: kernel-choice overrides (moe_lora_tuning_t); callers passing a
+ *     struct_size that ends before it get the library's choices.
+ *   side_stream, side_events: the two-stream schedule of the gate_up LoRA
+ *     ("[WIP][LoRA] BF16 support for the experimental_sgl_trtllm MoE-LoRA
+ *     path & lora expert_outer_shared", Summary "Phase 2" and Flow 1(B): the
+ *     gate_up LoRA runs on a second stream and joins on an event before its
+ *     result is used).  When side_stream is non-NULL, the gate_up LoRA shrink
+ *     U = s A_gu x runs on side_stream while ``stream`` gathers the permuted
+ *     rows; side_events[0] (recorded on ``stream`` after the permute) forks
+ *     and side_events[1] (recorded on side_stream after the shrink) joins
+ *     before the gate_up GEMM, which adds the expand s B_gu U.  The shrinks
+ *     then never run inside the GEMMs.  Both events are created by the
+ *     caller (cudaEventDisableTiming is fine) and must not be in use by
+ *     another call in flight; the sequence can be captured into a CUDA graph
+ *     from ``stream`` (the fork/join become graph edges).  With rank 0 or no
+ *     adapters the side stream is not used.  NULL events with a non-NULL
+ *     side_stream return MOE_ERR_NULL.
  * ------------------------------------------------------------------------- */
 typedef struct {
   uint32_t struct_size;           /* sizeof(moe_lora_args_t) */
@@ -266,6 +310,9 @@ typedef struct {
   int weight_format;              /* MOE_WEIGHTS_BF16 (0) or MOE_WEIGHTS_FP8_E4M3_B128 */
   const float* w13_scale;         /* FP8: [E, ceil(2I/128), ceil(H/128)] float32 */
   const float* w2_scale;          /* FP8: [E, ceil(H/128), ceil(I/128)] float32 */
+  moe_lora_tuning_t tuning;       /* zeroed = the library's choices */
+  struct CUstream_st* side_stream;       /* NULL, or see below */
+  struct CUevent_st* side_events[2];     /* caller-created events for side_stream */
 } moe_lora_args_t;
 
 /* Expert weight formats (moe_lora_args_t.weight_format). */

@@ -56,6 +56,12 @@ class LoraFactors(ctypes.Structure):
                 ("b_stride_adapter", ctypes.c_int64), ("b_stride_expert", ctypes.c_int64)]
 
 
+class Tuning(ctypes.Structure):
+    """Kernel-choice overrides (moe_lora_tuning_t); all zero = the library's choices."""
+    _fields_ = [("cta_pairs", ctypes.c_int), ("shrink_kernel", ctypes.c_int),
+                ("shrink_in_gemm", ctypes.c_int), ("gemm_max_ctas", ctypes.c_int)]
+
+
 class MoeLoraArgs(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_uint32),
                 ("T", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int), ("E", ctypes.c_int),
@@ -74,7 +80,9 @@ class MoeLoraArgs(ctypes.Structure):
                 ("adapter_scaling", ctypes.c_void_p),
                 ("local_expert_offset", ctypes.c_int), ("num_router_experts", ctypes.c_int),
                 ("weight_format", ctypes.c_int), ("w13_scale", ctypes.c_void_p),
-                ("w2_scale", ctypes.c_void_p)]
+                ("w2_scale", ctypes.c_void_p),
+                ("tuning", Tuning),
+                ("side_stream", ctypes.c_void_p), ("side_events", ctypes.c_void_p * 2)]
 
 
 class WorkspacePlan(ctypes.Structure):
@@ -313,7 +321,10 @@ class MoeLoraLayer:
 
     def make_args(self, hidden, router_logits, token_lora_mapping, out, topk_ids=None, topk_w=None,
                   expanded_to_permuted=None, tile_n=0, wait_timeout_ms=0, stage_events=None,
-                  debug_flags=0):
+                  debug_flags=0, tuning=None, side_stream=None, side_events=None):
+        """``tuning``: a Tuning or a dict of its fields.  ``side_stream`` (a
+        torch.cuda.Stream) with ``side_events`` (two torch.cuda.Event): the
+        two-stream schedule of the gate_up LoRA shrink."""
         T = hidden.shape[0]
         ws = self.workspace(T)
         a = MoeLoraArgs()
@@ -335,6 +346,16 @@ class MoeLoraLayer:
             a.weight_format = MOE_WEIGHTS_FP8_E4M3_B128
             a.w13_scale, a.w2_scale = self.w13_scale.data_ptr(), self.w2_scale.data_ptr()
         a.adapter_scaling = ctypes.cast(self._scales, ctypes.c_void_p) if self._scales is not None else None
+        if tuning is not None:
+            a.tuning = tuning if isinstance(tuning, Tuning) else Tuning(**tuning)
+        if side_stream is not None:
+            if side_events is None or len(side_events) != 2:
+                raise ValueError("side_stream needs two side_events")
+            for e in side_events:        # torch creates the CUDA event on first record
+                if not e.cuda_event:
+                    e.record()
+            a.side_stream = side_stream.cuda_stream
+            a.side_events[0], a.side_events[1] = side_events[0].cuda_event, side_events[1].cuda_event
         self._events_keepalive = None
         if stage_events is not None:
             if len(stage_events) != MOE_NUM_STAGE_EVENTS:
@@ -349,7 +370,8 @@ class MoeLoraLayer:
 
     def forward(self, hidden, router_logits, token_lora_mapping=None, out=None, topk_ids=None,
                 topk_w=None, expanded_to_permuted=None, tile_n=0, wait_timeout_ms=0,
-                stage_events: Optional[Sequence] = None, stream=None, debug_flags=0):
+                stage_events: Optional[Sequence] = None, stream=None, debug_flags=0, tuning=None,
+                side_stream=None, side_events=None):
         torch = _torch()
         T = hidden.shape[0]
         _require(hidden, torch.bfloat16, (T, self.H), "hidden")
@@ -360,7 +382,7 @@ class MoeLoraLayer:
             out = torch.empty((T, self.H), dtype=torch.bfloat16, device=hidden.device)
         args = self.make_args(hidden, router_logits, token_lora_mapping, out, topk_ids, topk_w,
                               expanded_to_permuted, tile_n, wait_timeout_ms, stage_events,
-                              debug_flags)
+                              debug_flags, tuning, side_stream, side_events)
         _check(moe_lora_forward(args, stream), "moe_lora_forward")
         return out
 

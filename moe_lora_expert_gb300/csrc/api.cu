@@ -306,12 +306,24 @@ int moe_read_device_status(const void* workspace, moe_stream_t stream) {
 int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   if (a == nullptr) return MOE_ERR_NULL;
   // Structures from before the expert-parallel fields end at adapter_scaling,
-  // those from before the weight-format fields at num_router_experts.
+  // those from before the weight-format fields at num_router_experts, those
+  // from before the tuning and side-stream fields at w2_scale.
   constexpr size_t kSizeNoShard = offsetof(moe_lora_args_t, local_expert_offset);
   constexpr size_t kSizeNoFormat = offsetof(moe_lora_args_t, weight_format);
+  constexpr size_t kSizeNoTuning = offsetof(moe_lora_args_t, tuning);
   if (a->struct_size < kSizeNoShard) return MOE_ERR_UNSUPPORTED;
   const bool has_shard = a->struct_size >= kSizeNoFormat;
-  const bool has_format = a->struct_size >= sizeof(moe_lora_args_t);
+  const bool has_format = a->struct_size >= kSizeNoTuning;
+  const bool has_tuning = a->struct_size >= sizeof(moe_lora_args_t);
+  moe_lora_tuning_t tune;
+  std::memset(&tune, 0, sizeof(tune));
+  if (has_tuning) tune = a->tuning;
+  if (tune.cta_pairs < 0 || tune.cta_pairs > 2 || tune.shrink_kernel < 0 || tune.shrink_kernel > 2 ||
+      tune.shrink_in_gemm < 0 || tune.shrink_in_gemm > 1 || tune.gemm_max_ctas < 0)
+    return MOE_ERR_UNSUPPORTED;
+  cudaStream_t side = has_tuning ? reinterpret_cast<cudaStream_t>(a->side_stream) : nullptr;
+  if (side != nullptr && (a->side_events[0] == nullptr || a->side_events[1] == nullptr))
+    return MOE_ERR_NULL;
   const int wfmt = has_format ? a->weight_format : MOE_WEIGHTS_BF16;
   const bool w8 = wfmt == MOE_WEIGHTS_FP8_E4M3_B128;
   const int T = a->T, H = a->H, I = a->I, E = a->E, K = a->top_k;
@@ -417,22 +429,12 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   // and the shrink variant follow the rows per local expert.
   const int64_t n_local = n * E / R;
   const int bn = a->tile_n ? a->tile_n : auto_tile_n(static_cast<int>(n_local), E);
-  // CTAs per cluster sharing a token tile (TMA multicast).  MOE_LORA_CLUSTER
-  // overrides the default for tuning (1, 2 or 4; 4 only with 256-wide tiles).
-  int cl = moe::gemm_cluster_size(bn);
-  if (const char* env = std::getenv("MOE_LORA_CLUSTER")) {
-    const int v = std::atoi(env);
-    if (v == 1 || (v == 2 && bn >= 128) || (v == 4 && bn == 256)) cl = v;
-  }
-  // CTA pairs sharing one M = 256 MMA (wide tiles, no multicast cluster).
-  // MOE_LORA_PAIR=0/1 overrides the default for tuning (128- or 256-wide tiles).
-  bool pair = cl == 1 && moe::gemm_use_pair(bn);
-  if (const char* env = std::getenv("MOE_LORA_PAIR")) pair = cl == 1 && std::atoi(env) != 0 && bn >= 128;
-  if (w8) {  // FP8 weights run one CTA per tile
-    pair = false;
-    cl = 1;
-  }
-  if (pair) cl = 2;  // a pair is a cluster of two; each CTA loads bn / 2 token rows
+  // CTA pairs sharing one M = 256 MMA (cta_group::2) for wide tiles; each CTA
+  // of a pair loads bn / 2 token rows.  FP8 weights run one CTA per tile.
+  bool pair = moe::gemm_use_pair(bn);
+  if (tune.cta_pairs == 1) pair = false;
+  if (tune.cta_pairs == 2) pair = bn >= 128;
+  if (w8) pair = false;
   const int sms = num_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
   // Many rows, or a large rank with several rows per expert (the factor is
@@ -441,16 +443,21 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   // 16-row kernel.
   bool row_blocks = n_local > 16 * static_cast<int64_t>(sms) ||
                     (r >= 64 && n_local >= 8 * std::min<int64_t>(E, n_local));
-  if (const char* env = std::getenv("MOE_LORA_SHRINK_ROWS")) row_blocks = std::atoi(env) != 0;  // tuning
+  if (tune.shrink_kernel != 0) row_blocks = tune.shrink_kernel == 2;
   // Decode-sized tiles: the row gather and the LoRA shrinks run inside the
   // expert GEMMs (their epilogue warps are idle until the first accumulator
   // is ready), so no kernel sits between the permute and the gate_up GEMM or
-  // between the GEMMs.  Needs the one-CTA permute (it clears the tile flags),
-  // one CTA per 16-wide tile, rank <= 32 and per-expert gate_up A factors.
-  // MOE_LORA_FUSE_SHRINK=0 turns it off (tuning).
-  bool fuse_shrink = lora && small_permute && bn == 16 && cl == 1 && !pair && r <= 32 &&
-                     !row_blocks && a->gate_up.a_stride_expert != 0;
-  if (const char* env = std::getenv("MOE_LORA_FUSE_SHRINK")) fuse_shrink = fuse_shrink && std::atoi(env) != 0;
+  // between the GEMMs.  Needs the one-CTA permute (it clears the tile flags
+  // and the row counters), one CTA per 16-wide tile, rank <= 32 and
+  // per-expert gate_up A factors.  The two-stream schedule keeps the shrinks
+  // in kernels of their own.
+  const bool fuse_shrink = lora && small_permute && bn == 16 && !pair && r <= 32 && !row_blocks &&
+                           a->gate_up.a_stride_expert != 0 && tune.shrink_in_gemm == 0 &&
+                           side == nullptr;
+  const bool two_streams = lora && side != nullptr;
+  // Persistent grid of the expert GEMMs.
+  int gemm_grid = sms * moe::gemm_ctas_per_sm(bn);
+  if (tune.gemm_max_ctas > 0) gemm_grid = std::min(gemm_grid, std::max(tune.gemm_max_ctas, pair ? 2 : 1));
   const uint64_t timeout_ns =
       static_cast<uint64_t>(a->wait_timeout_ms ? a->wait_timeout_ms : 2000) * 1000000ull;
 
@@ -460,10 +467,11 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   const uint64_t w2_dims[2] = {static_cast<uint64_t>(I), static_cast<uint64_t>(E) * H};
   const uint64_t w2_row[1] = {static_cast<uint64_t>(I) * (w8 ? 1 : 2)};
   const uint32_t w2_box[2] = {64, 128};
+  const int tok_box = pair ? bn / 2 : bn;  // token rows per CTA and stage
   bool enc = encode_w13(&tm_w13, a->w13, H, I, E, &gu_single_box, w8) &&
              encode_nd(&tm_w2, a->w2, 2, w2_dims, w2_row, w2_box, w8) &&
-             encode_2d(&tm_xp, xp, H, n, H * 2ull, 64, bn / cl) &&
-             encode_2d(&tm_h, h, I, n, I * 2ull, 64, bn / cl);
+             encode_2d(&tm_xp, xp, H, n, H * 2ull, 64, tok_box) &&
+             encode_2d(&tm_h, h, I, n, I * 2ull, 64, tok_box);
   int64_t gu_rs_a = 0, gu_rs_e = 0, dn_rs_a = 0, dn_rs_e = 0;
   if (enc && lora) {
     gu_rs_a = a->gate_up.b_stride_adapter / r;
@@ -475,8 +483,8 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
     if (gu_rows >= (1ull << 31) || dn_rows >= (1ull << 31)) return MOE_ERR_UNSUPPORTED;
     enc = encode_2d(&tm_bgu, a->gate_up.B, r, gu_rows, r * 2ull, 64, 16) &&
           encode_2d(&tm_bdn, a->down.B, r, dn_rows, r * 2ull, 64, 128) &&
-          encode_2d(&tm_u, U, static_cast<uint64_t>(A) * r, n, A * r * 2ull, 64, bn / cl) &&
-          encode_2d(&tm_v, V, static_cast<uint64_t>(A) * r, n, A * r * 2ull, 64, bn / cl);
+          encode_2d(&tm_u, U, static_cast<uint64_t>(A) * r, n, A * r * 2ull, 64, tok_box) &&
+          encode_2d(&tm_v, V, static_cast<uint64_t>(A) * r, n, A * r * 2ull, 64, tok_box);
   } else {
     tm_bgu = tm_w13;
     tm_bdn = tm_w2;
@@ -575,11 +583,28 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   sp.mapping = lora ? a->token_lora_mapping : nullptr;
   sp.tile_start_rows = tile_start + moe::tile_width_index(moe::rows_shrink_tile()) * (E + 1);
   sp.gmask = fp.gmask;
-  if (!fuse_shrink &&  // fused: the gate_up GEMM gathers the rows itself
-      (row_blocks && !sp.per_token ? moe::launch_rows_shrink(sp, static_cast<int>(n), stream)
-                                   : moe::launch_gather_shrink(sp, static_cast<int>(n), stream)) !=
-          cudaSuccess)
+  auto launch_shrink = [&](const ShrinkParams& q, cudaStream_t s) {
+    return row_blocks && !q.per_token ? moe::launch_rows_shrink(q, static_cast<int>(n), s)
+                                      : moe::launch_gather_shrink(q, static_cast<int>(n), s);
+  };
+  if (two_streams) {
+    // Fork after the permute: the shrink (U only) on the side stream, the
+    // row gather (xp only) here; join before the gate_up GEMM.
+    cudaEvent_t fork = reinterpret_cast<cudaEvent_t>(a->side_events[0]);
+    cudaEvent_t join = reinterpret_cast<cudaEvent_t>(a->side_events[1]);
+    ShrinkParams sq = sp;
+    sq.gathered = nullptr;
+    sp.U = nullptr;
+    if (cudaEventRecord(fork, stream) != cudaSuccess || cudaStreamWaitEvent(side, fork, 0) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (launch_shrink(sq, side) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaEventRecord(join, side) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_shrink(sp, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamWaitEvent(stream, join, 0) != cudaSuccess) return MOE_ERR_CUDA;
+  } else if (!fuse_shrink &&  // fused: the gate_up GEMM gathers the rows itself
+             launch_shrink(sp, stream) != cudaSuccess) {
     return MOE_ERR_CUDA;
+  }
   if (!mark()) return MOE_ERR_CUDA;
   // 4. gate_up GEMM + LoRA expand + SwiGLU -> h
   GemmParams gp{};
@@ -618,11 +643,11 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
     gp.sa_stride_expert = a->gate_up.a_stride_expert;
     gp.su = U;
     gp.tile_flags = flags_gu;
+    gp.row_counter = flags_gu + moe::shrink_flag_words(static_cast<int>(n), E) - 1;
     for (int i = 0; i < MOE_MAX_ADAPTERS; ++i) gp.sscale[i] = sp.scaling[i];
   }
-  if (moe::launch_expert_gemm(moe::kGateUp, bn, cl, pair, w8, tm_w13, tm_xp, tm_bgu, tm_u, gp,
-                              sms * moe::gemm_ctas_per_sm(bn), stream) !=
-      cudaSuccess)
+  if (moe::launch_expert_gemm(moe::kGateUp, bn, pair, w8, tm_w13, tm_xp, tm_bgu, tm_u, gp, gemm_grid,
+                              stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!mark()) return MOE_ERR_CUDA;
   // 5. down LoRA shrink: V = s * A_dn h (fused: inside the down GEMM)
@@ -663,13 +688,13 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
     gp.sa_stride_expert = a->down.a_stride_expert;
     gp.su = V;
     gp.tile_flags = flags_dn;
+    gp.row_counter = flags_dn + moe::shrink_flag_words(static_cast<int>(n), E) - 1;
   }
   gp.w_scale = w8 ? a->w2_scale : nullptr;
   gp.scale_nb = (H + 127) / 128;
   gp.scale_kb = (I + 127) / 128;
-  if (moe::launch_expert_gemm(moe::kDown, bn, cl, pair, w8, tm_w2, tm_h, tm_bdn, tm_v, gp,
-                              sms * moe::gemm_ctas_per_sm(bn), stream) !=
-      cudaSuccess)
+  if (moe::launch_expert_gemm(moe::kDown, bn, pair, w8, tm_w2, tm_h, tm_bdn, tm_v, gp, gemm_grid,
+                              stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!mark()) return MOE_ERR_CUDA;
   // 7. finalize

@@ -86,8 +86,8 @@ struct Work {
 };
 
 // Work unit u = (token tile, feature-block group).  Each CTA of a cluster of
-// CL takes feature block group * CL + its rank, so the CTAs of a cluster work
-// on the same token tile at the same time and can share its loads.
+// CL (a CTA pair: CL = 2) takes feature block group * CL + its rank, so the
+// two CTAs of a pair work on the same token tile at the same time.
 template <int BN>
 __device__ __forceinline__ Work decode_work(int u, int crank, int CL, const int* s_off,
                                             const int* s_ts, int E, int FBg) {
@@ -169,9 +169,12 @@ __device__ __forceinline__ void raise_timeout_at(int* status, volatile int* abor
   *abort_flag = 1;
 }
 
-// The LoRA shrink of rows blockIdx.x, blockIdx.x + gridDim.x, ... of the
-// permuted rows, by the four epilogue warps (ew = 0..3) before their first
-// accumulator (GemmParams::fuse_shrink).  For row p with adapter
+// The LoRA shrink of the permuted rows, by the four epilogue warps (ew =
+// 0..3) before their first accumulator (GemmParams::fuse_shrink).  Rows are
+// claimed one at a time from p.row_counter (thread 0 claims the next row
+// while the current one is computed), so only CTAs that are running take
+// rows: a producer that waits for a tile waits on rows that running CTAs,
+// its own included, finish without waiting on anything.  For row p with adapter
 // a = row_adapter[p] >= 0, su[p, a r + i] = bf16(s_a sum_k A[a, e][i][k]
 // sx[p][k]) for i < r; every other column of the row is zero.  The 128
 // threads split K in 8-element pieces (thread j takes k = 8 j + 1024 m), sum
@@ -188,7 +191,14 @@ __device__ void shrink_rows_in_gemm(const GemmParams& p, const int* s_off, const
   const int R = p.rank, ld = p.num_adapters * p.rank, K = p.K;
   const int tid = ew * 32 + lane;
   const int nrows_all = s_off[p.E];
-  for (int prow = blockIdx.x; prow < nrows_all; prow += gridDim.x) {
+  volatile int* s_row = reinterpret_cast<volatile int*>(s_red + 128);  // the claimed row
+  int next = tid == 0 ? atomicAdd(p.row_counter, 1) : 0;
+  while (true) {
+    if (tid == 0) *s_row = next;
+    named_barrier_sync(1, 128);  // the claimed row is visible to the four warps
+    const int prow = *s_row;
+    if (prow >= nrows_all) break;
+    if (tid == 0) next = atomicAdd(p.row_counter, 1);  // in flight while this row is computed
     int lo = 0, hi = p.E - 1;  // expert of the row: largest e with s_off[e] <= prow
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -259,6 +269,7 @@ __device__ void shrink_rows_in_gemm(const GemmParams& p, const int* s_off, const
       red_release_gpu_add(p.tile_flags + tile, 1);
     }
   }
+  named_barrier_sync(1, 128);  // every warp has read *s_row: the staging tiles are free
 }
 
 // Bounded wait until ``count`` rows of a token tile are published by the
@@ -349,10 +360,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                        const __grid_constant__ CUtensorMap tm_lb, const __grid_constant__ CUtensorMap tm_lu,
                        const GemmParams p) {
-  static_assert(!PAIR || CL == 2, "a pair is a cluster of two");
+  static_assert(PAIR == (CL == 2) && CL <= 2, "one CTA per tile, or a pair (a cluster of two)");
   static_assert(!W8 || (CL == 1 && !PAIR), "FP8 weights: one CTA per tile");
   using C = GemmCfg<BN, PAIR, W8>;
-  constexpr bool kMulticast = CL > 1 && !PAIR;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -384,9 +394,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
     }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], W8 ? C::kConvWarps : 1);  // FP8: one arrival per converter warp
-      // multicast: every CTA of the cluster releases the stage; pair: the
-      // leader's commit arrives once in each CTA
-      mbar_init(&empty[s], kMulticast ? CL : 1);
+      // pair: the leader's commit arrives once in each CTA
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accf[b], 1);
@@ -430,7 +439,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  // Peers multicast into this CTA's barriers: all of them must be initialised.
+  // The pair leader's loads and commits arrive on this CTA's barriers: all of
+  // them must be initialised.
   if (CL > 1) cluster_sync_all();
   const uint32_t tmem_base = *tmem_slot;
   const int crank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
@@ -438,8 +448,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
   const int unit_step = CL > 1 ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
   const int FBg = (p.feat_blocks + CL - 1) / CL;
   const int total_work = s_ts[p.E] * FBg;
-  constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CL) - 1u);
-  constexpr int kPieceRows = BN / CL;              // token rows each CTA loads and multicasts
   const bool leader = !PAIR || crank == 0;
 
   if (W8 && warp == 0) {
@@ -550,9 +558,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
       uint8_t* sB = smem + st * C::kStageBytes + C::kABytes;
       if constexpr (PAIR)
         tma_load_2d_pair(sB, map, mapa_shared(smem_u32(&full[st]), 0), c0, c1, pol_x);
-      else if constexpr (kMulticast)
-        tma_load_2d_multicast(sB + crank * kPieceRows * 128, map, &full[st], c0,
-                              c1 + crank * kPieceRows, kClusterMask, pol_x);
       else
         tma_load_2d(sB, map, &full[st], c0, c1, pol_x);
     };
@@ -703,7 +708,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
                             (b > 0 || ks > 0) ? 1u : 0u);
             }
             if constexpr (PAIR) tc_commit_pair(&empty[stage], 0x3);
-            else if constexpr (kMulticast) tc_commit_multicast(&empty[stage], kClusterMask);
             else tc_commit(&empty[stage]);
             if constexpr (W8) tc_commit(&empty8[s8]);
           } else {
@@ -1006,21 +1010,17 @@ static cudaError_t launch_one(const CUtensorMap& tm_w, const CUtensorMap& tm_x,
   return cudaLaunchKernelEx(&cfg, kern, tm_w, tm_x, tm_lb, tm_lu, p);
 }
 
-// Multicast of the token tile measured no faster than one CTA per tile on
-// prefill_T4096 (646.6 vs 646.0 us with 2; 686.8 with 4), so it is off by
-// default and kept as a tuning option.
-int gemm_cluster_size(int) { return 1; }
-
 // Wide token tiles run as CTA pairs (cta_group::2): each SM then lands half
 // of the token tile per stage, which leaves room for deeper stages.
 bool gemm_use_pair(int bn) { return bn == 256; }
 
-cudaError_t launch_expert_gemm(int mode, int bn, int cl, bool pair, bool w8, const CUtensorMap& tm_w,
+cudaError_t launch_expert_gemm(int mode, int bn, bool pair, bool w8, const CUtensorMap& tm_w,
                                const CUtensorMap& tm_x, const CUtensorMap& tm_lb,
                                const CUtensorMap& tm_lu, const GemmParams& p, int grid,
                                cudaStream_t s) {
+  const int cl = pair ? 2 : 1;
   if (w8) {
-    if (cl != 1 || pair) return cudaErrorInvalidValue;
+    if (pair) return cudaErrorInvalidValue;
 #define MOE_GEMM_W8_CASE(BNV)                                                                     \
     if (bn == BNV)                                                                                \
       return mode == kGateUp                                                                      \
@@ -1044,9 +1044,6 @@ cudaError_t launch_expert_gemm(int mode, int bn, int cl, bool pair, bool w8, con
   MOE_GEMM_CASE(64, 1, false)
   MOE_GEMM_CASE(128, 1, false)
   MOE_GEMM_CASE(256, 1, false)
-  MOE_GEMM_CASE(128, 2, false)
-  MOE_GEMM_CASE(256, 2, false)
-  MOE_GEMM_CASE(256, 4, false)
   MOE_GEMM_CASE(128, 2, true)
   MOE_GEMM_CASE(256, 2, true)
 #undef MOE_GEMM_CASE

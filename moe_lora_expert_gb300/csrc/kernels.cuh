@@ -76,7 +76,9 @@ constexpr int kPermuteChunk = 1024;
 size_t permute_scratch_bytes(int n, int E);
 size_t gmask_bytes(int n, int E);
 // Tile flags of the in-kernel shrink: two arrays (gate_up, down) of
-// ceil(n / 16) + E + 1 words each, after the adapter masks.
+// ceil(n / 16) + E + 1 words each, after the adapter masks.  A 16-wide tile
+// index is below ceil(n / 16) + E - 1, so the last word of each array is
+// free: it holds that GEMM's row counter (shrink_rows_in_gemm).
 size_t shrink_flag_words(int n, int E);
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s);
 
@@ -186,12 +188,14 @@ struct GemmParams {
   // may begin before this grid's own wait.  0: everything waits first.
   int tables_ready;
   // LoRA shrink inside the kernel (narrow tiles, one CTA per tile, rank <=
-  // 32): before their first accumulator, the epilogue warps of CTA b write
-  // permuted rows b, b + gridDim.x, ... of su = bf16(s_a A[a, e] x) (the
-  // row's own adapter's columns; zeros in the others) and count each row on
-  // its token tile's flag; the producer waits until a tile's flag equals its
-  // row count before the tile's first LoRA block.  The flags are cleared by
-  // the permute of the same forward.
+  // 32): before their first accumulator, the epilogue warps of every CTA
+  // claim permuted rows one at a time from row_counter and write each
+  // claimed row of su = bf16(s_a A[a, e] x) (the row's own adapter's
+  // columns; zeros in the others), then count the row on its token tile's
+  // flag; the producer waits until a tile's flag equals its row count before
+  // the tile's first LoRA block.  Rows go only to CTAs that are running, so
+  // every wait ends whatever number of CTAs the GPU holds at once.  The
+  // flags and the counter are cleared by the permute of the same forward.
   int fuse_shrink;
   const __nv_bfloat16* sx;             // [n, K]: the token rows (xp or h)
   // Or also gather them: sx row p = gather_src row gather_map[p] / gather_div
@@ -205,20 +209,19 @@ struct GemmParams {
   int64_t sa_stride_expert;            // elements between experts
   __nv_bfloat16* su;                   // [n, num_adapters * rank]
   int* tile_flags;                     // [tiles of this width]
+  int* row_counter;                    // next unclaimed permuted row (zeroed by the permute)
   float sscale[MOE_MAX_ADAPTERS];      // per adapter
 };
 enum GemmMode { kGateUp = 0, kDown = 1 };
 int gemm_stage_count(int bn, bool pair);
 int gemm_ctas_per_sm(int bn);
 size_t gemm_smem_bytes(int bn, bool pair);
-// cl: CTAs per cluster along the feature blocks (1, or 2/4 for wide token
-// tiles): the cluster's CTAs share each token tile through TMA multicast.
-int gemm_cluster_size(int bn);
-// pair: clusters of two CTAs sharing one M = 256 MMA (cta_group::2); cl = 2.
+// pair: clusters of two CTAs sharing one M = 256 MMA (cta_group::2).
 bool gemm_use_pair(int bn);
 // w8: FP8 block-scaled weights (tm_w is then a 1-byte view, p.w_scale set);
-// one CTA per tile (cl = 1, no pair).
-cudaError_t launch_expert_gemm(int mode, int bn, int cl, bool pair, bool w8, const CUtensorMap& tm_w,
+// one CTA per tile (no pair).  grid: CTAs of the persistent grid (pairs: at
+// most as many clusters of two as can be resident).
+cudaError_t launch_expert_gemm(int mode, int bn, bool pair, bool w8, const CUtensorMap& tm_w,
                                const CUtensorMap& tm_x, const CUtensorMap& tm_lb,
                                const CUtensorMap& tm_lu, const GemmParams& p, int grid,
                                cudaStream_t s);

@@ -51,8 +51,9 @@ def make_layer(inp, with_lora=True, **shard):
                           **shard)
 
 
-def run_gpu(inp, layer=None, tile_n=0, with_lora=True, mapping=None):
-    """Returns dict(out64, ids, w, e2p, status, layer)."""
+def run_gpu(inp, layer=None, tile_n=0, with_lora=True, mapping=None, **fwd):
+    """Returns dict(out64, ids, w, e2p, status, layer).  ``fwd``: further
+    forward arguments (tuning, side_stream, side_events, ...)."""
     import moe_lora_expert_gb300 as m
     torch = torch_mod()
     wl = inp.wl
@@ -65,7 +66,7 @@ def run_gpu(inp, layer=None, tile_n=0, with_lora=True, mapping=None):
     out = layer.forward(bf16_tensor(inp.hidden), torch.from_numpy(inp.logits).to(dev()),
                         torch.from_numpy(np.ascontiguousarray(mp, dtype=np.int32)).to(dev())
                         if layer.num_adapters else None,
-                        topk_ids=ids, topk_w=w, expanded_to_permuted=e2p, tile_n=tile_n)
+                        topk_ids=ids, topk_w=w, expanded_to_permuted=e2p, tile_n=tile_n, **fwd)
     status = layer.device_status()
     torch.cuda.synchronize()
     return {"out64": to_f64(out), "out": out, "ids": ids.cpu().numpy(), "w": w.cpu().numpy(),

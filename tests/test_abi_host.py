@@ -49,8 +49,9 @@ def test_abi_version_and_struct_layout(lib, tmp_path):
     if cc is None:
         pytest.skip("no C compiler")
     checks = []
-    for struct, ctype in [(m.LoraFactors, "moe_lora_factors_t"), (m.MoeLoraArgs, "moe_lora_args_t"),
-                          (m.WorkspacePlan, "moe_lora_workspace_plan_t")]:
+    structs = [(m.LoraFactors, "moe_lora_factors_t"), (m.MoeLoraArgs, "moe_lora_args_t"),
+               (m.WorkspacePlan, "moe_lora_workspace_plan_t"), (m.Tuning, "moe_lora_tuning_t")]
+    for struct, ctype in structs:
         checks.append(f'printf("%s sizeof %zu\\n", "{ctype}", sizeof({ctype}));')
         for fname, _ in struct._fields_:
             checks.append(f'printf("%s %s %zu\\n", "{ctype}", "{fname}", offsetof({ctype}, {fname}));')
@@ -65,8 +66,7 @@ def test_abi_version_and_struct_layout(lib, tmp_path):
         if ln.strip():
             *key, val = ln.split()
             got[" ".join(key)] = int(val)
-    for struct, ctype in [(m.LoraFactors, "moe_lora_factors_t"), (m.MoeLoraArgs, "moe_lora_args_t"),
-                          (m.WorkspacePlan, "moe_lora_workspace_plan_t")]:
+    for struct, ctype in structs:
         assert got[f"{ctype} sizeof"] == ctypes.sizeof(struct), ctype
         for fname, _ in struct._fields_:
             assert got[f"{ctype} {fname}"] == getattr(struct, fname).offset, (ctype, fname)
@@ -172,6 +172,16 @@ def _valid_args(**over):
     ({"weight_format": m.MOE_WEIGHTS_FP8_E4M3_B128, "w13_scale": 1 << 20, "w2_scale": (1 << 20) + 2},
      m.MOE_ERR_ALIGN),
     ({"weight_format": m.MOE_WEIGHTS_FP8_E4M3_B128, "H": 2056}, m.MOE_ERR_ALIGN),  # 1-byte rows
+    # kernel-choice overrides outside their sets
+    ({"tuning": m.Tuning(cta_pairs=3)}, m.MOE_ERR_UNSUPPORTED),
+    ({"tuning": m.Tuning(shrink_kernel=-1)}, m.MOE_ERR_UNSUPPORTED),
+    ({"tuning": m.Tuning(shrink_in_gemm=2)}, m.MOE_ERR_UNSUPPORTED),
+    ({"tuning": m.Tuning(gemm_max_ctas=-5)}, m.MOE_ERR_UNSUPPORTED),
+    # a structure from before the tuning fields ignores them (checks go on)
+    ({"struct_size": m.MoeLoraArgs.tuning.offset, "tuning": m.Tuning(cta_pairs=3), "hidden": None},
+     m.MOE_ERR_NULL),
+    # the two-stream schedule needs both events
+    ({"side_stream": 1 << 12}, m.MOE_ERR_NULL),
 ])
 def test_forward_rejects_on_host(lib, over, status):
     a = _valid_args(**over)

@@ -47,9 +47,11 @@ def test_shrink_in_gemm_conditions():
 
 
 def test_gemm_bytes_charge_the_in_gemm_shrink():
-    """With the gather and shrinks inside the GEMMs, the gate_up kernel is
-    charged the A factors, the hidden rows read and the permuted rows
-    written; the down kernel the down A factors.  The sums are rebuilt here
+    """Each expert GEMM is charged the weights and LoRA factors it reads and
+    none of the intermediates (permuted rows, LoRA operands, activation,
+    expert outputs).  With the gather and shrinks inside the GEMMs, the
+    gate_up kernel is also charged the A factors and the hidden input it
+    reads; the down kernel the down A factors.  The sums are rebuilt here
     term by term from the routing of the seeded inputs."""
     wl = workloads.WORKLOADS["decode_T16"]
     inp = workloads.make_inputs(wl)
@@ -61,11 +63,37 @@ def test_gemm_bytes_charge_the_in_gemm_shrink():
     adapted = [(t, int(inp.mapping[t])) for t in range(T) if inp.mapping[t] >= 0]
     pairs = len({(a, int(e)) for t, a in adapted for e in ids[t]})
     n_ad = len(adapted) * k
-    gu = experts * 2 * I * H * 2 + pairs * 2 * I * r * 2 + n * H * 2 + n_ad * r * 2 + n * I * 2
-    gu += pairs * r * H * 2 + T * H * 2 + n * H * 2
-    dn = experts * H * I * 2 + pairs * H * r * 2 + n * I * 2 + n_ad * r * 2 + n * H * 2
+    gu = experts * 2 * I * H * 2 + pairs * 2 * I * r * 2
+    gu += pairs * r * H * 2 + T * H * 2
+    dn = experts * H * I * 2 + pairs * H * r * 2
     dn += pairs * r * I * 2
     assert work["gemm_gate_up"]["bytes"] == gu
     assert work["gemm_down"]["bytes"] == dn
     assert work["gemm_gate_up"]["flops"] == n * 2 * 2 * I * H + n_ad * 2 * 2 * I * r + n_ad * 2 * r * H
     assert work["gemm_down"]["flops"] == n * 2 * H * I + n_ad * 2 * H * r + n_ad * 2 * r * I
+
+
+def test_gemm_bytes_without_the_in_gemm_shrink():
+    """Separate shrink kernels (prefill, or the in-GEMM shrink turned off):
+    the GEMMs are charged only their weights and B factors; the forward's
+    bytes are the same either way."""
+    wl = workloads.WORKLOADS["decode_T16"]
+    inp = workloads.make_inputs(wl)
+    ids, _ = oracle.route_topk(inp.logits, wl.top_k)
+    fused = bench.algorithmic_work(wl, ids, inp.mapping)
+    sep = bench.algorithmic_work(wl, ids, inp.mapping, in_gemm_allowed=False)
+    H, I, r = wl.H, wl.I, wl.rank
+    experts = len(set(int(e) for e in ids.ravel()))
+    pairs = fused["lora_pairs"]
+    assert sep["gemm_gate_up"]["bytes"] == experts * 2 * I * H * 2 + pairs * 2 * I * r * 2
+    assert sep["gemm_down"]["bytes"] == experts * H * I * 2 + pairs * H * r * 2
+    assert sep["bytes"] == fused["bytes"] and sep["flops"] == fused["flops"]
+
+
+def test_kernel_counts_of_the_other_schedules():
+    W = workloads.WORKLOADS
+    # separate shrinks: permute, gather+shrink, GEMM, shrink, GEMM, finalize
+    assert bench.kernels_per_forward(W["decode_T16"], in_gemm_allowed=False) == 6
+    # two streams: the gather and the gate_up shrink are two kernels
+    assert bench.kernels_per_forward(W["decode_T16"], two_streams=True) == 7
+    assert bench.kernels_per_forward(W["prefill_T4096"], two_streams=True) == 10

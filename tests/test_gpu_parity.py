@@ -250,30 +250,14 @@ def test_repeated_calls_are_deterministic():
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-@pytest.mark.parametrize("cluster", ["1", "2", "4"])
-def test_forward_cluster_sizes(cluster, monkeypatch):
-    """Wide token tiles shared by a cluster of CTAs through TMA multicast; I=136
-    and H=192 leave feature blocks that do not divide by the cluster size."""
-    monkeypatch.setenv("MOE_LORA_CLUSTER", cluster)
-    monkeypatch.setenv("MOE_LORA_PAIR", "0")
-    wl = workloads.small_workload("cluster", T=300, H=192, I=136, E=3, top_k=2, num_adapters=3,
-                                  rank=16, map_lo=-1, map_hi=2, seed=61)
-    inp = workloads.make_inputs(wl)
-    res = run_gpu(inp, tile_n=256)
-    assert res["status"] == 0, res["status_str"]
-    check_routing(res, inp)
-    assert_output_close(res["out64"], oracle.forward_inputs(inp)["out64"], f"cluster={cluster}")
-
-
 @pytest.mark.parametrize("with_lora", [True, False])
 @pytest.mark.parametrize("tile_n", [128, 256])
-def test_forward_cta_pairs(tile_n, with_lora, monkeypatch):
+def test_forward_cta_pairs(tile_n, with_lora):
     """Wide token tiles on CTA pairs that share one M = 256 MMA (cta_group::2).
     I=136 gives an odd number of gate_up feature blocks (the last pair's second
     CTA has none); T=700 over 3 experts gives full and partial tiles, some
     with no valid row in the second CTA's half; without LoRA the down GEMM
     follows the gate_up GEMM directly."""
-    monkeypatch.setenv("MOE_LORA_PAIR", "1")
     cases = [
         workloads.small_workload("pair_odd", T=300, H=192, I=136, E=3, top_k=2, num_adapters=3,
                                  rank=16, map_lo=-1, map_hi=2, seed=61),
@@ -286,7 +270,7 @@ def test_forward_cta_pairs(tile_n, with_lora, monkeypatch):
     ]
     for wl in cases:
         inp = workloads.make_inputs(wl)
-        res = run_gpu(inp, tile_n=tile_n, with_lora=with_lora)
+        res = run_gpu(inp, tile_n=tile_n, with_lora=with_lora, tuning={"cta_pairs": 2})
         assert res["status"] == 0, res["status_str"]
         check_routing(res, inp)
         ref = oracle.forward_inputs(inp, with_lora=with_lora)["out64"]
@@ -309,15 +293,14 @@ def test_forward_many_rows_row_block_shrink(with_lora):
     assert_output_close(res["out64"][tokens], ref, f"rows lora={with_lora}")
 
 
-@pytest.mark.parametrize("fused", ["1", "0"])
+@pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("name", ["decode_T16", "decode_T64_mixed8", "tiny_T8"])
-def test_forward_shrink_in_gemm_and_separate(name, fused, monkeypatch):
+def test_forward_shrink_in_gemm_and_separate(name, fused):
     """Decode-sized tiles compute the LoRA shrinks inside the expert GEMMs
-    (tile flags between CTAs); MOE_LORA_FUSE_SHRINK=0 keeps the separate
+    (tile flags between CTAs); tuning.shrink_in_gemm = 1 keeps the separate
     shrink kernels.  Both against the oracle."""
-    monkeypatch.setenv("MOE_LORA_FUSE_SHRINK", fused)
     inp = cached_inputs(name)
-    res = run_gpu(inp)
+    res = run_gpu(inp, tuning={"shrink_in_gemm": 0 if fused else 1})
     assert res["status"] == 0, res["status_str"]
     check_routing(res, inp)
     assert_output_close(res["out64"], oracle.forward_inputs(inp)["out64"], f"{name} fused={fused}")
@@ -460,3 +443,48 @@ def test_peft_adapters_separate_gate_up_mixed_ranks_and_scales(shape):
     ref, _ = oracle.moe_lora_forward_general(inp.hidden, inp.logits, inp.w13, inp.w2, mapping,
                                              wl.top_k, ads)
     assert_output_close(to_f64(out), ref, f"peft {shape}")
+
+
+@pytest.mark.parametrize("max_ctas", [152, 5, 1])
+@pytest.mark.parametrize("name", ["decode_T16", "decode_T64_mixed8"])
+def test_shrink_in_gemm_needs_no_co_resident_grid(name, max_ctas):
+    """The in-GEMM shrink hands its rows to running CTAs only (a row counter),
+    so a producer never waits on a row that a CTA which has not started owns.
+    With the expert GEMMs' persistent grid cut to one CTA per SM, to five
+    CTAs, or to one CTA (which then shrinks every row itself), the forward is
+    correct and no wait runs out."""
+    inp = cached_inputs(name)
+    res = run_gpu(inp, tuning={"gemm_max_ctas": max_ctas})
+    assert res["status"] == 0, res["status_str"]
+    check_routing(res, inp)
+    assert_output_close(res["out64"], oracle.forward_inputs(inp)["out64"], f"{name} ctas={max_ctas}")
+
+
+@pytest.mark.parametrize("name", ["tiny_T8", "decode_T16", "decode_T64_mixed8",
+                                  "skewed_T256_shared_outer_r64"])
+def test_two_stream_gate_up_shrink(name):
+    """The two-stream schedule: the gate_up LoRA shrink on a second stream,
+    forked after the permute and joined by an event before the gate_up GEMM,
+    while the main stream gathers the rows.  Against the oracle, eager and
+    replayed from a CUDA graph captured on the main stream."""
+    torch = torch_mod()
+    inp = cached_inputs(name)
+    side = torch.cuda.Stream()
+    evs = [torch.cuda.Event(), torch.cuda.Event()]
+    res = run_gpu(inp, side_stream=side, side_events=evs)
+    assert res["status"] == 0, res["status_str"]
+    check_routing(res, inp)
+    ref = oracle.forward_inputs(inp)["out64"]
+    assert_output_close(res["out64"], ref, f"{name} two streams")
+    layer = res["layer"]
+    hid = bf16_tensor(inp.hidden)
+    lg = torch.from_numpy(inp.logits).to(dev())
+    mp = torch.from_numpy(inp.mapping).to(dev())
+    out = torch.empty_like(res["out"])
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.forward(hid, lg, mp, out=out, side_stream=side, side_events=evs)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), res["out"].view(torch.int16)), name
+    assert layer.device_status() == 0
