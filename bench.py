@@ -44,6 +44,8 @@ def parse_args():
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--weights", choices=["bf16", "fp8"], default="bf16",
                     help="expert weight format (fp8: e4m3 with 128x128 block scales)")
+    ap.add_argument("--fp8-activations", action="store_true",
+                    help="with --weights fp8: FP8 activations too (W8A8, per-token-group quant)")
     ap.add_argument("--only-workload", action="store_true",
                     help="measure --workload alone (default: also the metric's other batch shapes)")
     ap.add_argument("--shrink-in-gemm", choices=["auto", "off"], default="auto",
@@ -143,7 +145,7 @@ def shrink_in_gemm(wl, fp8=False, allowed=True):
             not wl.shared_outer)
 
 
-def kernels_per_forward(wl, fp8=False, in_gemm_allowed=True, two_streams=False):
+def kernels_per_forward(wl, fp8=False, in_gemm_allowed=True, two_streams=False, w8a8=False):
     """Kernels one moe_lora_forward launches (mirrors the library's choices):
     routing (unless fused into the one-CTA permute), the permute (one CTA, or
     count + scan + scatter), the gather/gate_up shrink and the down shrink
@@ -155,6 +157,9 @@ def kernels_per_forward(wl, fp8=False, in_gemm_allowed=True, two_streams=False):
     fuse_route = small and wl.T <= 128
     lora = wl.num_adapters > 0 and wl.rank > 0
     two = two_streams and lora
+    if w8a8:  # the row quant, the gate_up shrink, the activation quant, the down shrink
+        return ((0 if fuse_route else 1) + (1 if small else 3) + 1 + (1 if lora else 0) + 1 + 1 +
+                (1 if lora else 0) + 1 + 1)
     fuse_shrink = shrink_in_gemm(wl, fp8, in_gemm_allowed and not two)
     return ((0 if fuse_route else 1) + (1 if small else 3) + (0 if fuse_shrink else 1) +
             (1 if two else 0) + 1 + (1 if lora and not fuse_shrink else 0) + 1 + 1)
@@ -342,6 +347,7 @@ def workload_config(wl, args, world):
             "top_k": wl.top_k, "num_adapters": wl.num_adapters, "rank": wl.rank,
             "lora_scaling": wl.scaling, "shared_outer": wl.shared_outer,
             "tile_n": args.tile_n or "auto", "weights": args.weights,
+            "activations": "fp8" if (args.fp8_activations and args.weights == "fp8") else "bf16",
             "l2": "GPU arm: flushed before every step (256 MiB write, outside the step events)",
             "parallelism": "replicas" if world > 1 else "single"}
 
@@ -380,7 +386,8 @@ class Layer:
         self.layer = m.MoeLoraLayer(w13_d, w2_d, wl.top_k,
                                     bf16(inp.A_gu) if lora else None, bf16(inp.B_gu) if lora else None,
                                     bf16(inp.A_dn) if lora else None, bf16(inp.B_dn) if lora else None,
-                                    scaling=wl.scaling, max_tokens=wl.T, **scales)
+                                    scaling=wl.scaling, max_tokens=wl.T,
+                                    fp8_activations=bool(args.fp8_activations and self.fp8), **scales)
         self.hidden = bf16(inp.hidden)
         self.logits = torch.from_numpy(inp.logits).to(dev)
         self.mapping = torch.from_numpy(inp.mapping).to(dev) if lora else None
@@ -389,7 +396,8 @@ class Layer:
         self.tile_n = args.tile_n
         self.tuning = tuning_from_args(args)
         self.side = None
-        self.in_gemm_allowed = args.shrink_in_gemm != "off" and not args.side_stream
+        self.in_gemm_allowed = (args.shrink_in_gemm != "off" and not args.side_stream and
+                                not (self.fp8 and args.fp8_activations))
         if args.side_stream:
             self.side = (torch.cuda.Stream(device=dev), [torch.cuda.Event(), torch.cuda.Event()])
 
@@ -518,7 +526,7 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     peaks, peak_src = load_peaks()
     fp8 = L.fp8
-    tag = lambda name: name + ("_fp8" if fp8 else "")
+    tag = lambda name: name + ("_w8a8" if fp8 and args.fp8_activations else "_fp8" if fp8 else "")
     run0 = time.perf_counter()
 
     step_ms, h0, h1 = time_steps(L, flush, args.steps, args.warmup, pg)
@@ -591,7 +599,8 @@ def run_ours(args):
              "e2e_value": round(world * wl.T * e2e_steps / (ge_ms / 1e3), 1), "unit": "tokens/s",
              "note": "one CUDA graph per step, replayed; e2e_value includes the host copies"}
     roof, fwd, stages_us = rooflines(L, ms_per_step, stage_ms, peaks, peak_src, tag(wl.name))
-    n_kernels = kernels_per_forward(wl, fp8, args.shrink_in_gemm != "off", args.side_stream)
+    n_kernels = kernels_per_forward(wl, fp8, args.shrink_in_gemm != "off", args.side_stream,
+                                    bool(fp8 and args.fp8_activations))
     del L, h_hidden, h_logits, h_mapping, d_hidden, d_logits, d_mapping, g_fwd, g_e2e
 
     # ---------------- the metric's other batch shapes (T=64, T=4096): the
@@ -633,7 +642,8 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16 (fp8 e4m3 expert weights, dequantized to bf16)" if fp8 else "bf16",
+        "dtype": ("fp8 e4m3 x e4m3 (W8A8; bf16 LoRA, fp32 accumulate)" if fp8 and args.fp8_activations
+                  else "bf16 (fp8 e4m3 expert weights, dequantized to bf16)" if fp8 else "bf16"),
         "data": "synthetic (seeded normal inputs and weights; no trained weights)",
         "config": workload_config(wl, args, world),
         "roofline": roof, "forward_roofline": fwd, "stages_us": stages_us,

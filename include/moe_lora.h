@@ -282,6 +282,11 @@ typedef struct {
  *     from ``stream`` (the fork/join become graph edges).  With rank 0 or no
  *     adapters the side stream is not used.  NULL events with a non-NULL
  *     side_stream return MOE_ERR_NULL.
+ *   activation_format: MOE_ACT_BF16, or MOE_ACT_FP8_E4M3_G128 for the W8A8
+ *     path (requires MOE_WEIGHTS_FP8_E4M3_B128 weights, else
+ *     MOE_ERR_UNSUPPORTED, and a workspace of moe_lora_workspace_size_ex()
+ *     with that format).  Callers passing a struct_size that ends before it
+ *     get bf16 activations.
  * ------------------------------------------------------------------------- */
 typedef struct {
   uint32_t struct_size;           /* sizeof(moe_lora_args_t) */
@@ -313,6 +318,7 @@ typedef struct {
   moe_lora_tuning_t tuning;       /* zeroed = the library's choices */
   struct CUstream_st* side_stream;       /* NULL, or see below */
   struct CUevent_st* side_events[2];     /* caller-created events for side_stream */
+  int activation_format;          /* MOE_ACT_BF16 (0) or MOE_ACT_FP8_E4M3_G128 */
 } moe_lora_args_t;
 
 /* Expert weight formats (moe_lora_args_t.weight_format). */
@@ -326,6 +332,50 @@ typedef struct {
  * Requires H % 16 == 0 and I % 16 == 0 (MOE_ERR_ALIGN) and both scale
  * arrays (MOE_ERR_NULL). */
 #define MOE_WEIGHTS_FP8_E4M3_B128 1
+
+/* Activation formats (moe_lora_args_t.activation_format). */
+#define MOE_ACT_BF16 0
+/* The pages' FP8 path ("[WIP][LoRA] BF16 support for the
+ * experimental_sgl_trtllm MoE-LoRA path & lora expert_outer_shared", Flow
+ * 1(A): the bf16 path is the FP8 one without a per_token_group_quant_fp8 of
+ * the hidden input and without a post-activation quant).  Read as: per row
+ * and group of MOE_ACT_FP8_GROUP consecutive columns, in float32, scale =
+ * max(amax, 1e-10) / 448 and code = e4m3(x / scale), nearest with ties to
+ * even, saturating at +-448 (see moe_per_token_group_quant_fp8).  The
+ * hidden rows are quantized before the gate_up GEMM; the activation h =
+ * silu(gate) * up is quantized from its float32 value before the down GEMM.
+ * Both expert GEMMs multiply e4m3 by e4m3 on the tensor cores, applying the
+ * weight-block x token-group scales per 128-K block; the LoRA deltas read
+ * the unquantized bf16 hidden rows and activation.  Token tiles are at most
+ * 128 wide (tile_n 256 runs as 128). */
+#define MOE_ACT_FP8_E4M3_G128 1
+#define MOE_ACT_FP8_GROUP 128
+
+/* ---------------------------------------------------------------------------
+ * moe_per_token_group_quant_fp8 -- the activation quantizer of the FP8 path.
+ *
+ * The per_token_group_quant_fp8 step of Flow 1(A) in "[WIP][LoRA] BF16
+ * support for the experimental_sgl_trtllm MoE-LoRA path & lora
+ * expert_outer_shared".  For output row i and column group g (columns
+ * [128 g, 128 g + 128) of K), in float32:
+ *   scales[i, g] = max(max_k |x[src(i), k]|, 1e-10) / 448      (IEEE divide)
+ *   codes[i, k]  = e4m3(x[src(i), k] / scales[i, g])           (IEEE divide,
+ *                  nearest, ties to even, |.| > 448 saturates to 448)
+ * with src(i) = row_map[i] / map_div when row_map is non-NULL (a negative
+ * row_map[i] gives a zero row: codes 0, scale 1e-10 / 448), else src(i) = i.
+ * e4m3 is the finite-only float8 variant (bias 7, max 448).
+ *
+ *   x        [*, K] device, bf16 (x_is_f32 = 0) or float32 (x_is_f32 = 1),
+ *            16-byte aligned.
+ *   rows, K  output rows and columns; K a multiple of 16 (MOE_ERR_ALIGN).
+ *   row_map  [rows] int32 device, or NULL.  map_div >= 1.
+ *   codes    [rows, K] uint8 device, written.
+ *   scales   [rows, ceil(K / 128)] float32 device, written.
+ * Returns MOE_OK once enqueued; rows == 0 is a no-op.
+ * ------------------------------------------------------------------------- */
+int moe_per_token_group_quant_fp8(const void* x, int x_is_f32, int rows, int K,
+                                  const int32_t* row_map, int map_div, uint8_t* codes,
+                                  float* scales, moe_stream_t stream);
 
 /* Test-only flag for debug_flags: the gate_up GEMM's MMA role first waits on
  * a barrier that nothing signals, so its wait runs out after wait_timeout_ms;
@@ -361,9 +411,16 @@ typedef struct {
 /* Fills ``plan`` (host pointer).  Returns MOE_OK or MOE_ERR_SHAPE/UNSUPPORTED. */
 int moe_lora_workspace_plan(int T, int H, int I, int E, int top_k, int num_adapters,
                             int rank, moe_lora_workspace_plan_t* plan);
-/* Bytes of workspace moe_lora_forward needs (0 on invalid sizes). */
+/* Bytes of workspace moe_lora_forward needs with bf16 activations (0 on
+ * invalid sizes). */
 size_t moe_lora_workspace_size(int T, int H, int I, int E, int top_k, int num_adapters,
                                int rank);
+/* As moe_lora_workspace_size, for the given activation_format: FP8
+ * activations add, after the bf16 plan, the quantized permuted rows and
+ * activation with their scales and the float32 activation (0 on invalid
+ * sizes or formats). */
+size_t moe_lora_workspace_size_ex(int T, int H, int I, int E, int top_k, int num_adapters,
+                                  int rank, int activation_format);
 
 /* ---------------------------------------------------------------------------
  * moe_lora_forward -- the whole layer forward (steps 1-7) on one stream.

@@ -32,6 +32,9 @@ MOE_ERR_BAD_EXPERT_ID = -9
 MOE_NUM_STAGE_EVENTS = 8
 MOE_WEIGHTS_BF16 = 0
 MOE_WEIGHTS_FP8_E4M3_B128 = 1
+MOE_ACT_BF16 = 0
+MOE_ACT_FP8_E4M3_G128 = 1
+MOE_ACT_FP8_GROUP = 128
 MOE_DEBUG_STALL_GATE_UP_MMA = 1
 MOE_DEBUG_HOLD_SHRINK_ROW = 2
 STAGE_NAMES = ["route", "permute", "shrink_gate_up", "gemm_gate_up", "shrink_down", "gemm_down",
@@ -40,7 +43,8 @@ STAGE_NAMES = ["route", "permute", "shrink_gate_up", "gemm_gate_up", "shrink_dow
 EXPORTED_SYMBOLS = [
     "moe_status_string", "moe_lora_abi_version", "moe_route_topk", "moe_permute_workspace_size",
     "moe_permute", "moe_lora_workspace_plan", "moe_lora_workspace_size", "moe_lora_forward",
-    "moe_read_device_status", "moe_permute_noalloc",
+    "moe_read_device_status", "moe_permute_noalloc", "moe_per_token_group_quant_fp8",
+    "moe_lora_workspace_size_ex",
 ]
 
 
@@ -82,7 +86,8 @@ class MoeLoraArgs(ctypes.Structure):
                 ("weight_format", ctypes.c_int), ("w13_scale", ctypes.c_void_p),
                 ("w2_scale", ctypes.c_void_p),
                 ("tuning", Tuning),
-                ("side_stream", ctypes.c_void_p), ("side_events", ctypes.c_void_p * 2)]
+                ("side_stream", ctypes.c_void_p), ("side_events", ctypes.c_void_p * 2),
+                ("activation_format", ctypes.c_int)]
 
 
 class WorkspacePlan(ctypes.Structure):
@@ -123,6 +128,10 @@ def lib() -> ctypes.CDLL:
         L.moe_read_device_status.argtypes = [vp, vp]
         L.moe_permute_noalloc.restype = i32
         L.moe_permute_noalloc.argtypes = [vp, i32, i32, i32, vp, i32, vp, vp, vp, vp, vp, vp]
+        L.moe_per_token_group_quant_fp8.restype = i32
+        L.moe_per_token_group_quant_fp8.argtypes = [vp, i32, i32, i32, vp, i32, vp, vp, vp]
+        L.moe_lora_workspace_size_ex.restype = sz
+        L.moe_lora_workspace_size_ex.argtypes = [i32] * 8
         _lib = L
     return _lib
 
@@ -221,6 +230,30 @@ def moe_lora_workspace_size(T, H, I, E, top_k, num_adapters, rank) -> int:
     return int(lib().moe_lora_workspace_size(T, H, I, E, top_k, num_adapters, rank))
 
 
+def moe_lora_workspace_size_ex(T, H, I, E, top_k, num_adapters, rank, activation_format) -> int:
+    return int(lib().moe_lora_workspace_size_ex(T, H, I, E, top_k, num_adapters, rank,
+                                                activation_format))
+
+
+def moe_per_token_group_quant_fp8(x, row_map=None, map_div=1, rows=None, stream=None):
+    """Codes (uint8 [rows, K]) and scales (float32 [rows, ceil(K / 128)]) of
+    the rows of ``x`` (bf16 or float32 [*, K]); ``row_map``: int32 [rows],
+    output row i reads x row row_map[i] // map_div (negative: a zero row)."""
+    torch = _torch()
+    if x.dtype not in (torch.bfloat16, torch.float32) or not x.is_contiguous() or x.dim() != 2:
+        raise ValueError("x must be a contiguous bf16 or float32 matrix")
+    K = x.shape[1]
+    if rows is None:
+        rows = row_map.shape[0] if row_map is not None else x.shape[0]
+    codes = torch.empty((rows, K), dtype=torch.uint8, device=x.device)
+    scales = torch.empty((rows, (K + MOE_ACT_FP8_GROUP - 1) // MOE_ACT_FP8_GROUP), dtype=torch.float32,
+                         device=x.device)
+    _check(lib().moe_per_token_group_quant_fp8(_ptr(x), 1 if x.dtype == torch.float32 else 0, rows, K,
+                                               _ptr(row_map), map_div, _ptr(codes), _ptr(scales),
+                                               _stream_handle(stream)), "moe_per_token_group_quant_fp8")
+    return codes, scales
+
+
 def moe_lora_forward(args: MoeLoraArgs, stream=None) -> int:
     """Raw call: returns the status code (no raise)."""
     return int(lib().moe_lora_forward(ctypes.byref(args), _stream_handle(stream)))
@@ -254,7 +287,7 @@ class MoeLoraLayer:
     def __init__(self, w13, w2, top_k: int, A_gu=None, B_gu=None, A_dn=None, B_dn=None,
                  scaling: float = 1.0, max_tokens: int = 0, adapter_scaling=None,
                  local_expert_offset: int = 0, num_router_experts: int = 0,
-                 w13_scale=None, w2_scale=None):
+                 w13_scale=None, w2_scale=None, fp8_activations: bool = False):
         torch = _torch()
         self.E, twoI, self.H = w13.shape
         self.local_expert_offset = int(local_expert_offset)
@@ -274,6 +307,9 @@ class MoeLoraLayer:
             _require(w13, torch.bfloat16, (self.E, 2 * self.I, self.H), "w13")
             _require(w2, torch.bfloat16, (self.E, self.H, self.I), "w2")
         self.w13_scale, self.w2_scale = w13_scale, w2_scale
+        if fp8_activations and not self.fp8:
+            raise TypeError("FP8 activations need FP8 weights (W8A8)")
+        self.act_format = MOE_ACT_FP8_E4M3_G128 if fp8_activations else MOE_ACT_BF16
         self.w13, self.w2, self.top_k, self.scaling = w13, w2, top_k, float(scaling)
         self.A_gu, self.B_gu, self.A_dn, self.B_dn = A_gu, B_gu, A_dn, B_dn
         if A_gu is not None:
@@ -307,8 +343,8 @@ class MoeLoraLayer:
 
     def workspace(self, T: int):
         torch = _torch()
-        need = moe_lora_workspace_size(T, self.H, self.I, self.E, self.top_k, self.num_adapters,
-                                       self.rank)
+        need = moe_lora_workspace_size_ex(T, self.H, self.I, self.E, self.top_k, self.num_adapters,
+                                          self.rank, self.act_format)
         if need == 0:
             raise MoeError(MOE_ERR_SHAPE, "moe_lora_workspace_size")
         if self._ws is None or self._ws.numel() < need:
@@ -342,6 +378,7 @@ class MoeLoraLayer:
         a.tile_n, a.wait_timeout_ms = int(tile_n), int(wait_timeout_ms)
         a.debug_flags = int(debug_flags)
         a.local_expert_offset, a.num_router_experts = self.local_expert_offset, self.num_router_experts
+        a.activation_format = self.act_format
         if self.fp8:
             a.weight_format = MOE_WEIGHTS_FP8_E4M3_B128
             a.w13_scale, a.w2_scale = self.w13_scale.data_ptr(), self.w2_scale.data_ptr()

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmoelora.so")
-SOURCES = ["api.cu", "routing.cu", "lora_shrink.cu", "expert_gemm.cu", "permute_noalloc.cu"]
+SOURCES = ["api.cu", "routing.cu", "lora_shrink.cu", "expert_gemm.cu", "fp8_gemm.cu", "permute_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]

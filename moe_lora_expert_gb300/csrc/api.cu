@@ -72,9 +72,10 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
 
 // N-D tensor (dims innermost first, strides in bytes for dims 1..rank-1),
 // zero fill out of bounds: bf16 with 128-byte swizzle, or (fp8) bytes
-// without swizzle (the converter warps read them).
+// without swizzle (the W8A16 converter warps read them) or, with sw128, with
+// 128-byte swizzle (the FP8 tensor-core operands).
 bool encode_nd(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-               const uint64_t* strides, const uint32_t* box, bool fp8 = false) {
+               const uint64_t* strides, const uint32_t* box, bool fp8 = false, bool sw128 = false) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t d[5], st[4];
@@ -87,7 +88,7 @@ bool encode_nd(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
   }
   return fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
             const_cast<void*>(base), d, st, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+            (fp8 && !sw128) ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -159,6 +160,35 @@ void fill_plan(int T, int H, int I, int E, int top_k, int num_adapters, int rank
   pl->lora_v = pl->lora_u;
   pl->act = take(n * static_cast<size_t>(I) * 2);
   pl->total_bytes = o;
+}
+
+// FP8 activations: buffers after the bf16 plan (byte offsets from the
+// workspace start).
+struct Fp8ActPlan {
+  size_t xq;     // uint8 [n, H]   quantized permuted hidden rows
+  size_t xs;     // float [n, ceil(H / 128)]
+  size_t hf;     // float [n, I]   activation before its quant
+  size_t hq;     // uint8 [n, I]
+  size_t hs;     // float [n, ceil(I / 128)]
+  size_t total_bytes;
+};
+
+void fill_fp8_plan(int T, int H, int I, int top_k, size_t base, Fp8ActPlan* f) {
+  const size_t n = static_cast<size_t>(T) * top_k;
+  const size_t gh = (static_cast<size_t>(H) + moe::kActGroup - 1) / moe::kActGroup;
+  const size_t gi = (static_cast<size_t>(I) + moe::kActGroup - 1) / moe::kActGroup;
+  size_t o = base;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align_up(bytes);
+    return at;
+  };
+  f->xq = take(n * H);
+  f->xs = take(n * gh * 4);
+  f->hf = take(n * I * 4);
+  f->hq = take(n * I);
+  f->hs = take(n * gi * 4);
+  f->total_bytes = o;
 }
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -294,6 +324,38 @@ size_t moe_lora_workspace_size(int T, int H, int I, int E, int top_k, int num_ad
   return pl.total_bytes;
 }
 
+size_t moe_lora_workspace_size_ex(int T, int H, int I, int E, int top_k, int num_adapters, int rank,
+                                  int activation_format) {
+  const size_t base = moe_lora_workspace_size(T, H, I, E, top_k, num_adapters, rank);
+  if (base == 0 || activation_format == MOE_ACT_BF16) return base;
+  if (activation_format != MOE_ACT_FP8_E4M3_G128) return 0;
+  Fp8ActPlan f;
+  fill_fp8_plan(T, H, I, top_k, base, &f);
+  return f.total_bytes;
+}
+
+int moe_per_token_group_quant_fp8(const void* x, int x_is_f32, int rows, int K, const int32_t* row_map,
+                                  int map_div, uint8_t* codes, float* scales, moe_stream_t stream) {
+  if (rows < 0 || K <= 0 || map_div < 1 || (x_is_f32 != 0 && x_is_f32 != 1)) return MOE_ERR_SHAPE;
+  if (K % 16 != 0) return MOE_ERR_ALIGN;
+  if (rows == 0) return MOE_OK;
+  if (x == nullptr || codes == nullptr || scales == nullptr) return MOE_ERR_NULL;
+  if (!aligned16(x) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(scales) & 3) != 0)
+    return MOE_ERR_ALIGN;
+  (void)cudaGetLastError();  // launch checks below must not report an earlier, unrelated error
+  moe::QuantParams q{};
+  q.x = x;
+  q.x_f32 = x_is_f32;
+  q.row_map = row_map;
+  q.map_div = map_div;
+  q.rows = rows;
+  q.K = K;
+  q.codes = codes;
+  q.scales = scales;
+  q.copy = nullptr;
+  return cuda_status(moe::launch_quant_groups(q, stream));
+}
+
 int moe_read_device_status(const void* workspace, moe_stream_t stream) {
   if (workspace == nullptr) return MOE_ERR_NULL;
   int host[4] = {0, 0, 0, 0};
@@ -311,10 +373,12 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   constexpr size_t kSizeNoShard = offsetof(moe_lora_args_t, local_expert_offset);
   constexpr size_t kSizeNoFormat = offsetof(moe_lora_args_t, weight_format);
   constexpr size_t kSizeNoTuning = offsetof(moe_lora_args_t, tuning);
+  constexpr size_t kSizeNoActFormat = offsetof(moe_lora_args_t, activation_format);
   if (a->struct_size < kSizeNoShard) return MOE_ERR_UNSUPPORTED;
   const bool has_shard = a->struct_size >= kSizeNoFormat;
   const bool has_format = a->struct_size >= kSizeNoTuning;
-  const bool has_tuning = a->struct_size >= sizeof(moe_lora_args_t);
+  const bool has_tuning = a->struct_size >= kSizeNoActFormat;
+  const bool has_act = a->struct_size >= sizeof(moe_lora_args_t);
   moe_lora_tuning_t tune;
   std::memset(&tune, 0, sizeof(tune));
   if (has_tuning) tune = a->tuning;
@@ -334,6 +398,10 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   if (st != MOE_OK) return st;
   if (R < E || R > MOE_MAX_EXPERTS || K > R || shard_off < 0 || shard_off > R - E) return MOE_ERR_SHAPE;
   if (wfmt != MOE_WEIGHTS_BF16 && wfmt != MOE_WEIGHTS_FP8_E4M3_B128) return MOE_ERR_UNSUPPORTED;
+  const int afmt = has_act ? a->activation_format : MOE_ACT_BF16;
+  if (afmt != MOE_ACT_BF16 && afmt != MOE_ACT_FP8_E4M3_G128) return MOE_ERR_UNSUPPORTED;
+  const bool a8 = afmt == MOE_ACT_FP8_E4M3_G128;  // W8A8: FP8 activations need FP8 weights
+  if (a8 && !w8) return MOE_ERR_UNSUPPORTED;
   // FP8 weight rows are 1 byte per element: TMA wants 16-byte row pitches.
   if (w8 && (H % 16 != 0 || I % 16 != 0)) return MOE_ERR_ALIGN;
   const bool lora = a->num_adapters > 0 && a->rank > 0;
@@ -391,7 +459,9 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   if ((reinterpret_cast<uintptr_t>(a->workspace) & (kAlign - 1)) != 0) return MOE_ERR_WORKSPACE;
   moe_lora_workspace_plan_t pl;
   fill_plan(T, H, I, E, K, A, r, &pl);
-  if (a->workspace_bytes < pl.total_bytes) return MOE_ERR_WORKSPACE;
+  Fp8ActPlan f8{};
+  if (a8) fill_fp8_plan(T, H, I, K, pl.total_bytes, &f8);
+  if (a->workspace_bytes < (a8 ? f8.total_bytes : pl.total_bytes)) return MOE_ERR_WORKSPACE;
   const int64_t n = static_cast<int64_t>(T) * K;
   if (n >= (int64_t(1) << 31) || static_cast<int64_t>(E) * 2 * I >= (int64_t(1) << 31) ||
       static_cast<int64_t>(E) * H >= (int64_t(1) << 31))
@@ -428,7 +498,8 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   // Rows this shard expects (all of them without sharding): the tile width
   // and the shrink variant follow the rows per local expert.
   const int64_t n_local = n * E / R;
-  const int bn = a->tile_n ? a->tile_n : auto_tile_n(static_cast<int>(n_local), E);
+  int bn = a->tile_n ? a->tile_n : auto_tile_n(static_cast<int>(n_local), E);
+  if (a8 && bn > 128) bn = 128;  // the W8A8 epilogue holds a tile row in registers
   // CTA pairs sharing one M = 256 MMA (cta_group::2) for wide tiles; each CTA
   // of a pair loads bn / 2 token rows.  FP8 weights run one CTA per tile.
   bool pair = moe::gemm_use_pair(bn);
@@ -453,10 +524,10 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   // in kernels of their own.
   const bool fuse_shrink = lora && small_permute && bn == 16 && !pair && r <= 32 && !row_blocks &&
                            a->gate_up.a_stride_expert != 0 && tune.shrink_in_gemm == 0 &&
-                           side == nullptr;
+                           side == nullptr && !a8;
   const bool two_streams = lora && side != nullptr;
   // Persistent grid of the expert GEMMs.
-  int gemm_grid = sms * moe::gemm_ctas_per_sm(bn);
+  int gemm_grid = sms * (a8 ? moe::fp8_gemm_ctas_per_sm(bn) : moe::gemm_ctas_per_sm(bn));
   if (tune.gemm_max_ctas > 0) gemm_grid = std::min(gemm_grid, std::max(tune.gemm_max_ctas, pair ? 2 : 1));
   const uint64_t timeout_ns =
       static_cast<uint64_t>(a->wait_timeout_ms ? a->wait_timeout_ms : 2000) * 1000000ull;
@@ -490,6 +561,31 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
     tm_bdn = tm_w2;
     tm_u = tm_xp;
     tm_v = tm_h;
+  }
+  // W8A8: e4m3 weights and token rows, 128-byte rows with 128-byte swizzle
+  uint8_t* xq = a8 ? ws + f8.xq : nullptr;
+  float* xs = a8 ? reinterpret_cast<float*>(ws + f8.xs) : nullptr;
+  float* hf = a8 ? reinterpret_cast<float*>(ws + f8.hf) : nullptr;
+  uint8_t* hq = a8 ? ws + f8.hq : nullptr;
+  float* hs = a8 ? reinterpret_cast<float*>(ws + f8.hs) : nullptr;
+  if (enc && a8) {
+    const uint64_t row = static_cast<uint64_t>(H);
+    const uint64_t d13[5] = {static_cast<uint64_t>(H), 16, 2, static_cast<uint64_t>(I / 16),
+                             static_cast<uint64_t>(E)};
+    const uint64_t s13[4] = {row, row * I, row * 16, row * 2 * I};
+    const uint32_t b13[5] = {128, 16, 2, 4, 1};
+    const uint64_t d2[2] = {static_cast<uint64_t>(I), static_cast<uint64_t>(E) * H};
+    const uint64_t s2[1] = {static_cast<uint64_t>(I)};
+    const uint32_t b2[2] = {128, 128};
+    const uint64_t dxq[2] = {static_cast<uint64_t>(H), static_cast<uint64_t>(n)};
+    const uint64_t sxq[1] = {static_cast<uint64_t>(H)};
+    const uint64_t dhq[2] = {static_cast<uint64_t>(I), static_cast<uint64_t>(n)};
+    const uint64_t shq[1] = {static_cast<uint64_t>(I)};
+    const uint32_t btok[2] = {128, static_cast<uint32_t>(bn)};
+    enc = encode_nd(&tm_w13, a->w13, 5, d13, s13, b13, true, true) &&
+          encode_nd(&tm_w2, a->w2, 2, d2, s2, b2, true, true) &&
+          encode_nd(&tm_xp, xq, 2, dxq, sxq, btok, true, true) &&
+          encode_nd(&tm_h, hq, 2, dhq, shq, btok, true, true);
   }
   if (!enc) return MOE_ERR_CUDA;
 
@@ -583,6 +679,21 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   sp.mapping = lora ? a->token_lora_mapping : nullptr;
   sp.tile_start_rows = tile_start + moe::tile_width_index(moe::rows_shrink_tile()) * (E + 1);
   sp.gmask = fp.gmask;
+  if (a8) {
+    // W8A8: the permuted rows go out quantized (no bf16 copy); the gate_up
+    // shrink reads the bf16 hidden rows through the permutation.
+    moe::QuantParams qp{};
+    qp.x = a->hidden;
+    qp.x_f32 = 0;
+    qp.row_map = p2e;
+    qp.map_div = K;
+    qp.rows = static_cast<int>(n);
+    qp.K = H;
+    qp.codes = xq;
+    qp.scales = xs;
+    if (moe::launch_quant_groups(qp, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    sp.gathered = nullptr;
+  }
   auto launch_shrink = [&](const ShrinkParams& q, cudaStream_t s) {
     return row_blocks && !q.per_token ? moe::launch_rows_shrink(q, static_cast<int>(n), s)
                                       : moe::launch_gather_shrink(q, static_cast<int>(n), s);
@@ -601,7 +712,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
     if (cudaEventRecord(join, side) != cudaSuccess) return MOE_ERR_CUDA;
     if (launch_shrink(sp, stream) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaStreamWaitEvent(stream, join, 0) != cudaSuccess) return MOE_ERR_CUDA;
-  } else if (!fuse_shrink &&  // fused: the gate_up GEMM gathers the rows itself
+  } else if (!fuse_shrink && (!a8 || lora) &&  // fused: the gate_up GEMM gathers the rows itself
              launch_shrink(sp, stream) != cudaSuccess) {
     return MOE_ERR_CUDA;
   }
@@ -633,6 +744,8 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.scale_nb = (2 * I + 127) / 128;
   gp.scale_kb = (H + 127) / 128;
   gp.fuse_shrink = fuse_shrink ? 1 : 0;
+  gp.x_scale = xs;
+  gp.out_f32 = hf;
   if (fuse_shrink) {
     gp.sx = xp;
     gp.gather_src = static_cast<const __nv_bfloat16*>(a->hidden);
@@ -646,10 +759,26 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
     gp.row_counter = flags_gu + moe::shrink_flag_words(static_cast<int>(n), E) - 1;
     for (int i = 0; i < MOE_MAX_ADAPTERS; ++i) gp.sscale[i] = sp.scaling[i];
   }
-  if (moe::launch_expert_gemm(moe::kGateUp, bn, pair, w8, tm_w13, tm_xp, tm_bgu, tm_u, gp, gemm_grid,
-                              stream) != cudaSuccess)
+  if ((a8 ? moe::launch_fp8_gemm(moe::kGateUp, bn, tm_w13, tm_xp, tm_bgu, tm_u, gp, gemm_grid, stream)
+          : moe::launch_expert_gemm(moe::kGateUp, bn, pair, w8, tm_w13, tm_xp, tm_bgu, tm_u, gp, gemm_grid,
+                                    stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!mark()) return MOE_ERR_CUDA;
+  if (a8) {
+    // post-activation quant from the float32 activation, plus the bf16 copy
+    // the down LoRA shrink reads
+    moe::QuantParams qp{};
+    qp.x = hf;
+    qp.x_f32 = 1;
+    qp.row_map = nullptr;
+    qp.map_div = 1;
+    qp.rows = static_cast<int>(n);
+    qp.K = I;
+    qp.codes = hq;
+    qp.scales = hs;
+    qp.copy = h;
+    if (moe::launch_quant_groups(qp, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  }
   // 5. down LoRA shrink: V = s * A_dn h (fused: inside the down GEMM)
   if (lora && !fuse_shrink) {
     sp.X = h;
@@ -693,8 +822,11 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.w_scale = w8 ? a->w2_scale : nullptr;
   gp.scale_nb = (H + 127) / 128;
   gp.scale_kb = (I + 127) / 128;
-  if (moe::launch_expert_gemm(moe::kDown, bn, pair, w8, tm_w2, tm_h, tm_bdn, tm_v, gp, gemm_grid,
-                              stream) != cudaSuccess)
+  gp.x_scale = hs;
+  gp.out_f32 = nullptr;
+  if ((a8 ? moe::launch_fp8_gemm(moe::kDown, bn, tm_w2, tm_h, tm_bdn, tm_v, gp, gemm_grid, stream)
+          : moe::launch_expert_gemm(moe::kDown, bn, pair, w8, tm_w2, tm_h, tm_bdn, tm_v, gp, gemm_grid,
+                                    stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!mark()) return MOE_ERR_CUDA;
   // 7. finalize

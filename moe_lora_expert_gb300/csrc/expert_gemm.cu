@@ -38,12 +38,11 @@
 #include <cuda_runtime.h>
 
 #include "../../include/moe_lora.h"
+#include "gemm_common.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
 
 namespace moe {
-
-constexpr unsigned kFullMask = 0xFFFFFFFFu;
 
 template <int BN, bool PAIR = false, bool W8 = false>
 struct GemmCfg {
@@ -80,94 +79,6 @@ struct GemmCfg {
   static_assert((2 * kStages + 2 * kStages8 + 6) * 8 + 16 <= kMetaBytes, "barriers fit");
   static_assert(kCtasPerSm * (kSmemBytes + 1024) <= 233472, "the CTAs of an SM fit its shared memory");
 };
-
-struct Work {
-  int e, fb, row0, nrows;
-};
-
-// Work unit u = (token tile, feature-block group).  Each CTA of a cluster of
-// CL (a CTA pair: CL = 2) takes feature block group * CL + its rank, so the
-// two CTAs of a pair work on the same token tile at the same time.
-template <int BN>
-__device__ __forceinline__ Work decode_work(int u, int crank, int CL, const int* s_off,
-                                            const int* s_ts, int E, int FBg) {
-  Work wk;
-  const int tile = u / FBg;
-  wk.fb = (u - tile * FBg) * CL + crank;
-  int lo = 0, hi = E - 1;
-  while (lo < hi) {  // largest e with s_ts[e] <= tile
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_ts[mid] <= tile) lo = mid;
-    else hi = mid - 1;
-  }
-  wk.e = lo;
-  wk.row0 = s_off[lo] + (tile - s_ts[lo]) * BN;
-  wk.nrows = min(BN, s_off[lo + 1] - wk.row0);
-  return wk;
-}
-
-// OR of (1 << adapter) over the tile's rows, computed by a whole warp.
-__device__ __forceinline__ uint64_t tile_adapter_mask(const int32_t* row_adapter, int row0,
-                                                      int nrows, int lane) {
-  uint64_t m = 0;
-  for (int i = lane; i < nrows; i += 32) {
-    const int a = __ldcg(row_adapter + row0 + i);
-    if (a >= 0) m |= 1ull << a;
-  }
-  const uint32_t lo = __reduce_or_sync(kFullMask, static_cast<uint32_t>(m));
-  const uint32_t hi = __reduce_or_sync(kFullMask, static_cast<uint32_t>(m >> 32));
-  return (static_cast<uint64_t>(hi) << 32) | lo;
-}
-
-// Bounded wait that also gives up as soon as another role raised the abort flag.
-// CLUSTER: acquire at cluster scope (arrivals come from the peer CTA too).
-template <bool CLUSTER = false>
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
-                                              volatile int* abort_flag) {
-  const uint32_t a = smem_u32(bar);
-  auto probe = [&]() { return CLUSTER ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity); };
-  if (probe()) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-    if (probe()) return true;
-    if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > limit_ns) return false;
-  }
-}
-
-__device__ __forceinline__ void raise_timeout(int* status, volatile int* abort_flag) {
-  set_status(status, MOE_ERR_DEVICE_TIMEOUT);
-  *abort_flag = 1;
-}
-
-// As raise_timeout; the first error also records where in the status detail
-// words: [1] = the wait (kWait*), [2] = (CTA << 8) | warp, [3] = (unit << 16)
-// | (K block << 4) | ring stage.
-enum WaitSite {
-  kWaitProducerW8 = 1, kWaitProducer = 2, kWaitMmaAccEmpty = 4, kWaitMmaFull = 5,
-  kWaitMmaFull8 = 6, kWaitEpilogue = 7, kWaitConvEmpty = 8, kWaitConvFull8 = 9,
-  kWaitDrainProducer = 10, kWaitDrainProducerW8 = 11, kWaitDrainConv = 12, kWaitDrainMma = 13,
-  kWaitShrinkFlag = 14
-};
-
-// A teardown wait that ran out: the status and its place, no abort (the
-// roles have left their loops already).
-__device__ __forceinline__ void note_drain_timeout(int* status, int site, int stage) {
-  if (status != nullptr && atomicCAS(status, 0, MOE_ERR_DEVICE_TIMEOUT) == 0) {
-    status[1] = site;
-    status[2] = static_cast<int>((blockIdx.x << 8) | (threadIdx.x >> 5));
-    status[3] = stage & 15;
-  }
-}
-__device__ __forceinline__ void raise_timeout_at(int* status, volatile int* abort_flag, int site, int unit,
-                                                 int blk, int stage) {
-  if (status != nullptr && atomicCAS(status, 0, MOE_ERR_DEVICE_TIMEOUT) == 0) {
-    status[1] = site;
-    status[2] = static_cast<int>((blockIdx.x << 8) | (threadIdx.x >> 5));
-    status[3] = (unit << 16) | ((blk & 0xFFF) << 4) | (stage & 15);
-  }
-  *abort_flag = 1;
-}
 
 // The LoRA shrink of the permuted rows, by the four epilogue warps (ew =
 // 0..3) before their first accumulator (GemmParams::fuse_shrink).  Rows are
@@ -281,62 +192,6 @@ __device__ __forceinline__ bool wait_tile_rows(const int* flag, int count, uint6
     if (*abort_flag || global_timer_ns() - t0 > limit_ns) return false;
   fence_proxy_async_global();
   return true;
-}
-
-// Weight-side (A operand) loads of one K block: 128 rows of the feature block.
-// gate_up: the map views w13 so that one box (or four, see the host code)
-// brings gate rows 64 fb + 16q + (0..15) to smem rows 32q + (0..15) and the
-// matching up rows to smem rows 32q + 16 + (0..15), q = 0..3.
-// PAIR: the bytes complete on the pair leader's barrier, ``cbar`` (a
-// shared::cluster address); otherwise on this CTA's ``bar``.
-template <bool PAIR>
-__device__ __forceinline__ void load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, uint32_t cbar,
-                                        int c0, int c1, uint64_t pol) {
-  if constexpr (PAIR) tma_load_2d_pair(dst, map, cbar, c0, c1, pol);
-  else tma_load_2d(dst, map, bar, c0, c1, pol);
-}
-
-// ESZ: bytes per weight element (2 bf16, 1 fp8): the smem offset between
-// the four 16-row boxes of the 3-D gate_up view.
-template <int MODE, bool PAIR, int ESZ = 2>
-__device__ __forceinline__ void load_weight_block(uint8_t* sA, const CUtensorMap* map,
-                                                  uint64_t* bar, uint32_t cbar, int kc, int e, int fb,
-                                                  int rows_per_expert, int gu_single_box,
-                                                  uint64_t pol) {
-  if (MODE == kGateUp) {
-    if (gu_single_box) {
-      // map dims {H, 16 rows, 2 halves, I/16 groups, E}
-      if constexpr (PAIR) tma_load_5d_pair(sA, map, cbar, kc, 0, 0, fb * 4, e, pol);
-      else tma_load_5d(sA, map, bar, kc, 0, 0, fb * 4, e, pol);
-    } else {
-      // map dims {H, I, 2E}, box {64, 16, 2}
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if constexpr (PAIR) tma_load_3d_pair(sA + q * 2048 * ESZ, map, cbar, kc, fb * 64 + q * 16, 2 * e, pol);
-        else tma_load_3d(sA + q * 2048 * ESZ, map, bar, kc, fb * 64 + q * 16, 2 * e, pol);
-      }
-    }
-  } else {
-    load_2d<PAIR>(sA, map, bar, cbar, kc, e * rows_per_expert + fb * 128, pol);
-  }
-}
-
-// LoRA B-factor (A operand of the expand) loads: same row arrangement, from
-// the 2-D map over all factor rows (box {64, 16} for gate_up, {64, 128} down).
-template <int MODE, bool PAIR>
-__device__ __forceinline__ void load_lora_b_block(uint8_t* sA, const CUtensorMap* map,
-                                                  uint64_t* bar, uint32_t cbar, int kc, int64_t row_base,
-                                                  int fb, int n_feat, uint64_t pol) {
-  if (MODE == kGateUp) {
-#pragma unroll
-    for (int bx = 0; bx < 8; ++bx) {
-      const int q = bx >> 1, up = bx & 1;
-      const int64_t row = row_base + static_cast<int64_t>(up) * n_feat + fb * 64 + q * 16;
-      load_2d<PAIR>(sA + bx * 2048, map, bar, cbar, kc, static_cast<int>(row), pol);
-    }
-  } else {
-    load_2d<PAIR>(sA, map, bar, cbar, kc, static_cast<int>(row_base + fb * 128), pol);
-  }
 }
 
 // PAIR (CL == 2): the two CTAs of the cluster take adjacent feature blocks

@@ -210,6 +210,11 @@ struct GemmParams {
   __nv_bfloat16* su;                   // [n, num_adapters * rank]
   int* tile_flags;                     // [tiles of this width]
   int* row_counter;                    // next unclaimed permuted row (zeroed by the permute)
+  // FP8 activations (fp8_gemm_kernel): token-row scales [n, ceil(K / 128)]
+  // of the e4m3 token operand, and (gate_up) the float32 activation output
+  // [n, n_feat] for the post-activation quant.
+  const float* x_scale;
+  float* out_f32;
   float sscale[MOE_MAX_ADAPTERS];      // per adapter
 };
 enum GemmMode { kGateUp = 0, kDown = 1 };
@@ -225,6 +230,33 @@ cudaError_t launch_expert_gemm(int mode, int bn, bool pair, bool w8, const CUten
                                const CUtensorMap& tm_x, const CUtensorMap& tm_lb,
                                const CUtensorMap& tm_lu, const GemmParams& p, int grid,
                                cudaStream_t s);
+
+// ------------------------------------------------ FP8 activations (W8A8)
+// Per row and group of kActGroup columns, float32: scale = max(amax, kActEps)
+// / kE4m3Max, code = e4m3(x / scale) (nearest even, saturating).
+constexpr int kActGroup = 128;
+constexpr float kActEps = 1e-10f;
+constexpr float kE4m3Max = 448.0f;
+struct QuantParams {
+  const void* x;                // source rows [*, K]: bf16 (x_f32 = 0) or float32
+  int x_f32;
+  const int32_t* row_map;       // or null: output row i reads source row row_map[i] / map_div
+  int map_div;                  //   (row_map[i] < 0: a zero row)
+  int rows;
+  int K;                        // a multiple of 16
+  uint8_t* codes;               // [rows, K]
+  float* scales;                // [rows, ceil(K / kActGroup)]
+  __nv_bfloat16* copy;          // or null: bf16 copy of each (float32) source row
+};
+cudaError_t launch_quant_groups(const QuantParams& p, cudaStream_t s);
+// W8A8 expert GEMM: e4m3 weights (tm_w: 1-byte views with 128-byte swizzle,
+// box {128, 16, 2, 4, 1} for gate_up, {128, 128} for down) and e4m3 token
+// rows (tm_x, box {128, bn}); p.w_scale, p.x_scale set; gate_up writes the
+// float32 activation to p.out_f32, down writes bf16 y to p.out.  bn <= 128.
+int fp8_gemm_ctas_per_sm(int bn);
+cudaError_t launch_fp8_gemm(int mode, int bn, const CUtensorMap& tm_w, const CUtensorMap& tm_x,
+                            const CUtensorMap& tm_lb, const CUtensorMap& tm_lu, const GemmParams& p, int grid,
+                            cudaStream_t s);
 
 // --------------------------------------------------------------- finalize
 cudaError_t launch_finalize(const __nv_bfloat16* y, const int32_t* e2p, const float* w, int T,

@@ -276,6 +276,35 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24);// M / 16
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, float8 e4m3 inputs (32 K elements per
+// instruction), fp32 accumulate.
+__device__ __forceinline__ void tc_mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor for kind::f8f6f4: e4m3 A and B (both K-major; the
+// e4m3 type code is 0), fp32 D, shape M x N.
+__host__ __device__ constexpr uint32_t make_idesc_e4m3(int M, int N) {
+  return (1u << 4)                               // D format: f32
+         | (static_cast<uint32_t>(N >> 3) << 17) // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);// M / 16
+}
+
+// Two float32 values to two float8 e4m3 codes, round to nearest (ties to
+// even), magnitudes beyond the largest finite value (448) saturate to it.
+// ``lo`` lands in the low byte, ``hi`` in the high byte.
+__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // Shared-memory matrix descriptor for a K-major operand laid out by TMA with
 // 128-byte swizzle: rows of 128 bytes (64 bf16 along K), 8-row groups 1024
 // bytes apart.  The tile base must be 1024-byte aligned; stepping along K

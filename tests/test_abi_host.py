@@ -182,6 +182,14 @@ def _valid_args(**over):
      m.MOE_ERR_NULL),
     # the two-stream schedule needs both events
     ({"side_stream": 1 << 12}, m.MOE_ERR_NULL),
+    # FP8 activations: a known format, FP8 weights, the larger workspace
+    ({"activation_format": 2}, m.MOE_ERR_UNSUPPORTED),
+    ({"activation_format": m.MOE_ACT_FP8_E4M3_G128}, m.MOE_ERR_UNSUPPORTED),   # bf16 weights
+    ({"activation_format": m.MOE_ACT_FP8_E4M3_G128, "weight_format": m.MOE_WEIGHTS_FP8_E4M3_B128,
+      "w13_scale": 1 << 20, "w2_scale": 1 << 20}, m.MOE_ERR_WORKSPACE),    # bf16-sized workspace
+    # a structure from before activation_format ignores it (checks go on)
+    ({"struct_size": m.MoeLoraArgs.activation_format.offset, "activation_format": 2, "hidden": None},
+     m.MOE_ERR_NULL),
 ])
 def test_forward_rejects_on_host(lib, over, status):
     a = _valid_args(**over)
@@ -215,3 +223,21 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(m, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         m.lib()
+
+
+def test_fp8_workspace_and_quant_host_checks(lib):
+    base = lib.moe_lora_workspace_size(16, 2048, 768, 128, 8, 4, 16)
+    assert lib.moe_lora_workspace_size_ex(16, 2048, 768, 128, 8, 4, 16, m.MOE_ACT_BF16) == base
+    n = 16 * 8
+    extra = lib.moe_lora_workspace_size_ex(16, 2048, 768, 128, 8, 4, 16, m.MOE_ACT_FP8_E4M3_G128) - base
+    # quantized rows, their scales, the float32 activation, its codes and scales
+    assert extra >= n * 2048 + n * 16 * 4 + n * 768 * 4 + n * 768 + n * 6 * 4
+    assert lib.moe_lora_workspace_size_ex(16, 2048, 768, 128, 8, 4, 16, 7) == 0
+    fake = 1 << 20
+    q = lib.moe_per_token_group_quant_fp8
+    assert q(fake, 0, 4, 24, None, 1, fake, fake, None) == m.MOE_ERR_ALIGN       # K % 16
+    assert q(fake, 2, 4, 32, None, 1, fake, fake, None) == m.MOE_ERR_SHAPE       # x type flag
+    assert q(fake, 0, 4, 32, None, 0, fake, fake, None) == m.MOE_ERR_SHAPE       # map_div
+    assert q(None, 0, 4, 32, None, 1, fake, fake, None) == m.MOE_ERR_NULL
+    assert q(fake + 8, 0, 4, 32, None, 1, fake, fake, None) == m.MOE_ERR_ALIGN
+    assert q(None, 0, 0, 32, None, 1, None, None, None) == m.MOE_OK              # nothing to do
