@@ -53,9 +53,16 @@ struct GemmCfg {
   static constexpr int kConvWarps = 4;
   static constexpr int kThreads = W8 ? 192 + 32 * kConvWarps : 192;
   static constexpr int kStageBudget = BN <= 64 ? (W8 ? 104 : 96) * 1024 : 200 * 1024;
-  static constexpr int kABytes = 128 * 64 * 2;   // 128 rows x 64 K of bf16
+  // 64-K sub-blocks per ring stage.  The MMA role commits once per stage
+  // (that releases it to the producer), and on sm_103a each commit costs
+  // about as much as a few MMAs, so wide tiles take two sub-blocks (eight
+  // MMAs per commit).  FP8 weights keep one.
+  static constexpr int kKSub = W8 ? 1 : (BN >= 128 ? 2 : 1);
+  static constexpr int kASub = 128 * 64 * 2;     // 128 rows x 64 K of bf16
   // A CTA of a pair holds half of the token tile.
-  static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * 64 * 2;
+  static constexpr int kBSub = (PAIR ? BN / 2 : BN) * 64 * 2;
+  static constexpr int kABytes = kKSub * kASub;
+  static constexpr int kBBytes = kKSub * kBSub;
   static constexpr int kStageBytes = kABytes + kBBytes;
   // FP8: a deep ring of (raw 128 x 64 e4m3 weight tile, token tile) stages
   // filled by TMA; the converter warps write the bf16 A tiles into a short
@@ -239,8 +246,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool use_lora = p.num_adapters > 0 && p.rank > 0;
-  const int nk = (p.K + 63) / 64;
-  const int lkb = (p.rank + 63) / 64;  // K blocks per adapter of the LoRA expand
+  constexpr int kBlockK = 64 * C::kKSub;  // K elements per ring stage
+  const int nk = (p.K + kBlockK - 1) / kBlockK;
+  const int lkb = (p.rank + kBlockK - 1) / kBlockK;  // K blocks per adapter of the LoRA expand
+  // 64-K sub-blocks of block b that hold any K (the rest are neither loaded
+  // nor multiplied); j: the block's index within its adapter's LoRA blocks
+  auto subs_of = [&](int b, int j) {
+    const int left = b < nk ? p.K - b * kBlockK : p.rank - j * kBlockK;
+    return min(C::kKSub, (left + 63) / 64);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages8; ++s) {
@@ -406,11 +420,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
     // previous kernel has completed (griddepcontrol.wait).
     bool waited = !p.tables_ready;
     int n_pend = 0;
-    const CUtensorMap* pend_map[C::kStages];
-    int pend_c0[C::kStages], pend_c1[C::kStages], pend_stage[C::kStages];
-    // Pair: c1 already names this CTA's half of the token tile.
-    auto issue_token_load = [&](const CUtensorMap* map, int st, int c0, int c1) {
-      uint8_t* sB = smem + st * C::kStageBytes + C::kABytes;
+    constexpr int kPend = C::kStages * C::kKSub;
+    const CUtensorMap* pend_map[kPend];
+    int pend_c0[kPend], pend_c1[kPend], pend_stage[kPend];
+    // Pair: c1 already names this CTA's half of the token tile.  c0 is the
+    // sub-block's first K element; st * kKSub + sub names stage and sub-block.
+    auto issue_token_load = [&](const CUtensorMap* map, int st_sub, int c0, int c1) {
+      const int st = st_sub / C::kKSub, sub = st_sub % C::kKSub;
+      uint8_t* sB = smem + st * C::kStageBytes + C::kABytes + sub * C::kBSub;
       if constexpr (PAIR)
         tma_load_2d_pair(sB, map, mapa_shared(smem_u32(&full[st]), 0), c0, c1, pol_x);
       else
@@ -447,34 +464,43 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
         if (lane == 0 && ok) {
           ok = wait_or_abort<PAIR>(&empty[stage], phase ^ 1, p.timeout_ns, abort_flag);
           if (ok) {
-            uint8_t* sA = smem + stage * C::kStageBytes;
+            const int nsub = subs_of(b, j);
             // the pair leader counts the bytes of both CTAs
-            if (leader) mbar_arrive_expect_tx(&full[stage], (PAIR ? 2 : 1) * C::kStageBytes);
+            if (leader)
+              mbar_arrive_expect_tx(&full[stage], (PAIR ? 2 : 1) * nsub * (C::kASub + C::kBSub));
             const uint32_t cbar = PAIR ? mapa_shared(smem_u32(&full[stage]), 0) : 0u;
-            const CUtensorMap* tmap;
-            int tc0;
-            if (b < nk) {
-              load_weight_block<MODE, PAIR>(sA, &tm_w, &full[stage], cbar, b * 64, wk.e, wk.fb,
-                                            p.rows_per_expert, p.gu_single_box, pol_w);
-              tmap = &tm_x;
-              tc0 = b * 64;
-            } else {
-              const int64_t frow = static_cast<int64_t>(adapter) * p.lb_row_stride_adapter +
-                                   static_cast<int64_t>(wk.e) * p.lb_row_stride_expert;
-              load_lora_b_block<MODE, PAIR>(sA, &tm_lb, &full[stage], cbar, j * 64, frow, wk.fb,
-                                            p.n_feat, pol_x);
-              tmap = &tm_lu;
-              tc0 = adapter * p.rank + j * 64;
+            for (int sub = 0; sub < nsub; ++sub) {
+              uint8_t* sA = smem + stage * C::kStageBytes + sub * C::kASub;
+              const CUtensorMap* tmap;
+              int tc0;
+              if (b < nk) {
+                const int kc = b * kBlockK + sub * 64;
+                load_weight_block<MODE, PAIR>(sA, &tm_w, &full[stage], cbar, kc, wk.e, wk.fb,
+                                              p.rows_per_expert, p.gu_single_box, pol_w);
+                tmap = &tm_x;
+                tc0 = kc;
+              } else {
+                const int kc = j * kBlockK + sub * 64;
+                const int64_t frow = static_cast<int64_t>(adapter) * p.lb_row_stride_adapter +
+                                     static_cast<int64_t>(wk.e) * p.lb_row_stride_expert;
+                load_lora_b_block<MODE, PAIR>(sA, &tm_lb, &full[stage], cbar, kc, frow, wk.fb,
+                                              p.n_feat, pol_x);
+                tmap = &tm_lu;
+                tc0 = adapter * p.rank + kc;
+              }
+              const int st_sub = stage * C::kKSub + sub;
+              if (waited) {
+                issue_token_load(tmap, st_sub, tc0, trow);
+              } else {
+                pend_map[n_pend] = tmap;
+                pend_c0[n_pend] = tc0;
+                pend_c1[n_pend] = trow;
+                pend_stage[n_pend] = st_sub;
+                ++n_pend;
+              }
             }
-            if (waited) {
-              issue_token_load(tmap, stage, tc0, trow);
-            } else {
-              pend_map[n_pend] = tmap;
-              pend_c0[n_pend] = tc0;
-              pend_c1[n_pend] = trow;
-              pend_stage[n_pend] = stage;
-              if (++n_pend == C::kStages) release_pending();
-            }
+            // before the ring wraps onto a stage whose token loads still wait
+            if (!waited && stage == C::kStages - 1) release_pending();
             armed |= 1u << stage;
             armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           } else {
@@ -543,24 +569,26 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
           }
           if (ok) {
             tc_fence_after_sync();
-            const uint32_t a_addr =
+            const uint32_t a_base =
                 smem_u32(smem + stage * (W8 ? C::kABytes : C::kStageBytes));
-            const uint32_t b_addr =
-                W8 ? smem_u32(w8ring + s8 * C::kW8Stage + C::kW8Bytes) : a_addr + C::kABytes;
-            const uint64_t adesc = make_sdesc_sw128(a_addr);
-            const uint64_t bdesc = make_sdesc_sw128(b_addr);
-            int ksteps = 4;
-            if (b >= nk) {
-              const int rem = p.rank - j * 64;
-              ksteps = rem >= 64 ? 4 : (rem + 15) / 16;
-            }
-            for (int ks = 0; ks < ksteps; ++ks) {
-              if constexpr (PAIR)
-                tc_mma_bf16_pair(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc,
-                                 (b > 0 || ks > 0) ? 1u : 0u);
-              else
-                tc_mma_bf16(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc,
-                            (b > 0 || ks > 0) ? 1u : 0u);
+            const uint32_t b_base =
+                W8 ? smem_u32(w8ring + s8 * C::kW8Stage + C::kW8Bytes) : a_base + C::kABytes;
+            const int nsub = subs_of(b, j);
+            for (int sub = 0; sub < nsub; ++sub) {
+              const uint64_t adesc = make_sdesc_sw128(a_base + sub * C::kASub);
+              const uint64_t bdesc = make_sdesc_sw128(b_base + sub * C::kBSub);
+              int ksteps = 4;
+              if (b >= nk) {
+                const int rem = p.rank - j * kBlockK - sub * 64;
+                ksteps = rem >= 64 ? 4 : (rem + 15) / 16;
+              }
+              for (int ks = 0; ks < ksteps; ++ks) {
+                const uint32_t accum = (b > 0 || sub > 0 || ks > 0) ? 1u : 0u;
+                if constexpr (PAIR)
+                  tc_mma_bf16_pair(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc, accum);
+                else
+                  tc_mma_bf16(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc, accum);
+              }
             }
             if constexpr (PAIR) tc_commit_pair(&empty[stage], 0x3);
             else tc_commit(&empty[stage]);
