@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
     for (int w = unit0; w < total_work && ok; w += unit_step) {
       if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
       const Work wk = decode_work<BN>(w, crank, CL, s_off, s_ts, p.E, FBg);
-      uint64_t amask = use_lora ? tile_adapter_mask(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
+      uint64_t amask = use_lora ? tile_adapter_mask<BN>(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
       const int nblocks = nk + __popcll(amask) * lkb;
       int adapter = -1, j = 0;
       for (int b = 0; b < nblocks; ++b) {
@@ -442,7 +442,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
     for (int w = unit0; w < total_work && ok; w += unit_step) {
       if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
       const Work wk = decode_work<BN>(w, crank, CL, s_off, s_ts, p.E, FBg);
-      uint64_t amask = use_lora ? tile_adapter_mask(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
+      uint64_t amask = use_lora ? tile_adapter_mask<BN>(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
       const int nblocks = nk + __popcll(amask) * lkb;
       // first token row this CTA loads: a pair splits the MMA's N in halves
       const int trow = PAIR ? wk.row0 + crank * (((wk.nrows + 31) / 32) * 16) : wk.row0;
@@ -541,11 +541,21 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
         raise_timeout(p.status, abort_flag);
       ok = false;
     }
+    // The next unit's row adapters are loaded while this unit's MMAs issue,
+    // so the mask costs the MMA role no round trip between units.
+    TileAdapters<BN> next_ad;
+    if (use_lora && unit0 < total_work) {
+      const Work w0 = decode_work<BN>(unit0, crank, CL, s_off, s_ts, p.E, FBg);
+      load_tile_adapters<BN>(p.row_adapter, w0.row0, w0.nrows, lane, next_ad);
+    }
     for (int w = unit0; w < total_work && ok; w += unit_step) {
       if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
       const Work wk = decode_work<BN>(w, crank, CL, s_off, s_ts, p.E, FBg);
-      const uint64_t amask =
-          use_lora ? tile_adapter_mask(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
+      const uint64_t amask = use_lora ? reduce_tile_adapters<BN>(next_ad) : 0;
+      if (use_lora && w + unit_step < total_work) {
+        const Work wn = decode_work<BN>(w + unit_step, crank, CL, s_off, s_ts, p.E, FBg);
+        load_tile_adapters<BN>(p.row_adapter, wn.row0, wn.nrows, lane, next_ad);
+      }
       const int nblocks = nk + __popcll(amask) * lkb;
       // a pair's N is split in halves of 16-row multiples
       const int ncols = PAIR ? ((wk.nrows + 31) / 32) * 32 : ((wk.nrows + 15) / 16) * 16;
@@ -558,57 +568,57 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
       if (!ok) break;
       tc_fence_after_sync();
       const uint32_t d_tmem = tmem_base + acc * BN;
-      int j = 0;
-      for (int b = 0; b < nblocks; ++b) {
-        if (lane == 0) {
+      // The unit's K loop runs in lane 0 alone: no warp-wide exchange per
+      // block between the MMA issues.
+      if (lane == 0) {
+        int j = 0;
+        for (int b = 0; b < nblocks; ++b) {
           ok = wait_or_abort<PAIR>(&full[stage], phase, p.timeout_ns, abort_flag);
           int site = kWaitMmaFull;
           if (W8 && ok) {
             ok = wait_or_abort(&full8[s8], ph8, p.timeout_ns, abort_flag);
             site = kWaitMmaFull8;
           }
-          if (ok) {
-            tc_fence_after_sync();
-            const uint32_t a_base =
-                smem_u32(smem + stage * (W8 ? C::kABytes : C::kStageBytes));
-            const uint32_t b_base =
-                W8 ? smem_u32(w8ring + s8 * C::kW8Stage + C::kW8Bytes) : a_base + C::kABytes;
-            const int nsub = subs_of(b, j);
-            for (int sub = 0; sub < nsub; ++sub) {
-              const uint64_t adesc = make_sdesc_sw128(a_base + sub * C::kASub);
-              const uint64_t bdesc = make_sdesc_sw128(b_base + sub * C::kBSub);
-              int ksteps = 4;
-              if (b >= nk) {
-                const int rem = p.rank - j * kBlockK - sub * 64;
-                ksteps = rem >= 64 ? 4 : (rem + 15) / 16;
-              }
-              for (int ks = 0; ks < ksteps; ++ks) {
-                const uint32_t accum = (b > 0 || sub > 0 || ks > 0) ? 1u : 0u;
-                if constexpr (PAIR)
-                  tc_mma_bf16_pair(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc, accum);
-                else
-                  tc_mma_bf16(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc, accum);
-              }
-            }
-            if constexpr (PAIR) tc_commit_pair(&empty[stage], 0x3);
-            else tc_commit(&empty[stage]);
-            if constexpr (W8) tc_commit(&empty8[s8]);
-          } else {
+          if (!ok) {
             raise_timeout_at(p.status, abort_flag, site, w, b, site == kWaitMmaFull8 ? s8 : stage);
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a_base = smem_u32(smem + stage * (W8 ? C::kABytes : C::kStageBytes));
+          const uint32_t b_base =
+              W8 ? smem_u32(w8ring + s8 * C::kW8Stage + C::kW8Bytes) : a_base + C::kABytes;
+          const int nsub = subs_of(b, j);
+          for (int sub = 0; sub < nsub; ++sub) {
+            const uint64_t adesc = make_sdesc_sw128(a_base + sub * C::kASub);
+            const uint64_t bdesc = make_sdesc_sw128(b_base + sub * C::kBSub);
+            int ksteps = 4;
+            if (b >= nk) {
+              const int rem = p.rank - j * kBlockK - sub * 64;
+              ksteps = rem >= 64 ? 4 : (rem + 15) / 16;
+            }
+            for (int ks = 0; ks < ksteps; ++ks) {
+              const uint32_t accum = (b > 0 || sub > 0 || ks > 0) ? 1u : 0u;
+              if constexpr (PAIR)
+                tc_mma_bf16_pair(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc, accum);
+              else
+                tc_mma_bf16(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc, accum);
+            }
+          }
+          if constexpr (PAIR) tc_commit_pair(&empty[stage], 0x3);
+          else tc_commit(&empty[stage]);
+          if constexpr (W8) tc_commit(&empty8[s8]);
+          if (b >= nk) j = (j + 1 == lkb) ? 0 : j + 1;
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+          if (W8 && ++s8 == C::kStages8) {
+            s8 = 0;
+            ph8 ^= 1;
           }
         }
-        ok = __shfl_sync(kFullMask, ok, 0);
-        if (!ok) break;
-        if (b >= nk) j = (j + 1 == lkb) ? 0 : j + 1;
-        if (++stage == C::kStages) {
-          stage = 0;
-          phase ^= 1;
-        }
-        if (W8 && ++s8 == C::kStages8) {
-          s8 = 0;
-          ph8 ^= 1;
-        }
       }
+      ok = __shfl_sync(kFullMask, ok, 0);
       if (!ok) break;
       if (lane == 0) {
         if constexpr (PAIR) tc_commit_pair(&accf[acc], 0x3);
@@ -720,7 +730,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
     for (int w = unit0; w < total_work && ok; w += unit_step) {
       if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
       const Work wk = decode_work<BN>(w, crank, CL, s_off, s_ts, p.E, FBg);
-      uint64_t amask = use_lora ? tile_adapter_mask(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
+      uint64_t amask = use_lora ? tile_adapter_mask<BN>(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
       const int nblocks = nk + __popcll(amask) * lkb;
       int adapter = -1, j = 0;
       for (int b = 0; b < nblocks; ++b) {

@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(Fp8Cfg<BN>::kThreads, Fp8Cfg<BN>::kCtasPerSm)
     for (int w = blockIdx.x; w < total_work && ok; w += gridDim.x) {
       if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
       const Work wk = decode_work<BN>(w, 0, 1, s_off, s_ts, p.E, FBg);
-      uint64_t amask = use_lora ? tile_adapter_mask(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
+      uint64_t amask = use_lora ? tile_adapter_mask<BN>(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
       const int nblocks = nk + __popcll(amask) * lkb;
       int adapter = -1, j = 0;
       for (int b = 0; b < nblocks; ++b) {
@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(Fp8Cfg<BN>::kThreads, Fp8Cfg<BN>::kCtasPerSm)
     for (int w = blockIdx.x; w < total_work && ok; w += gridDim.x) {
       if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
       const Work wk = decode_work<BN>(w, 0, 1, s_off, s_ts, p.E, FBg);
-      const uint64_t amask = use_lora ? tile_adapter_mask(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
+      const uint64_t amask = use_lora ? tile_adapter_mask<BN>(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
       const int nblocks = nk + __popcll(amask) * lkb;
       const int ncols = ((wk.nrows + 15) / 16) * 16;
       const uint32_t idesc8 = make_idesc_e4m3(128, ncols);
@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(Fp8Cfg<BN>::kThreads, Fp8Cfg<BN>::kCtasPerSm)
     for (int w = blockIdx.x; w < total_work; w += gridDim.x) {
       if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
       const Work wk = decode_work<BN>(w, 0, 1, s_off, s_ts, p.E, FBg);
-      const uint64_t amask = use_lora ? tile_adapter_mask(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
+      const uint64_t amask = use_lora ? tile_adapter_mask<BN>(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
       const int nblocks = nk + __popcll(amask) * lkb;
       const int ncols = ((wk.nrows + 15) / 16) * 16;
       // the weight row behind this thread's lane, and its scale row

@@ -40,17 +40,43 @@ __device__ __forceinline__ Work decode_work(int u, int crank, int CL, const int*
   return wk;
 }
 
-// OR of (1 << adapter) over the tile's rows, computed by a whole warp.
-__device__ __forceinline__ uint64_t tile_adapter_mask(const int32_t* row_adapter, int row0,
-                                                      int nrows, int lane) {
-  uint64_t m = 0;
-  for (int i = lane; i < nrows; i += 32) {
-    const int a = __ldcg(row_adapter + row0 + i);
-    if (a >= 0) m |= 1ull << a;
+// The adapter mask of a token tile: OR of (1 << adapter) over its rows,
+// computed by a whole warp.  The loads of a tile's (at most BN) row adapters
+// are issued together, BN / 32 per lane, so the mask costs one round trip to
+// L2; load_tile_adapters and reduce_tile_adapters split it so that the loads
+// can be in flight while the warp does other work.
+template <int BN>
+struct TileAdapters {
+  int v[(BN + 31) / 32];
+};
+
+template <int BN>
+__device__ __forceinline__ void load_tile_adapters(const int32_t* row_adapter, int row0, int nrows, int lane,
+                                                   TileAdapters<BN>& t) {
+#pragma unroll
+  for (int i = 0; i < (BN + 31) / 32; ++i) {
+    const int r = lane + 32 * i;
+    t.v[i] = r < nrows ? __ldcg(row_adapter + row0 + r) : -1;
   }
+}
+
+template <int BN>
+__device__ __forceinline__ uint64_t reduce_tile_adapters(const TileAdapters<BN>& t) {
+  uint64_t m = 0;
+#pragma unroll
+  for (int i = 0; i < (BN + 31) / 32; ++i)
+    if (t.v[i] >= 0) m |= 1ull << t.v[i];
   const uint32_t lo = __reduce_or_sync(kFullMask, static_cast<uint32_t>(m));
   const uint32_t hi = __reduce_or_sync(kFullMask, static_cast<uint32_t>(m >> 32));
   return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+template <int BN>
+__device__ __forceinline__ uint64_t tile_adapter_mask(const int32_t* row_adapter, int row0, int nrows,
+                                                      int lane) {
+  TileAdapters<BN> t;
+  load_tile_adapters<BN>(row_adapter, row0, nrows, lane, t);
+  return reduce_tile_adapters<BN>(t);
 }
 
 // Bounded wait that also gives up as soon as another role raised the abort flag.
