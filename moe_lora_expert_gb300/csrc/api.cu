@@ -587,6 +587,14 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
           encode_nd(&tm_xp, xq, 2, dxq, sxq, btok, true, true) &&
           encode_nd(&tm_h, hq, 2, dhq, shq, btok, true, true);
   }
+  // Wide bf16 tiles: token maps with 32-row boxes for tiles of few rows
+  CUtensorMap tm_xp_s = tm_xp, tm_h_s = tm_h, tm_u_s = tm_u, tm_v_s = tm_v;
+  if (enc && tok_box > 32 && !w8) {
+    enc = encode_2d(&tm_xp_s, xp, H, n, H * 2ull, 64, 32) && encode_2d(&tm_h_s, h, I, n, I * 2ull, 64, 32);
+    if (enc && lora)
+      enc = encode_2d(&tm_u_s, U, static_cast<uint64_t>(A) * r, n, A * r * 2ull, 64, 32) &&
+            encode_2d(&tm_v_s, V, static_cast<uint64_t>(A) * r, n, A * r * 2ull, 64, 32);
+  }
   if (!enc) return MOE_ERR_CUDA;
 
   if (!mark()) return MOE_ERR_CUDA;
@@ -760,8 +768,8 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
     for (int i = 0; i < MOE_MAX_ADAPTERS; ++i) gp.sscale[i] = sp.scaling[i];
   }
   if ((a8 ? moe::launch_fp8_gemm(moe::kGateUp, bn, tm_w13, tm_xp, tm_bgu, tm_u, gp, gemm_grid, stream)
-          : moe::launch_expert_gemm(moe::kGateUp, bn, pair, w8, tm_w13, tm_xp, tm_bgu, tm_u, gp, gemm_grid,
-                                    stream)) != cudaSuccess)
+          : moe::launch_expert_gemm(moe::kGateUp, bn, pair, w8, tm_w13, tm_xp, tm_bgu, tm_u, tm_xp_s, tm_u_s, gp,
+                                    gemm_grid, stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!mark()) return MOE_ERR_CUDA;
   if (a8) {
@@ -825,8 +833,8 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.x_scale = hs;
   gp.out_f32 = nullptr;
   if ((a8 ? moe::launch_fp8_gemm(moe::kDown, bn, tm_w2, tm_h, tm_bdn, tm_v, gp, gemm_grid, stream)
-          : moe::launch_expert_gemm(moe::kDown, bn, pair, w8, tm_w2, tm_h, tm_bdn, tm_v, gp, gemm_grid,
-                                    stream)) != cudaSuccess)
+          : moe::launch_expert_gemm(moe::kDown, bn, pair, w8, tm_w2, tm_h, tm_bdn, tm_v, tm_h_s, tm_v_s, gp,
+                                    gemm_grid, stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!mark()) return MOE_ERR_CUDA;
   // 7. finalize

@@ -61,6 +61,10 @@ struct GemmCfg {
   static constexpr int kASub = 128 * 64 * 2;     // 128 rows x 64 K of bf16
   // A CTA of a pair holds half of the token tile.
   static constexpr int kBSub = (PAIR ? BN / 2 : BN) * 64 * 2;
+  // Tiles of a few rows (an expert's last, nearly empty tile) load their
+  // token rows through a second tensor map whose box is kSmallRows high.
+  static constexpr int kSmallRows = 32;
+  static constexpr int kBSubSmall = kSmallRows * 64 * 2;
   static constexpr int kABytes = kKSub * kASub;
   static constexpr int kBBytes = kKSub * kBSub;
   static constexpr int kStageBytes = kABytes + kBBytes;
@@ -77,13 +81,19 @@ struct GemmCfg {
   static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr int kMetaBytes = 512;                         // barriers, flags
   static constexpr int kTableBytes = 2 * (MOE_MAX_EXPERTS + 1) * 4;
+  // Per-unit descriptors (K blocks, MMA width) that the producer publishes
+  // for the MMA role: a ring of more entries than there are stages, so the
+  // producer (at most kStages stages ahead) never overwrites one in use.
+  static constexpr int kUnitRing = 32;
+  static constexpr int kUnitBytes = kUnitRing * 8;
   // Epilogue: a 1 KB staging tile per epilogue warp (16 token columns of its
   // features), so the output leaves in 16-byte row segments.
-  static constexpr int kEpiOffset = (kMetaBytes + kTableBytes + 15) / 16 * 16;
+  static constexpr int kEpiOffset = (kMetaBytes + kTableBytes + kUnitBytes + 15) / 16 * 16;
   static constexpr int kEpiBytes = 4 * 1024;
   static constexpr int kSmemBytes =
       1024 + kARingBytes + kStages8 * kW8Stage + kEpiOffset + kEpiBytes;
   static_assert((2 * kStages + 2 * kStages8 + 6) * 8 + 16 <= kMetaBytes, "barriers fit");
+  static_assert(kUnitRing > kStages, "a unit has at least one stage");
   static_assert(kCtasPerSm * (kSmemBytes + 1024) <= 233472, "the CTAs of an SM fit its shared memory");
 };
 
@@ -221,6 +231,7 @@ template <int BN, int MODE, int CL, bool PAIR, bool W8>
 __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, PAIR, W8>::kCtasPerSm)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                        const __grid_constant__ CUtensorMap tm_lb, const __grid_constant__ CUtensorMap tm_lu,
+                       const __grid_constant__ CUtensorMap tm_xs, const __grid_constant__ CUtensorMap tm_lus,
                        const GemmParams p) {
   static_assert(PAIR == (CL == 2) && CL <= 2, "one CTA per tile, or a pair (a cluster of two)");
   static_assert(!W8 || (CL == 1 && !PAIR), "FP8 weights: one CTA per tile");
@@ -242,6 +253,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_off = reinterpret_cast<int*>(meta + C::kMetaBytes);
   int* s_ts = s_off + (MOE_MAX_EXPERTS + 1);
+  int2* s_units = reinterpret_cast<int2*>(meta + C::kMetaBytes + C::kTableBytes);
   uint8_t* s_epi = meta + C::kEpiOffset;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -439,13 +451,34 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
       for (int i = 0; i < n_pend; ++i) issue_token_load(pend_map[i], pend_stage[i], pend_c0[i], pend_c1[i]);
       n_pend = 0;
     };
-    for (int w = unit0; w < total_work && ok; w += unit_step) {
+    // The next unit's tile and row adapters are worked out while this unit's
+    // loads go out, so no gap opens in the load stream between units.
+    Work next_wk{};
+    TileAdapters<BN> next_ad;
+    if (unit0 < total_work) {
+      next_wk = decode_work<BN>(unit0, crank, CL, s_off, s_ts, p.E, FBg);
+      if (use_lora) load_tile_adapters<BN>(p.row_adapter, next_wk.row0, next_wk.nrows, lane, next_ad);
+    }
+    for (int w = unit0, ul = 0; w < total_work && ok; w += unit_step, ++ul) {
       if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
-      const Work wk = decode_work<BN>(w, crank, CL, s_off, s_ts, p.E, FBg);
-      uint64_t amask = use_lora ? tile_adapter_mask<BN>(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
+      const Work wk = next_wk;
+      uint64_t amask = use_lora ? reduce_tile_adapters<BN>(next_ad) : 0;
+      if (w + unit_step < total_work) {
+        next_wk = decode_work<BN>(w + unit_step, crank, CL, s_off, s_ts, p.E, FBg);
+        if (use_lora) load_tile_adapters<BN>(p.row_adapter, next_wk.row0, next_wk.nrows, lane, next_ad);
+      }
       const int nblocks = nk + __popcll(amask) * lkb;
+      // the MMA role reads this after the unit's first full barrier, whose
+      // arrival below releases it
+      if (lane == 0)
+        s_units[ul % C::kUnitRing] =
+            make_int2(nblocks, PAIR ? ((wk.nrows + 31) / 32) * 32 : ((wk.nrows + 15) / 16) * 16);
       // first token row this CTA loads: a pair splits the MMA's N in halves
       const int trow = PAIR ? wk.row0 + crank * (((wk.nrows + 31) / 32) * 16) : wk.row0;
+      // token rows this CTA's MMA operand needs; few: the small-box maps
+      const int my_rows = PAIR ? ((wk.nrows + 31) / 32) * 16 : ((wk.nrows + 15) / 16) * 16;
+      const bool small = BN > C::kSmallRows && my_rows <= C::kSmallRows;
+      const int bsub = small ? C::kBSubSmall : C::kBSub;
       int adapter = -1, j = 0;
       for (int b = 0; b < nblocks; ++b) {
         if (b >= nk) {  // next LoRA block: adapters in ascending order, lkb blocks each
@@ -466,8 +499,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
           if (ok) {
             const int nsub = subs_of(b, j);
             // the pair leader counts the bytes of both CTAs
-            if (leader)
-              mbar_arrive_expect_tx(&full[stage], (PAIR ? 2 : 1) * nsub * (C::kASub + C::kBSub));
+            if (leader) mbar_arrive_expect_tx(&full[stage], (PAIR ? 2 : 1) * nsub * (C::kASub + bsub));
             const uint32_t cbar = PAIR ? mapa_shared(smem_u32(&full[stage]), 0) : 0u;
             for (int sub = 0; sub < nsub; ++sub) {
               uint8_t* sA = smem + stage * C::kStageBytes + sub * C::kASub;
@@ -477,7 +509,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
                 const int kc = b * kBlockK + sub * 64;
                 load_weight_block<MODE, PAIR>(sA, &tm_w, &full[stage], cbar, kc, wk.e, wk.fb,
                                               p.rows_per_expert, p.gu_single_box, pol_w);
-                tmap = &tm_x;
+                tmap = small ? &tm_xs : &tm_x;
                 tc0 = kc;
               } else {
                 const int kc = j * kBlockK + sub * 64;
@@ -485,7 +517,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
                                      static_cast<int64_t>(wk.e) * p.lb_row_stride_expert;
                 load_lora_b_block<MODE, PAIR>(sA, &tm_lb, &full[stage], cbar, kc, frow, wk.fb,
                                               p.n_feat, pol_x);
-                tmap = &tm_lu;
+                tmap = small ? &tm_lus : &tm_lu;
                 tc0 = adapter * p.rank + kc;
               }
               const int st_sub = stage * C::kKSub + sub;
@@ -541,25 +573,18 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
         raise_timeout(p.status, abort_flag);
       ok = false;
     }
-    // The next unit's row adapters are loaded while this unit's MMAs issue,
-    // so the mask costs the MMA role no round trip between units.
-    TileAdapters<BN> next_ad;
-    if (use_lora && unit0 < total_work) {
-      const Work w0 = decode_work<BN>(unit0, crank, CL, s_off, s_ts, p.E, FBg);
-      load_tile_adapters<BN>(p.row_adapter, w0.row0, w0.nrows, lane, next_ad);
-    }
-    for (int w = unit0; w < total_work && ok; w += unit_step) {
+    // bf16: each unit's K-block count and MMA width come from the
+    // producer's descriptor ring (the producer works them out stages
+    // ahead), so the MMA role does no per-unit decoding between MMAs.
+    for (int w = unit0, ul = 0; w < total_work && ok; w += unit_step, ++ul) {
       if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
-      const Work wk = decode_work<BN>(w, crank, CL, s_off, s_ts, p.E, FBg);
-      const uint64_t amask = use_lora ? reduce_tile_adapters<BN>(next_ad) : 0;
-      if (use_lora && w + unit_step < total_work) {
-        const Work wn = decode_work<BN>(w + unit_step, crank, CL, s_off, s_ts, p.E, FBg);
-        load_tile_adapters<BN>(p.row_adapter, wn.row0, wn.nrows, lane, next_ad);
+      int nblocks_w8 = 0, ncols_w8 = 0;
+      if constexpr (W8) {
+        const Work wk = decode_work<BN>(w, crank, CL, s_off, s_ts, p.E, FBg);
+        const uint64_t amask = use_lora ? tile_adapter_mask<BN>(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
+        nblocks_w8 = nk + __popcll(amask) * lkb;
+        ncols_w8 = ((wk.nrows + 15) / 16) * 16;
       }
-      const int nblocks = nk + __popcll(amask) * lkb;
-      // a pair's N is split in halves of 16-row multiples
-      const int ncols = PAIR ? ((wk.nrows + 31) / 32) * 32 : ((wk.nrows + 15) / 16) * 16;
-      const uint32_t idesc = make_idesc_bf16(PAIR ? 256 : 128, ncols);
       if (lane == 0) {
         ok = wait_or_abort<PAIR>(&acce[acc], acc_phase ^ 1, p.timeout_ns, abort_flag);
         if (!ok) raise_timeout_at(p.status, abort_flag, kWaitMmaAccEmpty, w, 0, acc);
@@ -572,6 +597,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
       // block between the MMA issues.
       if (lane == 0) {
         int j = 0;
+        int nblocks = W8 ? nblocks_w8 : 1;  // bf16: known once the first block is in
+        uint32_t idesc = make_idesc_bf16(PAIR ? 256 : 128, W8 ? ncols_w8 : 16);
         for (int b = 0; b < nblocks; ++b) {
           ok = wait_or_abort<PAIR>(&full[stage], phase, p.timeout_ns, abort_flag);
           int site = kWaitMmaFull;
@@ -582,6 +609,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
           if (!ok) {
             raise_timeout_at(p.status, abort_flag, site, w, b, site == kWaitMmaFull8 ? s8 : stage);
             break;
+          }
+          if (!W8 && b == 0) {
+            const int2 d = s_units[ul % C::kUnitRing];
+            nblocks = d.x;
+            idesc = make_idesc_bf16(PAIR ? 256 : 128, d.y);
           }
           tc_fence_after_sync();
           const uint32_t a_base = smem_u32(smem + stage * (W8 ? C::kABytes : C::kStageBytes));
@@ -868,6 +900,7 @@ size_t gemm_smem_bytes(int bn, bool pair) {
 template <int BN, int MODE, int CL, bool PAIR, bool W8 = false>
 static cudaError_t launch_one(const CUtensorMap& tm_w, const CUtensorMap& tm_x,
                               const CUtensorMap& tm_lb, const CUtensorMap& tm_lu,
+                              const CUtensorMap& tm_xs, const CUtensorMap& tm_lus,
                               const GemmParams& p, int grid, cudaStream_t s) {
   using C = GemmCfg<BN, PAIR, W8>;
   auto kern = expert_gemm_kernel<BN, MODE, CL, PAIR, W8>;
@@ -875,7 +908,8 @@ static cudaError_t launch_one(const CUtensorMap& tm_w, const CUtensorMap& tm_x,
   cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
   if (CL == 1)
-    return launch_pdl(kern, dim3(grid), dim3(C::kThreads), smem, s, tm_w, tm_x, tm_lb, tm_lu, p);
+    return launch_pdl(kern, dim3(grid), dim3(C::kThreads), smem, s, tm_w, tm_x, tm_lb, tm_lu, tm_xs, tm_lus,
+                      p);
 
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(C::kThreads);
@@ -900,7 +934,7 @@ static cudaError_t launch_one(const CUtensorMap& tm_w, const CUtensorMap& tm_x,
   if (clusters < 1) clusters = 1;
   cfg.gridDim = dim3(clusters * CL);
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, tm_w, tm_x, tm_lb, tm_lu, p);
+  return cudaLaunchKernelEx(&cfg, kern, tm_w, tm_x, tm_lb, tm_lu, tm_xs, tm_lus, p);
 }
 
 // Wide token tiles run as CTA pairs (cta_group::2): each SM then lands half
@@ -909,7 +943,8 @@ bool gemm_use_pair(int bn) { return bn == 256; }
 
 cudaError_t launch_expert_gemm(int mode, int bn, bool pair, bool w8, const CUtensorMap& tm_w,
                                const CUtensorMap& tm_x, const CUtensorMap& tm_lb,
-                               const CUtensorMap& tm_lu, const GemmParams& p, int grid,
+                               const CUtensorMap& tm_lu, const CUtensorMap& tm_xs,
+                               const CUtensorMap& tm_lus, const GemmParams& p, int grid,
                                cudaStream_t s) {
   const int cl = pair ? 2 : 1;
   if (w8) {
@@ -917,8 +952,8 @@ cudaError_t launch_expert_gemm(int mode, int bn, bool pair, bool w8, const CUten
 #define MOE_GEMM_W8_CASE(BNV)                                                                     \
     if (bn == BNV)                                                                                \
       return mode == kGateUp                                                                      \
-                 ? launch_one<BNV, kGateUp, 1, false, true>(tm_w, tm_x, tm_lb, tm_lu, p, grid, s) \
-                 : launch_one<BNV, kDown, 1, false, true>(tm_w, tm_x, tm_lb, tm_lu, p, grid, s);
+                 ? launch_one<BNV, kGateUp, 1, false, true>(tm_w, tm_x, tm_lb, tm_lu, tm_xs, tm_lus, p, grid, s) \
+                 : launch_one<BNV, kDown, 1, false, true>(tm_w, tm_x, tm_lb, tm_lu, tm_xs, tm_lus, p, grid, s);
     MOE_GEMM_W8_CASE(16)
     MOE_GEMM_W8_CASE(32)
     MOE_GEMM_W8_CASE(64)
@@ -930,8 +965,8 @@ cudaError_t launch_expert_gemm(int mode, int bn, bool pair, bool w8, const CUten
 #define MOE_GEMM_CASE(BNV, CLV, PV)                                                               \
   if (bn == BNV && cl == CLV && pair == PV)                                                       \
     return mode == kGateUp                                                                        \
-               ? launch_one<BNV, kGateUp, CLV, PV>(tm_w, tm_x, tm_lb, tm_lu, p, grid, s)          \
-               : launch_one<BNV, kDown, CLV, PV>(tm_w, tm_x, tm_lb, tm_lu, p, grid, s);
+               ? launch_one<BNV, kGateUp, CLV, PV>(tm_w, tm_x, tm_lb, tm_lu, tm_xs, tm_lus, p, grid, s)          \
+               : launch_one<BNV, kDown, CLV, PV>(tm_w, tm_x, tm_lb, tm_lu, tm_xs, tm_lus, p, grid, s);
   MOE_GEMM_CASE(16, 1, false)
   MOE_GEMM_CASE(32, 1, false)
   MOE_GEMM_CASE(64, 1, false)

@@ -225,10 +225,13 @@ size_t gemm_smem_bytes(int bn, bool pair);
 bool gemm_use_pair(int bn);
 // w8: FP8 block-scaled weights (tm_w is then a 1-byte view, p.w_scale set);
 // one CTA per tile (no pair).  grid: CTAs of the persistent grid (pairs: at
-// most as many clusters of two as can be resident).
+// most as many clusters of two as can be resident).  tm_xs, tm_lus: the
+// token maps of tm_x and tm_lu with boxes 32 rows high, for tiles of at most
+// 32 rows per CTA (wide tiles only; otherwise pass tm_x and tm_lu).
 cudaError_t launch_expert_gemm(int mode, int bn, bool pair, bool w8, const CUtensorMap& tm_w,
                                const CUtensorMap& tm_x, const CUtensorMap& tm_lb,
-                               const CUtensorMap& tm_lu, const GemmParams& p, int grid,
+                               const CUtensorMap& tm_lu, const CUtensorMap& tm_xs,
+                               const CUtensorMap& tm_lus, const GemmParams& p, int grid,
                                cudaStream_t s);
 
 // ------------------------------------------------ FP8 activations (W8A8)
