@@ -155,14 +155,18 @@ def kernels_per_forward(wl, fp8=False, in_gemm_allowed=True, two_streams=False, 
     n, E = wl.T * wl.top_k, wl.E
     small = n <= 8192 and (((n + 1) & ~1) * 4 + 32 * E * 4 + (E + 1) * 4) <= 200 * 1024
     fuse_route = small and wl.T <= 128
+    # past the one-CTA permute: routing, count, scan + scatter (E <= 256,
+    # top_k dividing 1024), else routing, count, scan, scatter
+    chained = not small and E <= 256 and 1024 % wl.top_k == 0
+    route_permute = 1 if small else (3 if chained else 4)
     lora = wl.num_adapters > 0 and wl.rank > 0
     two = two_streams and lora
+    route_permute += 0 if (fuse_route or not small) else 1
     if w8a8:  # the row quant, the gate_up shrink, the activation quant, the down shrink
-        return ((0 if fuse_route else 1) + (1 if small else 3) + 1 + (1 if lora else 0) + 1 + 1 +
-                (1 if lora else 0) + 1 + 1)
+        return route_permute + 1 + (1 if lora else 0) + 1 + 1 + (1 if lora else 0) + 1 + 1
     fuse_shrink = shrink_in_gemm(wl, fp8, in_gemm_allowed and not two)
-    return ((0 if fuse_route else 1) + (1 if small else 3) + (0 if fuse_shrink else 1) +
-            (1 if two else 0) + 1 + (1 if lora and not fuse_shrink else 0) + 1 + 1)
+    return (route_permute + (0 if fuse_shrink else 1) + (1 if two else 0) + 1 +
+            (1 if lora and not fuse_shrink else 0) + 1 + 1)
 
 
 def max_over_ranks(value_ms, dist=None, device=None):

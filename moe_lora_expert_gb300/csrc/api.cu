@@ -472,7 +472,11 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   // The one-CTA permute clears the status word itself; otherwise clear it here.
   const bool small_permute = moe::small_permute_fits(static_cast<int>(n), E);
   const bool fuse_route = small_permute && T <= 128;
-  if (!small_permute && cudaMemsetAsync(status, 0, 16, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  // Past the one-CTA permute: routing and the permutation in two kernels
+  // (they clear the status word themselves), else routing + three kernels.
+  const bool route_permute = !small_permute && moe::route_permute_fits(T, K, E);
+  if (!small_permute && !route_permute && cudaMemsetAsync(status, 0, 16, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
 
   int32_t* topk_ids = a->topk_ids_out ? a->topk_ids_out : reinterpret_cast<int32_t*>(ws + pl.topk_ids);
   float* topk_w = a->topk_w_out ? a->topk_w_out : reinterpret_cast<float*>(ws + pl.topk_w);
@@ -626,12 +630,33 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   fp.clear_count = fuse_shrink ? static_cast<int>(2 * moe::shrink_flag_words(static_cast<int>(n), E)) : 0;
   fp.id_offset = shard_off;
   fp.id_limit = R;
-  if (!fuse_route &&
+  if (!fuse_route && !route_permute &&
       moe::launch_route_topk(a->router_logits, T, R, K, topk_ids, topk_w, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!mark()) return MOE_ERR_CUDA;
   if (small_permute) {
     if (moe::launch_small_permute(fp, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  } else if (route_permute) {
+    moe::RoutePermuteParams rp{};
+    rp.logits = a->router_logits;
+    rp.T = T;
+    rp.top_k = K;
+    rp.E = E;
+    rp.id_offset = shard_off;
+    rp.id_limit = R;
+    rp.topk_ids = topk_ids;
+    rp.topk_w = topk_w;
+    rp.mapping = fp.mapping;
+    rp.num_adapters = A;
+    rp.row_adapter = row_adapter;
+    rp.expert_offsets = offsets;
+    rp.e2p = e2p;
+    rp.p2e = p2e;
+    rp.chunk_counts = chunk_counts;
+    rp.tile_start = tile_start;
+    rp.tile_width_mask = fp.tile_width_mask;
+    rp.status = status;
+    if (moe::launch_route_permute(rp, stream) != cudaSuccess) return MOE_ERR_CUDA;
   } else {
     PermuteParams pp{};
     pp.topk_ids = topk_ids;

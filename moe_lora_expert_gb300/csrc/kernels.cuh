@@ -82,6 +82,34 @@ size_t gmask_bytes(int n, int E);
 size_t shrink_flag_words(int n, int E);
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t s);
 
+// Routing + permute of the forward in three chained kernels (past the one-CTA
+// permute; E <= kRoutePermuteMaxE, top_k dividing kPermuteChunk): routing,
+// count per chunk of whole tokens, then scan + scatter per chunk.  Writes topk ids and
+// weights, expert offsets, both maps, row adapters and the tile prefixes of
+// tile_width_mask; chunk_counts needs ceil(T * top_k / kPermuteChunk) x E
+// words.  Clears the device status words (status[0..3]).
+constexpr int kRoutePermuteMaxE = 256;
+struct RoutePermuteParams {
+  const float* logits;          // [T, id_limit]
+  int T, top_k, E;
+  int id_offset, id_limit;      // as in PermuteParams
+  int32_t* topk_ids;            // [T * top_k] global ids
+  float* topk_w;                // [T * top_k]
+  const int32_t* mapping;       // [T] or null
+  int num_adapters;
+  int32_t* row_adapter;         // [n] or null
+  int32_t* expert_offsets;      // [E + 1]
+  int32_t* e2p;                 // [n]
+  int32_t* p2e;                 // [n]
+  int32_t* chunk_counts;        // [nchunks, E]
+  int32_t* tile_start;          // [kNumTileWidths, E + 1]
+  uint32_t tile_width_mask;
+  int* status;
+  int tokens_per_chunk;         // set by the launcher
+};
+bool route_permute_fits(int T, int top_k, int E);
+cudaError_t launch_route_permute(const RoutePermuteParams& p, cudaStream_t s);
+
 // ------------------------------------------------- gather + LoRA shrink
 // Per 16-row tile of one expert: copy the source rows (gathered[p] = X[src(p)])
 // and/or U[p, a*r + i] = bf16(scaling * sum_k A[a, e(p)][i, k] * X[src(p), k])

@@ -91,6 +91,8 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
                                                          float* __restrict__ w) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  pdl_wait();  // no-ops unless launched as a programmatic dependent launch
+  pdl_launch_dependents();
   if (t >= T) return;
   int id;
   float wt;
@@ -99,6 +101,19 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
     ids[static_cast<size_t>(t) * k + lane] = id;
     w[static_cast<size_t>(t) * k + lane] = wt;
   }
+}
+
+cudaError_t launch_route_topk_pdl(const float* logits, int T, int E, int top_k, int32_t* ids, float* w,
+                                  cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const dim3 grid((T + 7) / 8), block(256);
+  const int epl = (E + 31) / 32;
+  if (epl <= 1) return launch_pdl(route_topk_kernel<1>, grid, block, 0, s, logits, T, E, top_k, ids, w);
+  if (epl <= 2) return launch_pdl(route_topk_kernel<2>, grid, block, 0, s, logits, T, E, top_k, ids, w);
+  if (epl <= 4) return launch_pdl(route_topk_kernel<4>, grid, block, 0, s, logits, T, E, top_k, ids, w);
+  if (epl <= 8) return launch_pdl(route_topk_kernel<8>, grid, block, 0, s, logits, T, E, top_k, ids, w);
+  if (epl <= 16) return launch_pdl(route_topk_kernel<16>, grid, block, 0, s, logits, T, E, top_k, ids, w);
+  return launch_pdl(route_topk_kernel<32>, grid, block, 0, s, logits, T, E, top_k, ids, w);
 }
 
 cudaError_t launch_route_topk(const float* logits, int T, int E, int top_k, int32_t* ids, float* w,
@@ -316,6 +331,162 @@ cudaError_t launch_permute(const PermuteParams& pin, cudaStream_t s) {
   if (p.hidden != nullptr && p.permuted != nullptr)
     permute_gather_kernel<<<(p.n + 7) / 8, 256, 0, s>>>(p);
   return cudaGetLastError();
+}
+
+// ------------------------------ routing + permute in three chained kernels
+// The forward's path past the one-CTA permute.  The slots are cut into
+// chunks of whole tokens (tokens_per_chunk * top_k <= kPermuteChunk slots).
+//   route_topk_kernel, one warp per token, over the whole GPU;
+//   route_count_kernel, one CTA of 32 warps per chunk: warp w ranks the
+//     slots of its segment [w seg, (w + 1) seg) among the earlier slots of
+//     the same expert (match_any, per-warp counters); a prefix over the
+//     warps' counters turns the ranks into ranks within the chunk, and the
+//     chunk's per-expert totals go out.
+//   scan_scatter_kernel, one CTA per chunk: every CTA reads all chunk totals,
+//     forms its chunk's per-expert base (the expert offset from a block scan
+//     of the expert totals, plus the counts of earlier chunks), and writes
+//     the final permuted index, the inverse map and the row adapter of its
+//     slots; CTA 0 also writes the expert offsets and the tile prefixes.
+// All three are programmatic dependent launches.  Stable order: slots in
+// expanded order within each expert, as in the other permutes.
+__global__ void __launch_bounds__(1024) route_count_kernel(const RoutePermuteParams p) {
+  extern __shared__ int rc_smem[];
+  const int E = p.E, k = p.top_k;
+  int* cnt = rc_smem;                                        // [32][E]
+  int16_t* s_ids = reinterpret_cast<int16_t*>(cnt + 32 * E);  // [kPermuteChunk]
+  int16_t* s_rank = s_ids + kPermuteChunk;                    // [kPermuteChunk]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t0 = blockIdx.x * p.tokens_per_chunk;
+  const int nt = min(p.tokens_per_chunk, p.T - t0);
+  const int ns = nt * k, x0 = t0 * k;
+  pdl_wait();
+  if (blockIdx.x == 0 && tid < 4) p.status[tid] = 0;
+  for (int i = tid; i < 32 * E; i += blockDim.x) cnt[i] = 0;
+  for (int x = tid; x < ns; x += blockDim.x) {  // the router's ids (global, always in range)
+    const int e = __ldcg(p.topk_ids + x0 + x) - p.id_offset;
+    s_ids[x] = static_cast<int16_t>(e >= 0 && e < E ? e : -1);
+  }
+  __syncthreads();
+  const int seg = (ns + 31) / 32;
+  const int xb = warp * seg, xe = min(xb + seg, ns);
+  int* my = cnt + warp * E;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int xs = xb; xs < xe; xs += 32) {
+    const int x = xs + lane;
+    const bool valid = x < xe;
+    const int id = valid ? s_ids[x] : -1;
+    const bool routed = id >= 0;
+    const unsigned grp = __match_any_sync(kFull, routed ? id : -2);
+    const int rank = __popc(grp & lt_mask);
+    const int prev = routed ? my[id] : 0;
+    __syncwarp();
+    if (routed && rank == 0) my[id] = prev + __popc(grp);
+    __syncwarp();
+    if (valid) s_rank[x] = static_cast<int16_t>(routed ? prev + rank : -1);
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < 32; ++w) {
+      const int v = cnt[w * E + e];
+      cnt[w * E + e] = run;
+      run += v;
+    }
+    p.chunk_counts[static_cast<size_t>(blockIdx.x) * E + e] = run;
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  for (int x = tid; x < ns; x += blockDim.x) {
+    const int id = s_ids[x];
+    p.e2p[x0 + x] = id >= 0 ? s_rank[x] + cnt[(x / seg) * E + id] : -1;  // rank within the chunk
+  }
+}
+
+__global__ void __launch_bounds__(1024) scan_scatter_kernel(const RoutePermuteParams p, int nchunks) {
+  __shared__ int warp_sums[32];
+  __shared__ int s_total;
+  extern __shared__ int ss_smem[];  // [E]: the chunk's base per expert
+  const int E = p.E, k = p.top_k, tid = threadIdx.x, c = blockIdx.x;
+  pdl_wait();
+  int pre = 0, total = 0;
+  if (tid < E) {
+    // loads in batches: one memory round trip per 16 chunks
+    constexpr int kBatch = 16;
+    for (int c0 = 0; c0 < nchunks; c0 += kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i)
+        v[i] = c0 + i < nchunks ? __ldcg(p.chunk_counts + static_cast<size_t>(c0 + i) * E + tid) : 0;
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        if (c0 + i < c) pre += v[i];
+        total += v[i];
+      }
+    }
+  }
+  const int off = block_exclusive_scan_1024(tid < E ? total : 0, warp_sums, &s_total);
+  const int routed_total = s_total;
+  if (tid < E) ss_smem[tid] = off + pre;
+  if (c == 0) {
+    if (tid < E) p.expert_offsets[tid] = off;
+    if (tid == 0) p.expert_offsets[E] = routed_total;
+    for (int wi = 0; wi < kNumTileWidths; ++wi) {
+      if (!((p.tile_width_mask >> wi) & 1u)) continue;
+      const int bn = tile_width_of(wi);
+      const int tiles = tid < E ? (total + bn - 1) / bn : 0;
+      const int ts = block_exclusive_scan_1024(tiles, warp_sums, &s_total);
+      if (tid < E) p.tile_start[wi * (E + 1) + tid] = ts;
+      if (tid == 0) p.tile_start[wi * (E + 1) + E] = s_total;
+    }
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  const int t0 = c * p.tokens_per_chunk;
+  const int nt = min(p.tokens_per_chunk, p.T - t0);
+  const int x0 = t0 * k;
+  for (int x = x0 + tid; x < x0 + nt * k; x += blockDim.x) {
+    const int r = __ldcg(p.e2p + x);
+    int pidx = -1;
+    if (r >= 0) {
+      const int e = __ldcg(p.topk_ids + x) - p.id_offset;  // routed here: a local expert
+      pidx = ss_smem[e] + r;
+      p.p2e[pidx] = x;
+      if (p.row_adapter != nullptr) {
+        int a = -1;
+        if (p.num_adapters > 0 && p.mapping != nullptr) {
+          a = __ldg(p.mapping + x / k);
+          if (a < -1 || a >= p.num_adapters) {
+            set_status(p.status, MOE_ERR_BAD_MAPPING);
+            a = -1;
+          }
+        }
+        p.row_adapter[pidx] = a;
+      }
+    }
+    p.e2p[x] = pidx;
+  }
+  // rows past the routed ones (slots dropped by expert parallelism) have no source
+  const int n = p.T * k;
+  for (int x = routed_total + c * blockDim.x + tid; x < n; x += gridDim.x * blockDim.x) p.p2e[x] = -1;
+}
+
+bool route_permute_fits(int T, int top_k, int E) {
+  return T > 0 && E <= kRoutePermuteMaxE && top_k <= 32 && kPermuteChunk % top_k == 0;
+}
+
+cudaError_t launch_route_permute(const RoutePermuteParams& pin, cudaStream_t s) {
+  RoutePermuteParams p = pin;
+  p.tokens_per_chunk = kPermuteChunk / p.top_k;
+  const int nchunks = (p.T + p.tokens_per_chunk - 1) / p.tokens_per_chunk;
+  const size_t smem1 = static_cast<size_t>(32) * p.E * 4 + 2 * kPermuteChunk * sizeof(int16_t);
+  const size_t smem2 = static_cast<size_t>(p.E) * 4;
+  cudaError_t err = launch_route_topk_pdl(p.logits, p.T, p.id_limit, p.top_k, p.topk_ids, p.topk_w, s);
+  if (err != cudaSuccess) return err;
+  err = ensure_smem_limit(reinterpret_cast<const void*>(route_count_kernel), (int)smem1);
+  if (err != cudaSuccess) return err;
+  err = launch_pdl(route_count_kernel, dim3(nchunks), dim3(1024), smem1, s, p);
+  if (err != cudaSuccess) return err;
+  return launch_pdl(scan_scatter_kernel, dim3(nchunks), dim3(1024), smem2, s, p, nchunks);
 }
 
 // ------------------------------------------------- one-CTA permute (fused)
@@ -584,7 +755,11 @@ static cudaError_t launch_finalize_k(const __nv_bfloat16* y, const int32_t* e2p,
     ctas[dev].store(resident, std::memory_order_relaxed);
   }
   const int ycols = (H / 8 + 255) / 256;
-  const int tok_ctas = std::max(1, std::min(T, resident / ycols));
+  // as few CTAs as give every CTA the same number of tokens (the last
+  // round of a persistent grid is otherwise partly idle)
+  const int cap = std::max(1, std::min(T, resident / ycols));
+  const int rounds = (T + cap - 1) / cap;
+  const int tok_ctas = (T + rounds - 1) / rounds;
   return launch_pdl(finalize_kernel<KMAX>, dim3(tok_ctas, ycols), dim3(256), 0, s, y, e2p, w, T,
                     top_k, H, out);
 }

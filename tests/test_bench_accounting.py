@@ -29,8 +29,11 @@ def test_kernel_counts_per_forward():
     assert bench.kernels_per_forward(W["decode_T16"], fp8=True) == 4
     # shared-outer rank 64: routing, permute, gather+shrink, GEMM, shrink, GEMM, finalize
     assert bench.kernels_per_forward(W["skewed_T256_shared_outer_r64"]) == 7
-    # prefill: routing, count + scan + scatter, row shrink, GEMM, row shrink, GEMM, finalize
-    assert bench.kernels_per_forward(W["prefill_T4096"]) == 9
+    # prefill: routing, count, scan+scatter, row shrink, GEMM, row shrink, GEMM, finalize
+    assert bench.kernels_per_forward(W["prefill_T4096"]) == 8
+    # more experts than the two-kernel permute takes: routing + count, scan, scatter
+    big_e = workloads.small_workload("e512", T=4096, H=256, I=128, E=512, top_k=8, num_adapters=1, rank=16)
+    assert bench.kernels_per_forward(big_e) == 9
 
 
 def test_shrink_in_gemm_conditions():
@@ -96,4 +99,4 @@ def test_kernel_counts_of_the_other_schedules():
     assert bench.kernels_per_forward(W["decode_T16"], in_gemm_allowed=False) == 6
     # two streams: the gather and the gate_up shrink are two kernels
     assert bench.kernels_per_forward(W["decode_T16"], two_streams=True) == 7
-    assert bench.kernels_per_forward(W["prefill_T4096"], two_streams=True) == 10
+    assert bench.kernels_per_forward(W["prefill_T4096"], two_streams=True) == 9

@@ -488,3 +488,38 @@ def test_two_stream_gate_up_shrink(name):
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), res["out"].view(torch.int16)), name
     assert layer.device_status() == 0
+
+
+@pytest.mark.parametrize("T,k,E,shard", [(2500, 4, 200, None), (5000, 2, 256, None), (3000, 8, 96, (40, 56))])
+def test_forward_two_kernel_route_permute(T, k, E, shard):
+    """Past the one-CTA permute (more than 8192 slots) routing and the
+    permutation run as three chained kernels (routing, count per chunk of
+    whole tokens, scan + scatter per chunk): ragged last chunk, E up to 256, top-k 2..8,
+    out-of-range mappings (flagged, treated as none), and an expert shard
+    (slots of other shards dropped).  Routing and the permutation bit-exact,
+    the output against the oracle."""
+    import moe_lora_expert_gb300 as m
+    wl = workloads.small_workload("rp", T=T, H=64, I=32, E=E, top_k=k, num_adapters=3, rank=8,
+                                  map_lo=-1, map_hi=2, seed=T + E)
+    inp = workloads.make_inputs(wl)
+    mapping = inp.mapping.copy()
+    mapping[::97] = 7          # outside [-1, 3): reported, treated as -1
+    ref_map = np.where((mapping >= -1) & (mapping < 3), mapping, -1).astype(np.int32)
+    if shard is None:
+        res = run_gpu(inp, mapping=mapping)
+        assert res["status"] == m.MOE_ERR_BAD_MAPPING, res["status_str"]
+        check_routing(res, inp)
+        ref_inp = workloads.LayerInputs(inp.wl, inp.logits, inp.hidden, inp.w13, inp.w2, inp.A_gu, inp.B_gu,
+                                        inp.A_dn, inp.B_dn, ref_map)
+        assert_output_close(res["out64"], oracle.forward_inputs(ref_inp)["out64"], f"rp T={T} k={k}")
+    else:
+        off, cnt = shard
+        sub = workloads.shard_experts(inp, off, cnt)
+        layer = make_layer(sub, local_expert_offset=off, num_router_experts=E)
+        res = run_gpu(sub, layer=layer, mapping=mapping)
+        assert res["status"] == m.MOE_ERR_BAD_MAPPING, res["status_str"]
+        check_routing(res, inp, shard=(off, cnt))
+        ref_sub = workloads.LayerInputs(sub.wl, sub.logits, sub.hidden, sub.w13, sub.w2, sub.A_gu, sub.B_gu,
+                                        sub.A_dn, sub.B_dn, ref_map)
+        ref = oracle.forward_inputs(ref_sub, local_expert_offset=off)["out64"]
+        assert_output_close(res["out64"], ref, f"rp shard {shard}")
