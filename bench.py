@@ -199,7 +199,7 @@ def load_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for name in ["expert_gemm.cu", "ptx.cuh", "kernels.cuh"]:
+    for name in ["expert_gemm.cu", "fp8_gemm.cu", "gemm_common.cuh", "ptx.cuh", "kernels.cuh"]:
         with open(os.path.join(ROOT, "moe_lora_expert_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
