@@ -141,7 +141,10 @@ int moe_permute(const int32_t* topk_ids, int T, int top_k, int E,
  * Limit: T * top_k <= MOE_NOALLOC_MAX_SLOTS and E <= MOE_MAX_EXPERTS; larger
  * sizes return MOE_ERR_UNSUPPORTED before anything is enqueued.
  * The first call on each device looks up the array's device address on the
- * current device; make that first call before any stream capture.
+ * current device and keeps it for the life of the process; make that first
+ * call before any stream capture.  A cudaDeviceReset (or a new primary
+ * context on the device) invalidates the kept address: do not call this
+ * entry point again on a device after resetting it.
  * Every call on a device uses the same array, and the array keeps the last
  * call's contents: calls whose work overlaps on the GPU (other streams,
  * other host threads) race and give undefined results.  Order them on one

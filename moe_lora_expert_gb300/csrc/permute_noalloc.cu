@@ -34,7 +34,9 @@ std::mutex g_setup_mutex;
 int32_t* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of the array on the current device.  The first call per
-// device looks it up (the name itself is only a host-side stand-in).
+// device looks it up (the name itself is only a host-side stand-in) and the
+// address is kept for the process: a device reset invalidates it, which the
+// header states.
 int32_t* scratch_on_current_device(int* status) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
