@@ -162,9 +162,10 @@ def kernels_per_forward(wl, fp8=False, in_gemm_allowed=True, two_streams=False, 
     lora = wl.num_adapters > 0 and wl.rank > 0
     two = two_streams and lora
     route_permute += 0 if (fuse_route or not small) else 1
-    if w8a8:  # the row quant, the gate_up shrink, the activation quant, the down shrink
-        return route_permute + 1 + (1 if lora else 0) + 1 + 1 + (1 if lora else 0) + 1 + 1
     fuse_shrink = shrink_in_gemm(wl, fp8, in_gemm_allowed and not two)
+    if w8a8:  # the row quant, the gate_up shrink, the activation quant, the down shrink
+        sh = 1 if lora and not fuse_shrink else 0
+        return route_permute + 1 + sh + 1 + 1 + sh + 1 + 1
     return (route_permute + (0 if fuse_shrink else 1) + (1 if two else 0) + 1 +
             (1 if lora and not fuse_shrink else 0) + 1 + 1)
 
@@ -400,8 +401,7 @@ class Layer:
         self.tile_n = args.tile_n
         self.tuning = tuning_from_args(args)
         self.side = None
-        self.in_gemm_allowed = (args.shrink_in_gemm != "off" and not args.side_stream and
-                                not (self.fp8 and args.fp8_activations))
+        self.in_gemm_allowed = args.shrink_in_gemm != "off" and not args.side_stream
         if args.side_stream:
             self.side = (torch.cuda.Stream(device=dev), [torch.cuda.Event(), torch.cuda.Event()])
 

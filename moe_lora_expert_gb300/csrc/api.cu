@@ -528,7 +528,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   // in kernels of their own.
   const bool fuse_shrink = lora && small_permute && bn == 16 && !pair && r <= 32 && !row_blocks &&
                            a->gate_up.a_stride_expert != 0 && tune.shrink_in_gemm == 0 &&
-                           side == nullptr && !a8;
+                           side == nullptr;
   const bool two_streams = lora && side != nullptr;
   // Persistent grid of the expert GEMMs.
   int gemm_grid = sms * (a8 ? moe::fp8_gemm_ctas_per_sm(bn) : moe::gemm_ctas_per_sm(bn));
@@ -780,7 +780,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.x_scale = xs;
   gp.out_f32 = hf;
   if (fuse_shrink) {
-    gp.sx = xp;
+    gp.sx = a8 ? nullptr : xp;  // W8A8: the GEMM reads the quantized rows; no bf16 copy
     gp.gather_src = static_cast<const __nv_bfloat16*>(a->hidden);
     gp.gather_map = p2e;
     gp.gather_div = K;

@@ -97,120 +97,6 @@ struct GemmCfg {
   static_assert(kCtasPerSm * (kSmemBytes + 1024) <= 233472, "the CTAs of an SM fit its shared memory");
 };
 
-// The LoRA shrink of the permuted rows, by the four epilogue warps (ew =
-// 0..3) before their first accumulator (GemmParams::fuse_shrink).  Rows are
-// claimed one at a time from p.row_counter (thread 0 claims the next row
-// while the current one is computed), so only CTAs that are running take
-// rows: a producer that waits for a tile waits on rows that running CTAs,
-// its own included, finish without waiting on anything.  For row p with adapter
-// a = row_adapter[p] >= 0, su[p, a r + i] = bf16(s_a sum_k A[a, e][i][k]
-// sx[p][k]) for i < r; every other column of the row is zero.  The 128
-// threads split K in 8-element pieces (thread j takes k = 8 j + 1024 m), sum
-// their pieces for 8 outputs at a time, reduce across each warp by shuffles
-// and across the four warps in shared memory (s_red, 4 x 32 floats).  Each
-// finished row adds one to the flag of its token tile (release, after a
-// proxy fence that makes the row visible to other CTAs' TMA reads); a tile
-// is complete when its flag equals its row count.  With p.gather_src the
-// pass first copies the row's token vector from gather_src (the hidden row
-// of its slot) into sx, so the gather needs no kernel of its own.
-template <int BN>
-__device__ void shrink_rows_in_gemm(const GemmParams& p, const int* s_off, const int* s_ts, int ew,
-                                    int lane, float* s_red) {
-  const int R = p.rank, ld = p.num_adapters * p.rank, K = p.K;
-  const int tid = ew * 32 + lane;
-  const int nrows_all = s_off[p.E];
-  volatile int* s_row = reinterpret_cast<volatile int*>(s_red + 128);  // the claimed row
-  int next = tid == 0 ? atomicAdd(p.row_counter, 1) : 0;
-  while (true) {
-    if (tid == 0) *s_row = next;
-    named_barrier_sync(1, 128);  // the claimed row is visible to the four warps
-    const int prow = *s_row;
-    if (prow >= nrows_all) break;
-    if (tid == 0) next = atomicAdd(p.row_counter, 1);  // in flight while this row is computed
-    int lo = 0, hi = p.E - 1;  // expert of the row: largest e with s_off[e] <= prow
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_off[mid] <= prow) lo = mid;
-      else hi = mid - 1;
-    }
-    const int e = lo;
-    const int tile = s_ts[e] + (prow - s_off[e]) / BN;
-    const int a = __ldcg(p.row_adapter + prow);
-    __nv_bfloat16* urow = p.su + static_cast<size_t>(prow) * ld;
-    const __nv_bfloat16* x = p.sx + static_cast<size_t>(prow) * K;
-    if (p.gather_src != nullptr) {
-      x = p.gather_src + static_cast<size_t>(__ldcg(p.gather_map + prow) / p.gather_div) * K;
-      __nv_bfloat16* dst = const_cast<__nv_bfloat16*>(p.sx) + static_cast<size_t>(prow) * K;
-      for (int k = tid * 8; k < K; k += 128 * 8)
-        *reinterpret_cast<uint4*>(dst + k) = __ldg(reinterpret_cast<const uint4*>(x + k));
-    }
-    // the other adapters' columns: zero (8 columns per store)
-    for (int c = tid * 8; c < ld; c += 128 * 8)
-      if (a < 0 || c / R != a) *reinterpret_cast<uint4*>(urow + c) = make_uint4(0, 0, 0, 0);
-    if (a >= 0) {  // uniform over the CTA
-      const __nv_bfloat16* A = p.sa + a * p.sa_stride_adapter + static_cast<int64_t>(e) * p.sa_stride_expert;
-      for (int i0 = 0; i0 < R; i0 += 8) {
-        float acc[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) acc[q] = 0.f;
-        for (int k = tid * 8; k < K; k += 128 * 8) {
-          const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + k));
-          const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xv);
-          float xf[8];
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const float2 f = __bfloat1622float2(x2[h]);
-            xf[2 * h] = f.x;
-            xf[2 * h + 1] = f.y;
-          }
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint4 av = __ldg(reinterpret_cast<const uint4*>(A + static_cast<size_t>(i0 + q) * K + k));
-            const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&av);
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const float2 f = __bfloat1622float2(a2[h]);
-              acc[q] = fmaf(f.x, xf[2 * h], acc[q]);
-              acc[q] = fmaf(f.y, xf[2 * h + 1], acc[q]);
-            }
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) acc[q] += __shfl_xor_sync(kFullMask, acc[q], off);
-        }
-        if (lane == 0) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) s_red[ew * 32 + i0 + q] = acc[q];
-        }
-      }
-      named_barrier_sync(1, 128);  // every warp's partial sums of this row
-      if (ew == 0 && lane < R)
-        urow[a * R + lane] = __float2bfloat16_rn(
-            p.sscale[a] * (s_red[lane] + s_red[32 + lane] + s_red[64 + lane] + s_red[96 + lane]));
-    }
-    fence_proxy_async_global();
-    named_barrier_sync(1, 128);  // the row is written; s_red is free again
-    if (tid == 0 && !(p.debug_hold_row && prow == 0)) {
-      __threadfence();
-      red_release_gpu_add(p.tile_flags + tile, 1);
-    }
-  }
-  named_barrier_sync(1, 128);  // every warp has read *s_row: the staging tiles are free
-}
-
-// Bounded wait until ``count`` rows of a token tile are published by the
-// in-kernel pass; then a proxy fence orders the TMA reads of them after it.
-__device__ __forceinline__ bool wait_tile_rows(const int* flag, int count, uint64_t limit_ns,
-                                               volatile int* abort_flag) {
-  const uint64_t t0 = global_timer_ns();
-  while (ld_acquire_gpu(flag) < count)
-    if (*abort_flag || global_timer_ns() - t0 > limit_ns) return false;
-  fence_proxy_async_global();
-  return true;
-}
-
 // PAIR (CL == 2): the two CTAs of the cluster take adjacent feature blocks
 // of the same token tile and share one M = 256 MMA (cta_group::2).  Each
 // loads its 128 weight rows and half of the token rows; all those bytes

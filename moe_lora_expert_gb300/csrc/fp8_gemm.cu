@@ -208,7 +208,13 @@ __global__ void __launch_bounds__(Fp8Cfg<BN>::kThreads, Fp8Cfg<BN>::kCtasPerSm)
           adapter = __ffsll(static_cast<long long>(amask)) - 1;
           amask &= amask - 1;
         }
-        if (lane == 0) {
+        if (lane == 0 && p.fuse_shrink && b == nk) {
+          // the tile's LoRA rows come from the in-kernel shrink of running
+          // CTAs (this one included): wait until all of them are published
+          ok = wait_tile_rows(p.tile_flags + w / FBg, wk.nrows, p.timeout_ns, abort_flag);
+          if (!ok && !*abort_flag) raise_timeout_at(p.status, abort_flag, kWaitShrinkFlag, w, b, stage);
+        }
+        if (lane == 0 && ok) {
           ok = wait_or_abort(&empty[stage], phase ^ 1, p.timeout_ns, abort_flag);
           if (ok) {
             uint8_t* sA = smem + stage * C::kStageBytes;
@@ -317,6 +323,10 @@ __global__ void __launch_bounds__(Fp8Cfg<BN>::kThreads, Fp8Cfg<BN>::kCtasPerSm)
     const int ldx = nk;           // token scales per row
     uint32_t slot = 0, sphase = 0;
     uint8_t* stg = s_epi + q * 1024;
+    // Decode-sized tiles: the LoRA shrink of the rows (u from the bf16
+    // hidden rows, v from the bf16 activation) runs here, before the first
+    // partial is ready (GemmParams::fuse_shrink).
+    if (p.fuse_shrink) shrink_rows_in_gemm<BN>(p, s_off, s_ts, warp - 2, lane, reinterpret_cast<float*>(s_epi));
     for (int w = blockIdx.x; w < total_work; w += gridDim.x) {
       if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
       const Work wk = decode_work<BN>(w, 0, 1, s_off, s_ts, p.E, FBg);
