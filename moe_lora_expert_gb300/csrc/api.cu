@@ -200,6 +200,13 @@ int num_sms() {
   return n;
 }
 
+size_t smem_per_sm() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess) return 0;
+  return static_cast<size_t>(n);
+}
+
 // Token-tile width from the rows per expert.  avg assumes every expert is
 // routed to; skewed routing touches fewer experts with more rows each, and a
 // tile narrower than an expert's rows streams that expert's weights once per
@@ -704,10 +711,13 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   sp.U = (lora && !fuse_shrink) ? U : nullptr;  // fused: the gather alone
   sp.status = status;
   sp.timeout_ns = timeout_ns;
-  sp.kc = moe::shrink_chunk(H, r, shrink_budget);
   // A shared gate_up A factor makes u a function of the token alone.
   sp.per_token = (lora && a->gate_up.a_stride_expert == 0) ? 1 : 0;
   sp.T = T;
+  // Per token: phases sized so that the whole grid is resident in one wave
+  // (more phases cost less than a second wave of CTAs).
+  sp.kc = moe::shrink_chunk(H, moe::gather_shrink_cta_rank(sp),
+                            sp.per_token ? moe::per_token_shrink_budget(sp, sms, smem_per_sm()) : shrink_budget);
   sp.e2p = e2p;
   sp.mapping = lora ? a->token_lora_mapping : nullptr;
   sp.tile_start_rows = tile_start + moe::tile_width_index(moe::rows_shrink_tile()) * (E + 1);
@@ -824,6 +834,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
     sp.U = V;
     sp.kc = moe::shrink_chunk(I, r, shrink_budget);
     sp.per_token = 0;
+    sp.tables_ready = 1;  // the permute completed before the gate_up GEMM let this grid launch
     if ((row_blocks ? moe::launch_rows_shrink(sp, static_cast<int>(n), stream)
                     : moe::launch_gather_shrink(sp, static_cast<int>(n), stream)) != cudaSuccess)
       return MOE_ERR_CUDA;

@@ -147,8 +147,22 @@ struct ShrinkParams {
   // absent there (no GEMM tile reads a's columns of these rows), unless it
   // owes the row gather (adapter slot 0).
   const uint64_t* gmask;
+  // 1 when the routing tables (offsets, tile prefixes, row adapters) are
+  // complete at launch (the down shrink, two kernels after the permute): the
+  // row-block kernel then reads them and prefetches its factor before it
+  // waits for the previous kernel (griddepcontrol.wait).
+  int tables_ready;
 };
 int shrink_chunk(int K, int rank, size_t smem_budget);
+// Factor columns one CTA of launch_gather_shrink holds (the rank, or a
+// 16-column slice of it in the per-token mode; 0 without U): the rank that
+// sizes its K phases.
+int gather_shrink_cta_rank(const ShrinkParams& p);
+// Per-token mode: the shared-memory budget of one CTA with which the whole
+// grid (ceil(T / 16) tiles x adapters x rank slices) is resident at once on
+// sms SMs of smem_per_sm bytes each (at most 200 KB; for grids beyond four
+// CTAs an SM, the budget of four).
+size_t per_token_shrink_budget(const ShrinkParams& p, int sms, size_t smem_per_sm);
 cudaError_t launch_gather_shrink(const ShrinkParams& p, int n_rows, cudaStream_t s);
 // Many rows: rows_shrink_tile()-row tiles of one expert, K streamed through a cp.async
 // pipeline.  Not for the per-token mode.  Uses p.tile_start_rows.

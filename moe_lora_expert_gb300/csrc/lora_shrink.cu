@@ -23,6 +23,8 @@
 // elements of rows g and g+8 and of factor row g of each 8-wide N tile and
 // feeds two m16n8k16 mma.sync steps with them (same K positions on both
 // operands); partial sums meet in shared memory.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -57,6 +59,7 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
   __nv_bfloat16* s_u = reinterpret_cast<__nv_bfloat16*>(s_red + 8 * 16 * R);  // [16][R]
   __shared__ int s_adapter[16];
   __shared__ int s_src[16];
+  __shared__ int s_dst[16 * MOE_MAX_TOP_K];  // per-token mode: e2p of the tile's tokens
   __shared__ int s_info[3];
   __shared__ int s_ok;
   __shared__ int s_ts[MOE_MAX_EXPERTS + 1];
@@ -64,7 +67,10 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
 
-  pdl_wait();
+  // Per-token mode: the tile (16 tokens), the rows and the factor are the
+  // layer's own inputs, so the loads and the product run while the permute
+  // is still going; only the scatter to permuted rows waits for it (below).
+  if (!p.per_token) pdl_wait();
   if (p.gmask != nullptr && !p.per_token) {
     // One round trip decides whether this (tile, adapter slot) has work.
     if (tid == 0) {
@@ -138,11 +144,9 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
 #pragma unroll
     for (int i = 0; i < 16; ++i) present |= (s_adapter[i] == ad);
   }
-  // Row gather: slot 0's CTA copies each row; in the per-token mode a token's
-  // top_k copies are shared out over the adapter-slot CTAs of the tile
-  // (slot j goes to CTA j mod gridDim.y).
-  const int gshare = p.per_token ? static_cast<int>(gridDim.y) : 1;
-  const bool do_gather = p.gathered != nullptr && rs == 0 && (p.per_token ? ad < p.top_k : ad == 0);
+  // Row gather: slot 0's CTA copies each row from the staged tile.  (The
+  // per-token mode copies after the permute, from global memory, below.)
+  const bool do_gather = p.gathered != nullptr && !p.per_token && ad == 0;
   const int passes = (present || do_gather) ? 1 : 0;
   const int K = p.K;
   uint32_t parity = 0;
@@ -184,13 +188,9 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
       parity ^= 1;
       if (do_gather) {
         const int vpr = cur / 8;
-        // permuted rows of a token this CTA copies: slots ad, ad + gshare, ...
-        const int copies = p.per_token ? (p.top_k - ad + gshare - 1) / gshare : 1;
-        for (int v = tid; v < nrows * copies * vpr; v += kShrinkThreads) {
-          const int rc = v / vpr, c = (v - rc * vpr) * 8;
-          const int row = rc / copies, j = ad + (rc - row * copies) * gshare;
-          const int dst = p.per_token ? p.e2p[(row0 + row) * p.top_k + j] : row0 + row;
-          if (dst < 0) continue;  // slot not routed here (dropped id, another shard's expert)
+        for (int v = tid; v < nrows * vpr; v += kShrinkThreads) {
+          const int row = v / vpr, c = (v - row * vpr) * 8;
+          const int dst = row0 + row;
           *reinterpret_cast<uint4*>(p.gathered + static_cast<size_t>(dst) * K + kc0 + c) =
               *reinterpret_cast<const uint4*>(Xs + row * pitch + c);
         }
@@ -237,6 +237,31 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
      }
     }
   }
+  if (p.per_token) {
+    // From here on the permute's tables: wait for it, then read the
+    // permuted rows of the tile's tokens once.
+    pdl_wait();
+    for (int i = tid; i < nrows * p.top_k; i += kShrinkThreads) s_dst[i] = p.e2p[row0 * p.top_k + i];
+    __syncthreads();
+    if (p.gathered != nullptr) {
+      // The tile's (token, copy j) pairs q = token * top_k + j are shared out
+      // over the C = gridDim.y * gridDim.z CTAs of the tile: CTA c copies
+      // pairs c, c + C, ... from the source rows (just read, so in L2).
+      const int C = static_cast<int>(gridDim.y * gridDim.z);
+      const int c0 = ad + static_cast<int>(gridDim.y) * rs;
+      const int npairs = nrows * p.top_k;
+      const int mine = npairs > c0 ? (npairs - c0 + C - 1) / C : 0;
+      const int vpr = K / 8;
+      for (int v = tid; v < mine * vpr; v += kShrinkThreads) {
+        const int i = v / vpr, c = (v - i * vpr) * 8;
+        const int q = c0 + i * C;
+        const int dst = s_dst[q];
+        if (dst < 0) continue;  // slot not routed here (dropped id, another shard's expert)
+        *reinterpret_cast<uint4*>(p.gathered + static_cast<size_t>(dst) * K + c) =
+            __ldg(reinterpret_cast<const uint4*>(p.X + static_cast<size_t>(row0 + q / p.top_k) * K + c));
+      }
+    }
+  }
   pdl_launch_dependents();
 
   if constexpr (NT > 0) {
@@ -247,8 +272,8 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
     for (int v = tid; v < nrows * copies * vec_per_row; v += kShrinkThreads) {
       const int rc = v / vec_per_row;
       const int c = (v - rc * vec_per_row) * 8;
-      const int row = rc / copies, j = rc - row * copies;
-      const int dst = p.per_token ? p.e2p[(row0 + row) * p.top_k + j] : row0 + row;
+      const int row = rc / copies;
+      const int dst = p.per_token ? s_dst[rc] : row0 + row;
       if (dst < 0) continue;  // slot not routed here
       uint4 val = zero;
       if (s_adapter[row] == ad) val = *reinterpret_cast<const uint4*>(s_u + row * R + c);
@@ -258,25 +283,44 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
   }
 }
 
+// The largest phase (a multiple of 64) that fits the budget fixes the number
+// of phases; the phases are then made equal, so that the shared memory of a
+// CTA is no larger than that number of phases needs.
 int shrink_chunk(int K, int rank, size_t budget) {
   if (shrink_smem_bytes(K, rank) <= budget) return K;
   int kc = 64;
   while (kc + 64 < K && shrink_smem_bytes(kc + 64, rank) <= budget) kc += 64;
-  return kc;
+  const int phases = (K + kc - 1) / kc;
+  return ((K + phases - 1) / phases + 63) / 64 * 64;
 }
 
-size_t shrink_launch_smem(const ShrinkParams& p) { return shrink_smem_bytes(p.kc, p.rank); }
+// The per-token mode has few tiles (16 tokens each): a rank of 32 or more
+// is split into 16-column slices, one CTA each, so that more CTAs share the
+// factor reads.
+static int gather_shrink_slices(const ShrinkParams& p) {
+  return (p.per_token && p.U != nullptr && p.rank >= 32 && p.rank % 16 == 0) ? p.rank / 16 : 1;
+}
+
+int gather_shrink_cta_rank(const ShrinkParams& p) { return p.U != nullptr ? p.rank / gather_shrink_slices(p) : 0; }
+
+size_t per_token_shrink_budget(const ShrinkParams& p, int sms, size_t smem_per_sm) {
+  const int64_t ctas = static_cast<int64_t>((p.T + 15) / 16) * (p.U != nullptr ? p.num_adapters : 1) *
+                       gather_shrink_slices(p);
+  // Beyond four CTAs an SM the grid runs in waves whatever the phase size;
+  // four then stay resident with phases of about 700 elements.
+  const int64_t per_sm = std::min<int64_t>(4, std::max<int64_t>(1, (ctas + sms - 1) / sms));
+  // 4 KB a CTA for its static shared memory and the per-block reservation.
+  const int64_t fit = static_cast<int64_t>(smem_per_sm) / per_sm - 4096;
+  return static_cast<size_t>(std::max<int64_t>(std::min<int64_t>(fit, 200 * 1024), 16 * 1024));
+}
 
 cudaError_t launch_gather_shrink(const ShrinkParams& p, int n_rows, cudaStream_t s) {
   if (n_rows == 0) return cudaSuccess;
-  // The per-token mode has few tiles (16 tokens each): a rank of 32 or more
-  // is split into 16-column slices, one CTA each, so that more CTAs share
-  // the factor reads.
-  const int slices = (p.per_token && p.U != nullptr && p.rank >= 32 && p.rank % 16 == 0) ? p.rank / 16 : 1;
+  const int slices = gather_shrink_slices(p);
   const int NT = p.rank / 8 / slices;
   const int tiles = p.per_token ? (p.T + 15) / 16 : (n_rows + 15) / 16 + (p.E < n_rows ? p.E : n_rows);
   const dim3 grid(tiles, (NT > 0 && p.U != nullptr) ? p.num_adapters : 1, slices);
-  const size_t smem = shrink_smem_bytes(p.kc, p.U != nullptr ? p.rank / slices : 0);
+  const size_t smem = shrink_smem_bytes(p.kc, gather_shrink_cta_rank(p));
 #define MOE_SHRINK_CASE(N)                                                                        \
   case N: {                                                                                       \
     cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(gather_shrink_kernel<N>), (int)smem); \
@@ -348,8 +392,11 @@ __global__ void __launch_bounds__(kRowThreads) rows_shrink_kernel(const ShrinkPa
   const int g = lane >> 2, t4 = lane & 3;
   const int a = static_cast<int>(blockIdx.y);
 
-  pdl_wait();
-  for (int i = tid; i <= p.E; i += kRowThreads) s_ts[i] = p.tile_start_rows[i];
+  // tables_ready: the routing tables are complete at launch, so the tile,
+  // its rows and the factor are worked out (L2 loads: no stale L1 line) and
+  // the factor prefetched while the previous kernel, which writes X, drains.
+  if (!p.tables_ready) pdl_wait();
+  for (int i = tid; i <= p.E; i += kRowThreads) s_ts[i] = __ldcg(p.tile_start_rows + i);
   __syncthreads();
   if (tid == 0) {
     const int tile = blockIdx.x;
@@ -362,8 +409,8 @@ __global__ void __launch_bounds__(kRowThreads) rows_shrink_kernel(const ShrinkPa
         else hi = mid - 1;
       }
       e = lo;
-      row0 = p.expert_offsets[lo] + (tile - s_ts[lo]) * kRowTile;
-      nrows = min(kRowTile, p.expert_offsets[lo + 1] - row0);
+      row0 = __ldcg(p.expert_offsets + lo) + (tile - s_ts[lo]) * kRowTile;
+      nrows = min(kRowTile, __ldcg(p.expert_offsets + lo + 1) - row0);
     }
     s_info[0] = e;
     s_info[1] = row0;
@@ -378,7 +425,7 @@ __global__ void __launch_bounds__(kRowThreads) rows_shrink_kernel(const ShrinkPa
   // Compact the rows this CTA loads, in tile order (block-wide ballot scan).
   bool take = false;
   if (tid < kRowTile) {
-    const int ad = (tid < nrows && lora) ? p.row_adapter[row0 + tid] : -1;
+    const int ad = (tid < nrows && lora) ? __ldcg(p.row_adapter + row0 + tid) : -1;
     s_adp[tid] = ad;
     take = tid < nrows && (do_gather || ad == a);
   }
@@ -399,6 +446,14 @@ __global__ void __launch_bounds__(kRowThreads) rows_shrink_kernel(const ShrinkPa
   const __nv_bfloat16* Af =
       lora ? p.A + a * p.a_stride_adapter + static_cast<int64_t>(e) * p.a_stride_expert : nullptr;
   const bool compute = lora && m > 0;
+  if (p.tables_ready) {
+    if (compute && warp == 0) {  // R rows of K: one contiguous block, in 16 KB pieces
+      const uint32_t bytes = static_cast<uint32_t>(R) * K * 2;
+      for (uint32_t off = lane * 16384u; off < bytes; off += 32u * 16384u)
+        bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(Af) + off, min(16384u, bytes - off));
+    }
+    pdl_wait();
+  }
 
   // This thread's share of every chunk: column jc of compacted rows
   // (tid >> 3) + kRowStride q, and column jc of factor rows (tid >> 3) + kRowStride q.

@@ -524,6 +524,11 @@ __global__ void __launch_bounds__(1024) small_permute_kernel(const FusedPermuteP
   for (int i = tid; i < p.clear_count; i += blockDim.x) p.clear_flags[i] = 0;
   for (int i = tid; i < 32 * E; i += blockDim.x) s_cnt[i] = 0;
   __syncthreads();
+  // The next kernel may start now (after the status word and the flags are
+  // cleared): every consumer of the tables below waits for this grid to
+  // complete (griddepcontrol.wait) before it reads them, and the per-token
+  // shrink does its factor product meanwhile.
+  pdl_launch_dependents();
   if (p.logits != nullptr) {
     for (int t = warp; t < p.T; t += 32) {
       int id;
@@ -595,7 +600,6 @@ __global__ void __launch_bounds__(1024) small_permute_kernel(const FusedPermuteP
   if (p.gmask != nullptr)
     for (int i = tid; i < ntiles16; i += blockDim.x) s_m16[i] = 0ull;
   __syncthreads();
-  pdl_launch_dependents();
 
   for (int x = tid; x < n; x += blockDim.x) {
     const int id = s_ids[x];
