@@ -92,7 +92,7 @@ struct GemmCfg {
   static constexpr int kEpiBytes = 4 * 1024;
   static constexpr int kSmemBytes =
       1024 + kARingBytes + kStages8 * kW8Stage + kEpiOffset + kEpiBytes;
-  static_assert((2 * kStages + 2 * kStages8 + 6) * 8 + 16 <= kMetaBytes, "barriers fit");
+  static_assert((2 * kStages + 2 * kStages8 + 6) * 8 + 16 <= kMetaBytes, "barriers, TMEM slot, flag, key fit");
   static_assert(kUnitRing > kStages, "a unit has at least one stage");
   static_assert(kCtasPerSm * (kSmemBytes + 1024) <= 233472, "the CTAs of an SM fit its shared memory");
 };
@@ -137,6 +137,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
   uint64_t* empty8 = full8 + C::kStages8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty8 + C::kStages8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  unsigned long long* s_grid_key = reinterpret_cast<unsigned long long*>(tmem_slot + 2);
   int* s_off = reinterpret_cast<int*>(meta + C::kMetaBytes);
   int* s_ts = s_off + (MOE_MAX_EXPERTS + 1);
   int2* s_units = reinterpret_cast<int2*>(meta + C::kMetaBytes + C::kTableBytes);
@@ -171,6 +172,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
     mbar_init(drain, 1);
     mbar_init(never, 1);
     *abort_flag = 0;
+    *s_grid_key = ~0ull;
     fence_mbarrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -211,10 +213,16 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
   if (CL > 1) cluster_sync_all();
   const uint32_t tmem_base = *tmem_slot;
   const int crank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const int unit0 = CL > 1 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
-  const int unit_step = CL > 1 ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
   const int FBg = (p.feat_blocks + CL - 1) / CL;
   const int total_work = s_ts[p.E] * FBg;
+  // Units are dealt round robin over the first unit_step CTAs of the grid,
+  // a count that evens out the last round of these HBM-bound tiles; the rest
+  // take none.  CTA pairs (wide tiles) are bound by the tensor pipe, whose
+  // last round is no shorter with fewer units in it: all of them take units.
+  const int unit_step = CL > 1 ? static_cast<int>(cluster_count_x())
+                               : balanced_grid(total_work, static_cast<int>(gridDim.x), s_grid_key);
+  const int unit_id = CL > 1 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int unit0 = unit_id < unit_step ? unit_id : total_work;
   const bool leader = !PAIR || crank == 0;
 
   if (W8 && warp == 0) {

@@ -119,7 +119,7 @@ struct Fp8Cfg {
   static constexpr int kEpiOffset = (kMetaBytes + kTableBytes + 15) / 16 * 16;
   static constexpr int kEpiBytes = 4 * 1024;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiOffset + kEpiBytes;
-  static_assert((2 * kStages + 2 * kSlots + 2) * 8 + 16 <= kMetaBytes, "barriers fit");
+  static_assert((2 * kStages + 2 * kSlots + 2) * 8 + 16 <= kMetaBytes, "barriers, TMEM slot, flag, key fit");
   static_assert(kCtasPerSm * (kSmemBytes + 1024) <= 233472, "the CTAs of an SM fit its shared memory");
   static_assert(kCtasPerSm * kTmemCols <= 512, "the CTAs of an SM fit its tensor memory");
 };
@@ -141,6 +141,7 @@ __global__ void __launch_bounds__(Fp8Cfg<BN>::kThreads, Fp8Cfg<BN>::kCtasPerSm)
   uint64_t* drain = pempty + C::kSlots;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  unsigned long long* s_grid_key = reinterpret_cast<unsigned long long*>(tmem_slot + 2);
   int* s_off = reinterpret_cast<int*>(meta + C::kMetaBytes);
   int* s_ts = s_off + (MOE_MAX_EXPERTS + 1);
   uint8_t* s_epi = meta + C::kEpiOffset;
@@ -161,6 +162,7 @@ __global__ void __launch_bounds__(Fp8Cfg<BN>::kThreads, Fp8Cfg<BN>::kCtasPerSm)
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
+    *s_grid_key = ~0ull;
     fence_mbarrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -190,6 +192,10 @@ __global__ void __launch_bounds__(Fp8Cfg<BN>::kThreads, Fp8Cfg<BN>::kCtasPerSm)
   const uint32_t tmem_base = *tmem_slot;
   const int FBg = p.feat_blocks;
   const int total_work = s_ts[p.E] * FBg;
+  // Units are dealt round robin over the first unit_step CTAs of the grid,
+  // a count that evens out the last round; the rest take none.
+  const int unit_step = balanced_grid(total_work, static_cast<int>(gridDim.x), s_grid_key);
+  const int unit0 = static_cast<int>(blockIdx.x) < unit_step ? static_cast<int>(blockIdx.x) : total_work;
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
@@ -197,7 +203,7 @@ __global__ void __launch_bounds__(Fp8Cfg<BN>::kThreads, Fp8Cfg<BN>::kCtasPerSm)
     const uint64_t pol_x = l2_policy_evict_last();
     uint32_t stage = 0, phase = 0, armed = 0, armed_parity = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total_work && ok; w += gridDim.x) {
+    for (int w = unit0; w < total_work && ok; w += unit_step) {
       if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
       const Work wk = decode_work<BN>(w, 0, 1, s_off, s_ts, p.E, FBg);
       uint64_t amask = use_lora ? tile_adapter_mask<BN>(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
@@ -259,7 +265,7 @@ __global__ void __launch_bounds__(Fp8Cfg<BN>::kThreads, Fp8Cfg<BN>::kCtasPerSm)
     // -------------------------------------------------------- MMA issuer
     uint32_t stage = 0, phase = 0, slot = 0, sphase = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total_work && ok; w += gridDim.x) {
+    for (int w = unit0; w < total_work && ok; w += unit_step) {
       if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
       const Work wk = decode_work<BN>(w, 0, 1, s_off, s_ts, p.E, FBg);
       const uint64_t amask = use_lora ? tile_adapter_mask<BN>(p.row_adapter, wk.row0, wk.nrows, lane) : 0;
@@ -327,7 +333,7 @@ __global__ void __launch_bounds__(Fp8Cfg<BN>::kThreads, Fp8Cfg<BN>::kCtasPerSm)
     // hidden rows, v from the bf16 activation) runs here, before the first
     // partial is ready (GemmParams::fuse_shrink).
     if (p.fuse_shrink) shrink_rows_in_gemm<BN>(p, s_off, s_ts, warp - 2, lane, reinterpret_cast<float*>(s_epi));
-    for (int w = blockIdx.x; w < total_work; w += gridDim.x) {
+    for (int w = unit0; w < total_work; w += unit_step) {
       if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
       const Work wk = decode_work<BN>(w, 0, 1, s_off, s_ts, p.E, FBg);
       const uint64_t amask = use_lora ? tile_adapter_mask<BN>(p.row_adapter, wk.row0, wk.nrows, lane) : 0;

@@ -40,6 +40,34 @@ __device__ __forceinline__ Work decode_work(int u, int crank, int CL, const int*
   return wk;
 }
 
+// How many of the persistent grid's pmax CTAs (or clusters) take work units,
+// given u units dealt round robin.  Every full round streams one unit per
+// working CTA; the last round holds the u mod P leftover units, and a few
+// CTAs alone cannot pull the memory bandwidth that all of them share (each
+// is limited by the bytes its ring keeps in flight; about 70% of the grid
+// saturates it).  In units of one unit's bytes at full bandwidth the time
+// is (rounds - 1) P + max(fill, 0.7 pmax); the smallest over P in
+// [3/4 pmax, pmax] is taken (the largest P on ties).  The CTAs beyond it
+// take no units; they still join the in-kernel row passes.  The candidates
+// are scored one per thread and meet in *s_key, which thread 0 set to ~0
+// before the CTA's last barrier; every thread of the CTA calls this (it
+// holds a barrier when u > pmax).
+__device__ __forceinline__ int balanced_grid(int u, int pmax, unsigned long long* s_key) {
+  if (u <= pmax) return pmax;  // one round
+  const int psat = (pmax * 7) / 10;
+  const int ncand = pmax - (3 * pmax + 3) / 4 + 1;
+  for (int c = threadIdx.x; c < ncand; c += blockDim.x) {
+    const int P = pmax - c;
+    const int rounds = (u + P - 1) / P;
+    const int fill = u - (rounds - 1) * P;
+    const unsigned long long t =
+        static_cast<unsigned long long>(rounds - 1) * P + static_cast<unsigned long long>(fill > psat ? fill : psat);
+    atomicMin(s_key, (t << 20) | static_cast<unsigned long long>(c));
+  }
+  __syncthreads();
+  return pmax - static_cast<int>(*s_key & 0xFFFFFull);
+}
+
 // The adapter mask of a token tile: OR of (1 << adapter) over its rows,
 // computed by a whole warp.  The loads of a tile's (at most BN) row adapters
 // are issued together, BN / 32 per lane, so the mask costs one round trip to
