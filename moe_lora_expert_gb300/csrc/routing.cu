@@ -53,22 +53,21 @@ __device__ __forceinline__ void route_token(const float* __restrict__ row, int E
   int my_id = 0;
   for (int j = 0; j < k; ++j) {
     // this lane's best: the largest key, the lowest slot (= id) among equals
+    // (selects only, no conditional stores: the keys stay in registers)
     uint32_t best = 0u;
     int bs = 0;
 #pragma unroll
-    for (int s = 0; s < EPL; ++s)
-      if (key[s] > best) {
-        best = key[s];
-        bs = s;
-      }
+    for (int s = 0; s < EPL; ++s) {
+      const bool gt = key[s] > best;
+      bs = gt ? s : bs;
+      best = gt ? key[s] : best;
+    }
     const uint32_t m = __reduce_max_sync(kFull, best);
     const uint32_t cand = (best == m) ? static_cast<uint32_t>(bs * 32 + lane) : 0xFFFFFFFFu;
     const uint32_t idx = __reduce_min_sync(kFull, cand);
-    if (static_cast<int>(idx & 31u) == lane) {
+    const bool mine = static_cast<int>(idx & 31u) == lane;
 #pragma unroll
-      for (int s = 0; s < EPL; ++s)
-        if (static_cast<uint32_t>(s) == (idx >> 5)) key[s] = 0u;
-    }
+    for (int s = 0; s < EPL; ++s) key[s] = (mine && static_cast<uint32_t>(s) == (idx >> 5)) ? 0u : key[s];
     if (lane == j) {
       my_logit = float_from_order_bits(m);
       my_id = static_cast<int>(idx);
