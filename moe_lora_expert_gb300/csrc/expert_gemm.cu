@@ -217,9 +217,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, PAIR, W8>::kThreads, GemmCfg<BN, P
   const int total_work = s_ts[p.E] * FBg;
   // Units are dealt round robin over the first unit_step CTAs of the grid,
   // a count that evens out the last round of these HBM-bound tiles; the rest
-  // take none.  CTA pairs (wide tiles) are bound by the tensor pipe, whose
-  // last round is no shorter with fewer units in it: all of them take units.
+  // take none.  CTA pairs (wide tiles, bound by the tensor pipe) and FP8
+  // weights (bound by the converter warps) run no faster with fewer units in
+  // the last round: there every CTA takes units.
   const int unit_step = CL > 1 ? static_cast<int>(cluster_count_x())
+                        : W8   ? static_cast<int>(gridDim.x)
                                : balanced_grid(total_work, static_cast<int>(gridDim.x), s_grid_key);
   const int unit_id = CL > 1 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
   const int unit0 = unit_id < unit_step ? unit_id : total_work;
