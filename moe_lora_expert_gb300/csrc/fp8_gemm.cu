@@ -111,8 +111,10 @@ struct Fp8Cfg {
   static constexpr int kStagesRaw = kStageBudget / kStageBytes;
   static constexpr int kStages = kStagesRaw > 16 ? 16 : kStagesRaw;
   // TMEM partial slots of BN columns (a power-of-two allocation; two CTAs
-  // of narrow tiles share an SM's 512 columns)
-  static constexpr int kSlots = BN <= 32 ? 8 : (BN == 64 ? 4 : 4);
+  // of narrow tiles share an SM's 512 columns).  16-wide tiles take 16, so
+  // the MMA can run two units of the down GEMM ahead of the epilogue warps
+  // while they do the in-kernel shrink pass.
+  static constexpr int kSlots = BN <= 16 ? 16 : (BN <= 32 ? 8 : 4);
   static constexpr int kTmemCols = kSlots * BN < 32 ? 32 : kSlots * BN;
   static constexpr int kMetaBytes = 512;
   static constexpr int kTableBytes = 2 * (MOE_MAX_EXPERTS + 1) * 4;
