@@ -198,9 +198,13 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(fp8_activations=False):
+    """Hash of the source of the expert GEMM kernels: the bf16 / FP8-weight
+    kernel (expert_gemm.cu), or with FP8 activations the W8A8 kernel
+    (fp8_gemm.cu), with the headers both include."""
     h = hashlib.sha256()
-    for name in ["expert_gemm.cu", "fp8_gemm.cu", "gemm_common.cuh", "ptx.cuh", "kernels.cuh"]:
+    main = "fp8_gemm.cu" if fp8_activations else "expert_gemm.cu"
+    for name in [main, "gemm_common.cuh", "ptx.cuh", "kernels.cuh"]:
         with open(os.path.join(ROOT, "moe_lora_expert_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -208,7 +212,8 @@ def kernel_source_hash():
 
 def committed_traffic(kernel, workload):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel source; else None."""
+    the current source of that kernel; else None.  Workload tags ending in
+    _w8a8 are the W8A8 kernels."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
@@ -216,7 +221,7 @@ def committed_traffic(kernel, workload):
     except Exception:
         return None
     ent = doc.get(kernel, {}).get(workload)
-    if not ent or ent.get("kernel_source_sha") != kernel_source_hash():
+    if not ent or ent.get("kernel_source_sha") != kernel_source_hash(workload.endswith("_w8a8")):
         return None
     return ent.get("dram_bytes_per_launch")
 
