@@ -19,6 +19,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -198,15 +199,23 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def _code_only(text):
+    """C++ source without its comments and blank lines (string literals in
+    these files hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash(fp8_activations=False):
-    """Hash of the source of the expert GEMM kernels: the bf16 / FP8-weight
-    kernel (expert_gemm.cu), or with FP8 activations the W8A8 kernel
-    (fp8_gemm.cu), with the headers both include."""
+    """Hash of the code (comments left out) of the expert GEMM kernels: the
+    bf16 / FP8-weight kernel (expert_gemm.cu), or with FP8 activations the
+    W8A8 kernel (fp8_gemm.cu), with the headers both include."""
     h = hashlib.sha256()
     main = "fp8_gemm.cu" if fp8_activations else "expert_gemm.cu"
     for name in [main, "gemm_common.cuh", "ptx.cuh", "kernels.cuh"]:
-        with open(os.path.join(ROOT, "moe_lora_expert_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "moe_lora_expert_gb300", "csrc", name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -28,9 +28,10 @@
 //
 // Roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
 // owner, warps 2..5 = epilogue (TMEM lane quadrant = warp % 4).  The kernel
-// is persistent: CTA b takes work items b, b + gridDim.x, ...; the TMEM
-// accumulator is double-buffered so the epilogue of one item overlaps the
-// MMAs of the next.
+// is persistent: CTA b < P takes work items b, b + P, ... (P, at most the
+// grid, chosen on the device so that the last round is not a thin one; see
+// balanced_grid); the TMEM accumulator is double-buffered so the epilogue of
+// one item overlaps the MMAs of the next.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
