@@ -688,20 +688,23 @@ __global__ void __launch_bounds__(256) finalize_kernel(const __nv_bfloat16* __re
                                                        const float* __restrict__ w, int T, int k,
                                                        int H, __nv_bfloat16* __restrict__ out) {
   const int c8 = blockIdx.y * blockDim.x + threadIdx.x;
-  pdl_wait();
-  pdl_launch_dependents();
-  if (c8 * 8 >= H) return;
   int p_cur[KMAX], p_nxt[KMAX];
   float w_cur[KMAX], w_nxt[KMAX];
   auto load_idx = [&](int tok, int (&pp)[KMAX], float (&ww)[KMAX]) {
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
-      pp[j] = j < k ? __ldg(e2p + static_cast<size_t>(tok) * k + j) : -1;
-      ww[j] = j < k ? __ldg(w + static_cast<size_t>(tok) * k + j) : 0.f;
+      pp[j] = j < k ? __ldcg(e2p + static_cast<size_t>(tok) * k + j) : -1;
+      ww[j] = j < k ? __ldcg(w + static_cast<size_t>(tok) * k + j) : 0.f;
     }
   };
+  // The slot indices and weights come from the permute, which completed
+  // before the down GEMM let this grid launch: the first token's are read
+  // while that GEMM drains; y only after the wait.
   int t = blockIdx.x;
-  if (t < T) load_idx(t, p_cur, w_cur);
+  if (t < T && c8 * 8 < H) load_idx(t, p_cur, w_cur);
+  pdl_wait();
+  pdl_launch_dependents();
+  if (c8 * 8 >= H) return;
   for (; t < T; t += gridDim.x) {
     uint4 v[KMAX];
 #pragma unroll
