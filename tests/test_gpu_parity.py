@@ -382,6 +382,25 @@ def test_device_wait_timeout_is_reported_and_recoverable():
     assert_output_close(to_f64(out), oracle.forward_inputs(inp)["out64"], "after timeout")
 
 
+@pytest.mark.parametrize("T,A,rank", [(403, 3, 64), (1000, 2, 32)])
+def test_forward_shared_outer_multi_phase(T, A, rank):
+    """Shared gate_up A factor with more 16-token tiles than one wave of
+    single-phase CTAs holds: the per-token shrink splits K (H = 2048) into
+    three (T = 403, rank 64 in four slices, a ragged last tile) or two
+    (T = 1000, rank 32 in two slices) equal phases so that the grid is
+    resident at once; its factor product runs before the permute is known to
+    be complete and its row gather is shared by every CTA of a tile."""
+    wl = workloads.small_workload("so_phases", T=T, H=2048, I=64, E=8, top_k=2, num_adapters=A,
+                                  rank=rank, map_lo=-1, map_hi=A - 1, shared_outer=True, seed=T + rank)
+    inp = workloads.make_inputs(wl)
+    res = run_gpu(inp)
+    assert res["status"] == 0, res["status_str"]
+    check_routing(res, inp)
+    tokens = list(range(0, T, 7)) + [T - 1]
+    ref = oracle.forward_inputs(inp, tokens=tokens)["out64"]
+    assert_output_close(res["out64"][tokens], ref, f"shared-outer phases T={T} r={rank}")
+
+
 @pytest.mark.parametrize("rank", [16, 48, 128])
 def test_forward_shared_outer_rank_slices(rank):
     """Shared gate_up A factor (per-token shrink): ranks of 32 or more are
