@@ -147,3 +147,24 @@ def test_w8a8_no_adapter_tokens_match_plain_w8a8():
     a = run_gpu(inp, layer=w8a8_layer(inp, fp8), mapping=none)["out"]
     b = run_gpu(inp, layer=w8a8_layer(inp, fp8, with_lora=False), with_lora=False)["out"]
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_w8a8_shrink_flag_wait_timeout_is_reported_and_recoverable():
+    """The W8A8 GEMM holds a tile's LoRA operand loads until the in-kernel
+    shrink has published the tile's rows.  With permuted row 0 never counted
+    (test flag) that tile never completes: the held load's wait runs out,
+    the forward reports MOE_ERR_DEVICE_TIMEOUT and the kernels drain and
+    exit; the next call on the same workspace is correct."""
+    import moe_lora_expert_gb300 as m
+    torch = torch_mod()
+    inp = workloads.make_inputs(workloads.WORKLOADS["decode_T16"])
+    fp8 = workloads.fp8_weights(inp)
+    layer = w8a8_layer(inp, fp8)
+    hid = bf16_tensor(inp.hidden)
+    lg = torch.from_numpy(inp.logits).to(dev())
+    mp = torch.from_numpy(inp.mapping).to(dev())
+    layer.forward(hid, lg, mp, wait_timeout_ms=20, debug_flags=m.MOE_DEBUG_HOLD_SHRINK_ROW)
+    assert layer.device_status() == m.MOE_ERR_DEVICE_TIMEOUT
+    out = layer.forward(hid, lg, mp)
+    assert layer.device_status() == m.MOE_OK
+    assert_output_close(to_f64(out), w8a8_ref(inp, fp8), "w8a8 after flag timeout")
