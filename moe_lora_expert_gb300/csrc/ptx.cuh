@@ -187,8 +187,6 @@ __device__ __forceinline__ void tma_load_5d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-// Untiled bulk copy global -> shared, completion counted in bytes on ``bar``.
-// Both addresses 16-byte aligned, size a multiple of 16.
 // Bulk prefetch of [src, src + bytes) into L2 (no completion to wait for);
 // src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
@@ -196,6 +194,8 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
                : "memory");
 }
 
+// Untiled bulk copy global -> shared, completion counted in bytes on ``bar``.
+// Both addresses 16-byte aligned, size a multiple of 16.
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes,
                                           uint64_t* bar) {
   asm volatile(
