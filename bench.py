@@ -49,8 +49,9 @@ def parse_args():
                     help="with --weights fp8: FP8 activations too (W8A8, per-token-group quant)")
     ap.add_argument("--only-workload", action="store_true",
                     help="measure --workload alone (default: also the metric's other batch shapes)")
-    ap.add_argument("--shrink-in-gemm", choices=["auto", "off"], default="auto",
-                    help="off: separate gather/shrink kernels (A/B of the in-GEMM shrink)")
+    ap.add_argument("--shrink-in-gemm", choices=["auto", "off", "with-gather"], default="auto",
+                    help="off: separate gather/shrink kernels (A/B of the in-GEMM shrink); "
+                         "with-gather: the row gather inside the gate_up GEMM too")
     ap.add_argument("--side-stream", action="store_true",
                     help="two-stream schedule: gate_up LoRA shrink on a side stream")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -63,7 +64,7 @@ def parse_args():
 # Algorithmic work of one forward (from the actual routing of the inputs)
 # ---------------------------------------------------------------------------
 
-def algorithmic_work(wl, ids, mapping, fp8=False, in_gemm_allowed=True):
+def algorithmic_work(wl, ids, mapping, fp8=False, in_gemm_allowed=True, gemm_reads_hidden=False):
     """Bytes and FLOPs the forward must move / compute, intermediates excluded.
 
     Bytes: every touched expert's w13 and w2 once (fp8: one byte per weight
@@ -74,9 +75,10 @@ def algorithmic_work(wl, ids, mapping, fp8=False, in_gemm_allowed=True):
     slots (the shared gate_up shrink once per token).
 
     Per expert GEMM the same rule: the weights and LoRA factors it reads, plus
-    the layer input where it reads that itself (the row gather inside the
-    gate_up GEMM); the permuted rows, the LoRA operands, the activation and
-    the expert outputs are intermediates and are not charged.
+    the layer input where it reads that itself (``gemm_reads_hidden``: the
+    gate_up GEMM's in-kernel shrink reads the hidden rows, W8A8, or the row
+    gather runs inside it); the permuted rows, the LoRA operands, the
+    activation and the expert outputs are intermediates and are not charged.
     """
     T, H, I, E, k, A, r = wl.T, wl.H, wl.I, wl.E, wl.top_k, wl.num_adapters, wl.rank
     n = T * k
@@ -113,9 +115,9 @@ def algorithmic_work(wl, ids, mapping, fp8=False, in_gemm_allowed=True):
         "flops": n * 2 * H * I + n_ad * 2 * H * r,
     }
     if shrink_in_gemm(wl, fp8, in_gemm_allowed):
-        # the GEMMs also gather the rows (gate_up: the hidden input) and run
-        # the LoRA shrinks (A factors)
-        work["gemm_gate_up"]["bytes"] += gu_A + T * H * 2
+        # the GEMMs also run the LoRA shrinks (A factors; gate_up, where it
+        # reads them itself, the hidden rows)
+        work["gemm_gate_up"]["bytes"] += gu_A + (T * H * 2 if gemm_reads_hidden else 0)
         work["gemm_gate_up"]["flops"] += n_ad * 2 * r * H
         work["gemm_down"]["bytes"] += dn_A
         work["gemm_down"]["flops"] += n_ad * 2 * r * I
@@ -135,8 +137,8 @@ def auto_tile_n(n_rows, E):
 
 
 def shrink_in_gemm(wl, fp8=False, allowed=True):
-    """Whether the library runs the row gather and the LoRA shrinks inside
-    the expert GEMMs (api.cu: 16-wide tiles, so at most four rows per expert
+    """Whether the library runs the LoRA shrinks inside the expert GEMMs
+    (api.cu: 16-wide tiles, so at most four rows per expert
     on average and never the row-block shrink; rank <= 32; per-expert gate_up
     A factors; the one-CTA permute; bf16 or FP8 weights alike)."""
     n, E = wl.T * wl.top_k, wl.E
@@ -146,13 +148,15 @@ def shrink_in_gemm(wl, fp8=False, allowed=True):
             not wl.shared_outer)
 
 
-def kernels_per_forward(wl, fp8=False, in_gemm_allowed=True, two_streams=False, w8a8=False):
+def kernels_per_forward(wl, fp8=False, in_gemm_allowed=True, two_streams=False, w8a8=False,
+                        gather_in_gemm=False):
     """Kernels one moe_lora_forward launches (mirrors the library's choices):
     routing (unless fused into the one-CTA permute), the permute (one CTA, or
     count + scan + scatter), the gather/gate_up shrink and the down shrink
-    (unless both run inside the GEMMs; the two-stream schedule splits the
-    first into a gather and a shrink), the gate_up GEMM, the down GEMM and
-    the finalize."""
+    (with the shrinks inside the GEMMs: the row gather alone, unless it runs
+    inside the gate_up GEMM too; the two-stream schedule splits the first
+    into a gather and a shrink), the gate_up GEMM, the down GEMM and the
+    finalize."""
     n, E = wl.T * wl.top_k, wl.E
     small = n <= 8192 and (((n + 1) & ~1) * 4 + 32 * E * 4 + (E + 1) * 4) <= 200 * 1024
     fuse_route = small and wl.T <= 128
@@ -167,7 +171,7 @@ def kernels_per_forward(wl, fp8=False, in_gemm_allowed=True, two_streams=False, 
     if w8a8:  # the row quant, the gate_up shrink, the activation quant, the down shrink
         sh = 1 if lora and not fuse_shrink else 0
         return route_permute + 1 + sh + 1 + 1 + sh + 1 + 1
-    return (route_permute + (0 if fuse_shrink else 1) + (1 if two else 0) + 1 +
+    return (route_permute + (0 if fuse_shrink and gather_in_gemm else 1) + (1 if two else 0) + 1 +
             (1 if lora and not fuse_shrink else 0) + 1 + 1)
 
 
@@ -375,6 +379,8 @@ def tuning_from_args(args):
     t = {}
     if args.shrink_in_gemm == "off":
         t["shrink_in_gemm"] = 1
+    elif args.shrink_in_gemm == "with-gather":
+        t["shrink_in_gemm"] = 2
     return t or None
 
 
@@ -416,6 +422,10 @@ class Layer:
         self.tuning = tuning_from_args(args)
         self.side = None
         self.in_gemm_allowed = args.shrink_in_gemm != "off" and not args.side_stream
+        self.a8 = bool(args.fp8_activations and self.fp8)
+        # the gate_up GEMM reads the hidden rows itself: W8A8's in-kernel
+        # shrink, or the row gather inside the GEMM
+        self.gemm_reads_hidden = self.a8 or args.shrink_in_gemm == "with-gather"
         if args.side_stream:
             self.side = (torch.cuda.Stream(device=dev), [torch.cuda.Event(), torch.cuda.Event()])
 
@@ -481,7 +491,8 @@ def rooflines(L, ms_per_step, stage_ms, peaks, peak_src, workload_tag):
     import moe_lora_expert_gb300 as m
     wl = L.wl
     ids_np = L.ids.cpu().numpy()
-    work = algorithmic_work(wl, ids_np, L.inp.mapping, fp8=L.fp8, in_gemm_allowed=L.in_gemm_allowed)
+    work = algorithmic_work(wl, ids_np, L.inp.mapping, fp8=L.fp8, in_gemm_allowed=L.in_gemm_allowed,
+                            gemm_reads_hidden=L.gemm_reads_hidden)
     med = [statistics.median(s[j] for s in stage_ms) for j in range(len(m.STAGE_NAMES))]
     stages_us = {nm: round(v * 1e3, 2) for nm, v in zip(m.STAGE_NAMES, med)}
     top = "gemm_gate_up" if med[3] >= med[5] else "gemm_down"
@@ -618,7 +629,7 @@ def run_ours(args):
              "note": "one CUDA graph per step, replayed; e2e_value includes the host copies"}
     roof, fwd, stages_us = rooflines(L, ms_per_step, stage_ms, peaks, peak_src, tag(wl.name))
     n_kernels = kernels_per_forward(wl, fp8, args.shrink_in_gemm != "off", args.side_stream,
-                                    bool(fp8 and args.fp8_activations))
+                                    bool(fp8 and args.fp8_activations), args.shrink_in_gemm == "with-gather")
     del L, h_hidden, h_logits, h_mapping, d_hidden, d_logits, d_mapping, g_fwd, g_e2e
 
     # ---------------- the metric's other batch shapes (T=64, T=4096): the

@@ -197,9 +197,10 @@ typedef struct {
  *   shrink_kernel:  0 = auto, 1 = the 16-row-tile LoRA shrink kernel,
  *                   2 = the row-block shrink kernel (not for a shared gate_up
  *                   A factor, which always uses the 16-row kernel).
- *   shrink_in_gemm: 0 = auto (the row gather and both LoRA shrinks run
- *                   inside the expert GEMMs for decode-sized tiles),
- *                   1 = never (separate gather/shrink kernels).
+ *   shrink_in_gemm: 0 = auto (for decode-sized tiles both LoRA shrinks run
+ *                   inside the expert GEMMs, after a row-gather kernel),
+ *                   1 = never (separate gather/shrink kernels),
+ *                   2 = the row gather inside the gate_up GEMM as well.
  *   gemm_max_ctas:  0 = auto (SM count x resident CTAs per SM); otherwise
  *                   at most this many CTAs in each expert GEMM's persistent
  *                   grid (rounded up to a pair for CTA pairs).  Any value is

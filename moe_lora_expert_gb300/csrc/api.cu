@@ -390,7 +390,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   std::memset(&tune, 0, sizeof(tune));
   if (has_tuning) tune = a->tuning;
   if (tune.cta_pairs < 0 || tune.cta_pairs > 2 || tune.shrink_kernel < 0 || tune.shrink_kernel > 2 ||
-      tune.shrink_in_gemm < 0 || tune.shrink_in_gemm > 1 || tune.gemm_max_ctas < 0)
+      tune.shrink_in_gemm < 0 || tune.shrink_in_gemm > 2 || tune.gemm_max_ctas < 0)
     return MOE_ERR_UNSUPPORTED;
   cudaStream_t side = has_tuning ? reinterpret_cast<cudaStream_t>(a->side_stream) : nullptr;
   if (side != nullptr && (a->side_events[0] == nullptr || a->side_events[1] == nullptr))
@@ -526,16 +526,23 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   bool row_blocks = n_local > 16 * static_cast<int64_t>(sms) ||
                     (r >= 64 && n_local >= 8 * std::min<int64_t>(E, n_local));
   if (tune.shrink_kernel != 0) row_blocks = tune.shrink_kernel == 2;
-  // Decode-sized tiles: the row gather and the LoRA shrinks run inside the
-  // expert GEMMs (their epilogue warps are idle until the first accumulator
-  // is ready), so no kernel sits between the permute and the gate_up GEMM or
-  // between the GEMMs.  Needs the one-CTA permute (it clears the tile flags
-  // and the row counters), one CTA per 16-wide tile, rank <= 32 and
-  // per-expert gate_up A factors.  The two-stream schedule keeps the shrinks
-  // in kernels of their own.
+  // Decode-sized tiles: the LoRA shrinks run inside the expert GEMMs (their
+  // epilogue warps are idle until the first accumulator is ready), so no
+  // shrink kernel sits between the permute and the gate_up GEMM or between
+  // the GEMMs.  Needs the one-CTA permute (it clears the tile flags and the
+  // row counters), one CTA per 16-wide tile, rank <= 32 and per-expert
+  // gate_up A factors.  The two-stream schedule keeps the shrinks in kernels
+  // of their own.
   const bool fuse_shrink = lora && small_permute && bn == 16 && !pair && r <= 32 && !row_blocks &&
-                           a->gate_up.a_stride_expert != 0 && tune.shrink_in_gemm == 0 &&
+                           a->gate_up.a_stride_expert != 0 && tune.shrink_in_gemm != 1 &&
                            side == nullptr;
+  // With bf16 activations the row gather runs first as a small kernel of its
+  // own, which lets the gate_up GEMM launch as soon as the permute is done and
+  // stream weights before the rows are in; only its LoRA blocks then wait for
+  // the in-kernel shrink.  (Tuning 2: the gather inside the gate_up GEMM too,
+  // whose first loads then wait for the tile's rows.)  W8A8 gathers in its
+  // row quantizer.
+  const bool gather_kernel = fuse_shrink && !a8 && tune.shrink_in_gemm != 2;
   const bool two_streams = lora && side != nullptr;
   // Persistent grid of the expert GEMMs.
   int gemm_grid = sms * (a8 ? moe::fp8_gemm_ctas_per_sm(bn) : moe::gemm_ctas_per_sm(bn));
@@ -755,8 +762,11 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
     if (cudaEventRecord(join, side) != cudaSuccess) return MOE_ERR_CUDA;
     if (launch_shrink(sp, stream) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaStreamWaitEvent(stream, join, 0) != cudaSuccess) return MOE_ERR_CUDA;
-  } else if (!fuse_shrink && (!a8 || lora) &&  // fused: the gate_up GEMM gathers the rows itself
+  } else if (!fuse_shrink && (!a8 || lora) &&  // fused: the shrink runs inside the gate_up GEMM
              launch_shrink(sp, stream) != cudaSuccess) {
+    return MOE_ERR_CUDA;
+  } else if (gather_kernel &&  // fused: the row gather alone (sp.U is null)
+             moe::launch_gather_shrink(sp, static_cast<int>(n), stream) != cudaSuccess) {
     return MOE_ERR_CUDA;
   }
   if (!mark()) return MOE_ERR_CUDA;
@@ -780,9 +790,11 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.out = h;
   gp.status = status;
   gp.timeout_ns = timeout_ns;
-  // Launched right after the gate_up shrink (n > 0 here), or (fused) right
-  // after the permute, whose tables may still be in flight.
-  gp.tables_ready = fuse_shrink ? 0 : 1;
+  // Launched right after the gate_up shrink or the row gather (n > 0 here),
+  // which wait for the permute before they let this grid launch, or (gather
+  // inside the GEMM) right after the permute, whose tables may still be in
+  // flight.
+  gp.tables_ready = (fuse_shrink && !gather_kernel) ? 0 : 1;
   gp.w_scale = w8 ? a->w13_scale : nullptr;
   gp.scale_nb = (2 * I + 127) / 128;
   gp.scale_kb = (H + 127) / 128;
@@ -791,7 +803,7 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   gp.out_f32 = hf;
   if (fuse_shrink) {
     gp.sx = a8 ? nullptr : xp;  // W8A8: the GEMM reads the quantized rows; no bf16 copy
-    gp.gather_src = static_cast<const __nv_bfloat16*>(a->hidden);
+    gp.gather_src = gather_kernel ? nullptr : static_cast<const __nv_bfloat16*>(a->hidden);
     gp.gather_map = p2e;
     gp.gather_div = K;
     gp.sa = static_cast<const __nv_bfloat16*>(a->gate_up.A);

@@ -71,6 +71,9 @@ __global__ void __launch_bounds__(kShrinkThreads) gather_shrink_kernel(const Shr
   // layer's own inputs, so the loads and the product run while the permute
   // is still going; only the scatter to permuted rows waits for it (below).
   if (!p.per_token) pdl_wait();
+  // The gather alone: the next kernel reads the gathered rows only after its
+  // own griddepcontrol.wait, and the tables are complete now.
+  if (!p.per_token && p.U == nullptr) pdl_launch_dependents();
   if (p.gmask != nullptr && !p.per_token) {
     // One round trip decides whether this (tile, adapter slot) has work.
     if (tid == 0) {

@@ -175,7 +175,7 @@ def _valid_args(**over):
     # kernel-choice overrides outside their sets
     ({"tuning": m.Tuning(cta_pairs=3)}, m.MOE_ERR_UNSUPPORTED),
     ({"tuning": m.Tuning(shrink_kernel=-1)}, m.MOE_ERR_UNSUPPORTED),
-    ({"tuning": m.Tuning(shrink_in_gemm=2)}, m.MOE_ERR_UNSUPPORTED),
+    ({"tuning": m.Tuning(shrink_in_gemm=3)}, m.MOE_ERR_UNSUPPORTED),
     ({"tuning": m.Tuning(gemm_max_ctas=-5)}, m.MOE_ERR_UNSUPPORTED),
     # a structure from before the tuning fields ignores them (checks go on)
     ({"struct_size": m.MoeLoraArgs.tuning.offset, "tuning": m.Tuning(cta_pairs=3), "hidden": None},

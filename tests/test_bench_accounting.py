@@ -23,10 +23,14 @@ def test_auto_tile_n(n_rows, E, bn):
 
 def test_kernel_counts_per_forward():
     W = workloads.WORKLOADS
-    # decode: permute (routing fused) + two GEMMs (gather and shrinks inside) + finalize
-    assert bench.kernels_per_forward(W["decode_T16"]) == 4
-    assert bench.kernels_per_forward(W["decode_T64_mixed8"]) == 4
-    assert bench.kernels_per_forward(W["decode_T16"], fp8=True) == 4
+    # decode: permute (routing fused) + row gather + two GEMMs (shrinks inside) + finalize
+    assert bench.kernels_per_forward(W["decode_T16"]) == 5
+    assert bench.kernels_per_forward(W["decode_T64_mixed8"]) == 5
+    assert bench.kernels_per_forward(W["decode_T16"], fp8=True) == 5
+    # the row gather inside the gate_up GEMM as well
+    assert bench.kernels_per_forward(W["decode_T16"], gather_in_gemm=True) == 4
+    # W8A8: permute, row quant (the gather), GEMM, activation quant, GEMM, finalize
+    assert bench.kernels_per_forward(W["decode_T16"], fp8=True, w8a8=True) == 6
     # shared-outer rank 64: routing, permute, gather+shrink, GEMM, shrink, GEMM, finalize
     assert bench.kernels_per_forward(W["skewed_T256_shared_outer_r64"]) == 7
     # prefill: routing, count, scan+scatter, row shrink, GEMM, row shrink, GEMM, finalize
@@ -52,14 +56,16 @@ def test_shrink_in_gemm_conditions():
 def test_gemm_bytes_charge_the_in_gemm_shrink():
     """Each expert GEMM is charged the weights and LoRA factors it reads and
     none of the intermediates (permuted rows, LoRA operands, activation,
-    expert outputs).  With the gather and shrinks inside the GEMMs, the
-    gate_up kernel is also charged the A factors and the hidden input it
-    reads; the down kernel the down A factors.  The sums are rebuilt here
-    term by term from the routing of the seeded inputs."""
+    expert outputs).  With the shrinks inside the GEMMs, the gate_up kernel
+    is also charged the A factors it reads, and the hidden input where it
+    reads that itself (W8A8, or the row gather inside it); the down kernel
+    the down A factors.  The sums are rebuilt here term by term from the
+    routing of the seeded inputs."""
     wl = workloads.WORKLOADS["decode_T16"]
     inp = workloads.make_inputs(wl)
     ids, _ = oracle.route_topk(inp.logits, wl.top_k)
     work = bench.algorithmic_work(wl, ids, inp.mapping)
+    own = bench.algorithmic_work(wl, ids, inp.mapping, gemm_reads_hidden=True)
     T, H, I, E, k, r = wl.T, wl.H, wl.I, wl.E, wl.top_k, wl.rank
     n = T * k
     experts = len(set(int(e) for e in ids.ravel()))
@@ -67,10 +73,12 @@ def test_gemm_bytes_charge_the_in_gemm_shrink():
     pairs = len({(a, int(e)) for t, a in adapted for e in ids[t]})
     n_ad = len(adapted) * k
     gu = experts * 2 * I * H * 2 + pairs * 2 * I * r * 2
-    gu += pairs * r * H * 2 + T * H * 2
+    gu += pairs * r * H * 2
     dn = experts * H * I * 2 + pairs * H * r * 2
     dn += pairs * r * I * 2
     assert work["gemm_gate_up"]["bytes"] == gu
+    assert own["gemm_gate_up"]["bytes"] == gu + T * H * 2
+    assert own["bytes"] == work["bytes"] and own["gemm_down"] == work["gemm_down"]
     assert work["gemm_down"]["bytes"] == dn
     assert work["gemm_gate_up"]["flops"] == n * 2 * 2 * I * H + n_ad * 2 * 2 * I * r + n_ad * 2 * r * H
     assert work["gemm_down"]["flops"] == n * 2 * H * I + n_ad * 2 * H * r + n_ad * 2 * r * I

@@ -293,17 +293,31 @@ def test_forward_many_rows_row_block_shrink(with_lora):
     assert_output_close(res["out64"][tokens], ref, f"rows lora={with_lora}")
 
 
-@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 @pytest.mark.parametrize("name", ["decode_T16", "decode_T64_mixed8", "tiny_T8"])
-def test_forward_shrink_in_gemm_and_separate(name, fused):
+def test_forward_shrink_in_gemm_and_separate(name, mode):
     """Decode-sized tiles compute the LoRA shrinks inside the expert GEMMs
-    (tile flags between CTAs); tuning.shrink_in_gemm = 1 keeps the separate
-    shrink kernels.  Both against the oracle."""
+    (tile flags between CTAs) after a row-gather kernel (tuning 0);
+    tuning.shrink_in_gemm = 1 keeps the separate shrink kernels, 2 moves the
+    row gather into the gate_up GEMM too.  Each against the oracle."""
     inp = cached_inputs(name)
-    res = run_gpu(inp, tuning={"shrink_in_gemm": 0 if fused else 1})
+    res = run_gpu(inp, tuning={"shrink_in_gemm": mode})
     assert res["status"] == 0, res["status_str"]
     check_routing(res, inp)
-    assert_output_close(res["out64"], oracle.forward_inputs(inp)["out64"], f"{name} fused={fused}")
+    assert_output_close(res["out64"], oracle.forward_inputs(inp)["out64"], f"{name} mode={mode}")
+
+
+@pytest.mark.parametrize("name", ["decode_T16", "decode_T64_mixed8"])
+def test_row_gather_kernel_or_inside_the_gemm_bit_identical(name):
+    """The row gather as a kernel of its own or inside the gate_up GEMM
+    moves the same rows; the shrinks and GEMMs then compute the same
+    products in the same order, so the two outputs agree bit for bit."""
+    torch = torch_mod()
+    inp = cached_inputs(name)
+    a = run_gpu(inp, tuning={"shrink_in_gemm": 0})
+    b = run_gpu(inp, tuning={"shrink_in_gemm": 2})
+    assert a["status"] == 0 and b["status"] == 0
+    assert torch.equal(a["out"].view(torch.int16), b["out"].view(torch.int16))
 
 
 def test_forward_shrink_in_gemm_full_tiles():
