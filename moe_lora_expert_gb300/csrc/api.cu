@@ -793,7 +793,9 @@ int moe_lora_forward(const moe_lora_args_t* a, moe_stream_t stream) {
   // Launched right after the gate_up shrink or the row gather (n > 0 here),
   // which wait for the permute before they let this grid launch, or (gather
   // inside the GEMM) right after the permute, whose tables may still be in
-  // flight.
+  // flight.  W8A8 with the in-kernel shrink also waits first (fp8_gemm reads
+  // no tables_ready): weights streamed before its row quantizer completes
+  // slowed the in-kernel shrink that its first LoRA blocks wait for.
   gp.tables_ready = (fuse_shrink && !gather_kernel) ? 0 : 1;
   gp.w_scale = w8 ? a->w13_scale : nullptr;
   gp.scale_nb = (2 * I + 127) / 128;
